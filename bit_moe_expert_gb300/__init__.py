@@ -1,1 +1,252 @@
-"""GB300-native 4-bit groupwise-affine mixture-of-experts layer (sm_103a)."""
+"""GB300-native 4-bit groupwise-affine mixture-of-experts layer (sm_103a).
+
+Thin Python binding over the C ABI in include/moe.h.  The functions carry the C
+names and only marshal arguments (torch tensors -> device pointers, the current
+CUDA stream); every step of the layer runs in the CUDA library.  There is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libbitmoe.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NONFINITE"}
+
+# Every symbol include/moe.h declares.
+EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_scales",
+            "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_forward_workspace_bytes",
+            "moe_forward", "moe_check_status")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class _QMat(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("sb", C.c_void_p)]
+
+
+class _Experts(C.Structure):
+    _fields_ = [("gate", _QMat), ("up", _QMat), ("down", _QMat), ("n_experts", C.c_int)]
+
+
+class _Routing(C.Structure):
+    _fields_ = [("ids", C.c_void_p), ("w", C.c_void_p), ("counts", C.c_void_p), ("offsets", C.c_void_p),
+                ("perm", C.c_void_p), ("inv_perm", C.c_void_p), ("block_map", C.c_void_p),
+                ("num_blocks", C.c_void_p), ("block_rows", C.c_int)]
+
+
+_lib_handle = None
+
+
+def lib(path: Optional[str] = None):
+    """Loads the CUDA library (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
+        L = C.CDLL(p)
+        L.moe_status_string.restype = C.c_char_p
+        L.moe_status_string.argtypes = [C.c_int]
+        L.moe_device_sm_count.restype = C.c_int
+        L.moe_prepack_bytes.restype = C.c_size_t
+        L.moe_prepack_bytes.argtypes = [C.c_int, C.c_int, C.c_int]
+        L.moe_prepack_scales.restype = C.c_int
+        L.moe_prepack_scales.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.moe_route_max_blocks.restype = C.c_int
+        L.moe_route_max_blocks.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int]
+        L.moe_route_workspace_bytes.restype = C.c_size_t
+        L.moe_route_workspace_bytes.argtypes = [C.c_int, C.c_int, C.c_int]
+        L.moe_route.restype = C.c_int
+        L.moe_route.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
+                                C.c_void_p, C.c_size_t, C.c_void_p]
+        L.moe_forward_workspace_bytes.restype = C.c_size_t
+        L.moe_forward_workspace_bytes.argtypes = [C.c_int] * 6
+        L.moe_forward.restype = C.c_int
+        L.moe_forward.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Experts),
+                                  C.POINTER(_Experts), C.c_int, C.POINTER(_Routing), C.c_void_p, C.c_void_p,
+                                  C.c_size_t, C.c_void_p]
+        L.moe_check_status.restype = C.c_int
+        L.moe_check_status.argtypes = [C.c_void_p, C.c_void_p]
+        _lib_handle = L
+    return _lib_handle
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+# ----------------------------------------------------------------------- data holders
+
+@dataclasses.dataclass
+class QMat:
+    """One stacked packed matrix on the device: q int32 [E][N][K/8], sb int32 [E][K/64][N]."""
+    q: "object"
+    sb: "object"
+
+    def _c(self) -> _QMat:
+        return _QMat(_ptr(self.q), _ptr(self.sb))
+
+
+@dataclasses.dataclass
+class Experts:
+    gate: QMat
+    up: QMat
+    down: QMat
+
+    @property
+    def n_experts(self) -> int:
+        return int(self.gate.q.shape[0])
+
+    @property
+    def I(self) -> int:
+        return int(self.gate.q.shape[1])
+
+    def _c(self) -> _Experts:
+        return _Experts(self.gate._c(), self.up._c(), self.down._c(), self.n_experts)
+
+
+@dataclasses.dataclass
+class Routing:
+    """Device buffers written by moe_route."""
+    ids: "object"
+    w: "object"
+    counts: "object"
+    offsets: "object"
+    perm: "object"
+    inv_perm: "object"
+    block_map: "object"
+    num_blocks: "object"
+    block_rows: int
+
+    @staticmethod
+    def empty(T: int, E: int, k: int, block_rows: int, device="cuda") -> "Routing":
+        import torch
+        i32 = dict(dtype=torch.int32, device=device)
+        A = T * k
+        mb = max(1, moe_route_max_blocks(T, E, k, block_rows))
+        return Routing(ids=torch.empty((T, k), **i32), w=torch.empty((T, k), dtype=torch.float32, device=device),
+                       counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                       perm=torch.empty(max(A, 1), **i32), inv_perm=torch.empty(max(A, 1), **i32),
+                       block_map=torch.empty((mb, 3), **i32), num_blocks=torch.zeros(1, **i32),
+                       block_rows=block_rows)
+
+    def _c(self) -> _Routing:
+        return _Routing(_ptr(self.ids), _ptr(self.w), _ptr(self.counts), _ptr(self.offsets), _ptr(self.perm),
+                        _ptr(self.inv_perm), _ptr(self.block_map), _ptr(self.num_blocks), self.block_rows)
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A zero-filled, 256-byte aligned device workspace."""
+    import torch
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------- the C functions
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def moe_device_sm_count() -> int:
+    return int(lib().moe_device_sm_count())
+
+
+def moe_prepack_bytes(E: int, N: int, K: int) -> int:
+    return int(lib().moe_prepack_bytes(E, N, K))
+
+
+def moe_prepack_scales(scale, bias, sb, stream=None) -> None:
+    """scale, bias: int16/uint16-bit [E][N][K/64] device tensors; sb: int32 [E][K/64][N]."""
+    E, N, G = scale.shape
+    assert bias.shape == scale.shape and tuple(sb.shape) == (E, G, N)
+    _check("moe_prepack_scales",
+           lib().moe_prepack_scales(_ptr(scale), _ptr(bias), E, N, G * 64, _ptr(sb), _stream(stream)))
+
+
+def moe_route_max_blocks(T: int, E: int, k: int, block_rows: int) -> int:
+    return int(lib().moe_route_max_blocks(T, E, k, block_rows))
+
+
+def moe_route_workspace_bytes(T: int, E: int, k: int) -> int:
+    return int(lib().moe_route_workspace_bytes(T, E, k))
+
+
+def moe_route(logits, k: int, block_rows: int, out: Routing, ws, stream=None) -> None:
+    T, E = logits.shape
+    r = out._c()
+    _check("moe_route", lib().moe_route(_ptr(logits), T, E, k, block_rows, C.byref(r), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+    out.block_rows = r.block_rows
+
+
+def moe_forward_workspace_bytes(T: int, d: int, I: int, E: int, k: int, I_shared: int) -> int:
+    return int(lib().moe_forward_workspace_bytes(T, d, I, E, k, I_shared))
+
+
+def moe_forward(X, routed: Experts, shared: Optional[Experts], routing: Routing, Y, ws, stream=None) -> None:
+    T, d = X.shape
+    k = int(routing.ids.shape[1])
+    re = routed._c()
+    se = shared._c() if shared is not None else None
+    I_sh = shared.I if shared is not None else 0
+    rr = routing._c()
+    _check("moe_forward", lib().moe_forward(_ptr(X), T, d, routed.I, k, C.byref(re),
+                                            C.byref(se) if se is not None else None, I_sh, C.byref(rr), _ptr(Y),
+                                            _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_check_status(ws, stream=None) -> int:
+    return int(lib().moe_check_status(_ptr(ws), _stream(stream)))
+
+
+# ----------------------------------------------------------------------- weight preparation
+
+def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
+    """Device copy of one expert set in the kernels' format.
+
+    ex maps "gate", "up", "down" to (q, scale, bias): q uint32/int32 [E][N][K/8],
+    scale and bias uint16/int16 bf16 bits [E][N][K/64], as NumPy arrays or
+    torch tensors.  The group parameters are converted once with
+    moe_prepack_scales (a one-time layout change, like loading a checkpoint).
+    """
+    import numpy as np
+    import torch
+
+    def dev(a, np_view, torch_dtype):
+        if isinstance(a, np.ndarray):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np_view)).to(device)
+        return a.to(device=device).view(torch_dtype).contiguous()
+
+    mats = {}
+    for name in ("gate", "up", "down"):
+        q, s, b = ex[name]
+        qd = dev(q, np.int32, torch.int32)
+        sd = dev(s, np.int16, torch.int16)
+        bd = dev(b, np.int16, torch.int16)
+        E, N, G = sd.shape
+        sb = torch.empty((E, G, N), dtype=torch.int32, device=device)
+        moe_prepack_scales(sd, bd, sb, stream)
+        mats[name] = QMat(qd, sb)
+    return Experts(**mats)

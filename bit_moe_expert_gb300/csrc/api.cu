@@ -1,0 +1,335 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace layout, TMA tensor-map encoding and kernel launches.  Nothing here
+// allocates device memory or synchronises, except moe_check_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "moe.h"
+
+namespace bm {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// codes q [E][N][K/8] uint32
+bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_words,
+                  cuuint32_t box_rows, CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 8) * 4, static_cast<cuuint64_t>(K / 8) * 4 * N};
+  const cuuint32_t box[3] = {box_words, box_rows, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, sw);
+}
+
+// group parameters sb [E][K/64][N] uint32
+bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_rows,
+                   cuuint32_t box_groups) {
+  const int G = K / 64;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(N) * 4 * G};
+  const cuuint32_t box[3] = {box_rows, box_groups, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// bf16 activations [rows][cols], 128-byte swizzle, box (64, box_rows)
+bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols, cuuint32_t box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int g_sm_count[64] = {0};
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool env_flag(const char* name, bool dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return !(v[0] == '0' || v[0] == 'n' || v[0] == 'N' || v[0] == 'f' || v[0] == 'F');
+}
+
+enum class Path { kGemv, kGemm };
+
+// Forward workspace: header, then one region used by either path.
+struct FwdLayout {
+  size_t gemv_h_routed, gemv_h_shared;              // fp32
+  size_t gemm_h_routed, gemm_h_shared, gemm_ypart;  // bf16, bf16, fp32
+  size_t total;
+};
+
+FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
+  FwdLayout L;
+  const size_t A = static_cast<size_t>(T) * k;
+  size_t o = sizeof(WsHeader);
+  const size_t base = o;
+  L.gemv_h_routed = o;
+  o = round256(o + A * I * 4);
+  L.gemv_h_shared = o;
+  o = round256(o + static_cast<size_t>(T) * I_shared * 4);
+  const size_t gemv_end = o;
+  o = base;
+  L.gemm_h_routed = o;
+  o = round256(o + A * I * 2);
+  L.gemm_h_shared = o;
+  o = round256(o + static_cast<size_t>(T) * I_shared * 2);
+  L.gemm_ypart = o;
+  o = round256(o + static_cast<size_t>(T) * (k + 1) * d * 4);
+  L.total = o > gemv_end ? o : gemv_end;
+  return L;
+}
+
+bool qmat_ok(const moe_qmat& m) { return m.q && m.sb && aligned16(m.q) && aligned16(m.sb); }
+
+bool experts_ok(const moe_experts* ex) {
+  return ex && qmat_ok(ex->gate) && qmat_ok(ex->up) && qmat_ok(ex->down) && ex->n_experts >= 1;
+}
+
+}  // namespace
+
+size_t gemv_smem_gateup(int d);
+size_t gemv_smem_down(int I, int I_shared, int k);
+
+}  // namespace bm
+
+using namespace bm;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_NONFINITE: return "MOE_ERR_NONFINITE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+int moe_device_sm_count(void) { return sm_count(); }
+
+size_t moe_prepack_bytes(int E, int N, int K) {
+  if (E < 1 || N < 1 || K < 64 || K % 64) return 0;
+  return static_cast<size_t>(E) * (K / 64) * N * 4;
+}
+
+moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
+                              moe_stream stream) {
+  if (!scale || !bias || !sb || E < 1 || N < 1 || K < 64 || K % 64) return MOE_ERR_INVALID_ARG;
+  if (launch_prepack(scale, bias, E, N, K, sb, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_route_max_blocks(int T, int E, int k, int block_rows) {
+  if (T < 0 || E < 1 || k < 1 || block_rows < 1) return 0;
+  const long long A = static_cast<long long>(T) * k;
+  return static_cast<int>((A + block_rows - 1) / block_rows + E);
+}
+
+size_t moe_route_workspace_bytes(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  const size_t A = static_cast<size_t>(T) * k;
+  return round256(sizeof(WsHeader) + (route_hist_elems(T, E) + A) * 4);
+}
+
+moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, moe_routing* out, void* ws,
+                     size_t ws_bytes, moe_stream stream) {
+  if (!out || T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if ((T > 0 && !logits) || !out->ids || !out->w || !out->counts || !out->offsets || !out->perm ||
+      !out->inv_perm || !out->block_map || !out->num_blocks)
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < moe_route_workspace_bytes(T, E, k))
+    return MOE_ERR_WORKSPACE;
+  out->block_rows = block_rows;
+  RouteOut o{out->ids, out->w, out->counts, out->offsets, out->perm, out->inv_perm, out->block_map, out->num_blocks};
+  const bool pdl = env_flag("MOE_PDL", true);
+  if (launch_route(logits, T, E, k, block_rows, o, ws, reinterpret_cast<cudaStream_t>(stream), pdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shared) {
+  if (T < 0 || d < 1 || I < 1 || E < 1 || k < 1 || I_shared < 0) return 0;
+  return fwd_layout(T, d, I, k, I_shared).total;
+}
+
+moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
+                       const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y, void* ws,
+                       size_t ws_bytes, moe_stream stream) {
+  if (T < 0 || d < 64 || I < 64 || k < 1 || I_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (d % 64 || I % 64 || I_shared % 64) return MOE_ERR_INVALID_ARG;
+  if ((shared != nullptr) != (I_shared > 0)) return MOE_ERR_INVALID_ARG;
+  if (!experts_ok(routed) || (shared && (!experts_ok(shared) || shared->n_experts != 1)))
+    return MOE_ERR_INVALID_ARG;
+  const int E = routed->n_experts;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (!r || !r->ids || !r->w || !r->perm || !r->block_map || !r->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      ws_bytes < moe_forward_workspace_bytes(T, d, I, E, k, I_shared))
+    return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (!X || !Y || !aligned16(X) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (!get_encoder()) return MOE_ERR_CUDA;
+
+  const FwdLayout L = fwd_layout(T, d, I, k, I_shared);
+  char* wsb = static_cast<char*>(ws);
+  uint32_t* status = &static_cast<WsHeader*>(ws)->status;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool pdl = env_flag("MOE_PDL", true);
+
+  // Path: decode kernels for small T unless their shared-memory plan does not fit.
+  Path path = T <= kGemvMaxT ? Path::kGemv : Path::kGemm;
+  if (const char* p = std::getenv("MOE_PATH")) {
+    if (!std::strcmp(p, "gemv")) path = Path::kGemv;
+    if (!std::strcmp(p, "gemm")) path = Path::kGemm;
+  }
+  const size_t smem_limit = 227 * 1024;
+  const bool gemv_fits = gemv_smem_gateup(d) <= smem_limit && gemv_smem_down(I, I_shared, k) <= smem_limit;
+  if (path == Path::kGemv && !gemv_fits) path = Path::kGemm;
+
+  if (path == Path::kGemv) {
+    GemvMaps mr, ms;
+    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_codes(&mr.q_up, routed->up.q, E, I, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_codes(&mr.q_down, routed->down.q, E, d, I, 32, kGemvRowsDown, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemvRowsGU, d / 64) &&
+              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemvRowsGU, d / 64) &&
+              encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemvRowsDown, I / 64);
+    if (ok && shared)
+      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, 32, kGemvRowsDown,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemvRowsGU, d / 64) &&
+           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemvRowsGU, d / 64) &&
+           encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemvRowsDown, I_shared / 64);
+    if (!ok) return MOE_ERR_CUDA;
+    GemvArgs a{};
+    a.X = X;
+    a.ids = r->ids;
+    a.w = r->w;
+    a.Y = Y;
+    a.h_routed = reinterpret_cast<float*>(wsb + L.gemv_h_routed);
+    a.h_shared = reinterpret_cast<float*>(wsb + L.gemv_h_shared);
+    a.status = status;
+    a.T = T;
+    a.d = d;
+    a.I = I;
+    a.k = k;
+    a.I_shared = I_shared;
+    a.E = E;
+    if (launch_gemv(a, &mr, shared ? &ms : nullptr, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+
+  if (r->block_rows < 1 || r->block_rows > kGemmBN) return MOE_ERR_UNSUPPORTED;
+  const int A = T * k;
+  GemmMaps mr, ms;
+  GemmActMaps act;
+  uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
+  uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
+  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            encode_codes(&mr.q_up, routed->up.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            encode_codes(&mr.q_down, routed->down.q, E, d, I, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
+            encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
+            encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
+            encode_act(&act.x, X, T, d, 1) && encode_act(&act.h_routed, hr, A, I, 16);
+  if (ok && shared)
+    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+         encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
+         encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
+         encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&
+         encode_act(&act.h_shared, hs, T, I_shared, 16);
+  if (ok && !shared) act.h_shared = act.h_routed;  // never read without a shared expert
+  if (!ok) return MOE_ERR_CUDA;
+
+  GemmArgs a{};
+  a.perm = r->perm;
+  a.block_map = r->block_map;
+  a.num_blocks = r->num_blocks;
+  a.w = r->w;
+  a.ypart = reinterpret_cast<float*>(wsb + L.gemm_ypart);
+  a.h_routed = hr;
+  a.h_shared = hs;
+  a.Y = Y;
+  a.status = status;
+  a.T = T;
+  a.d = d;
+  a.I = I;
+  a.k = k;
+  a.I_shared = I_shared;
+  a.E = E;
+  a.num_sms = sm_count();
+  a.max_blocks = moe_route_max_blocks(T, E, k, r->block_rows);
+  if (a.num_sms <= 0) return MOE_ERR_CUDA;
+  if (launch_gemm(a, &mr, shared ? &ms : nullptr, &act, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_check_status(void* ws, moe_stream stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  WsHeader* h = static_cast<WsHeader*>(ws);
+  if (cudaMemcpyAsync(&v, &h->status, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemsetAsync(&h->status, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status>(v);
+}
+
+}  // extern "C"

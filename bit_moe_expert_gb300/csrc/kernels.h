@@ -1,0 +1,88 @@
+// Launch entry points of the kernels, called by the host boundary (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "status.h"
+
+namespace bm {
+
+struct RouteOut {
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* block_map;
+  int32_t* num_blocks;
+};
+
+size_t route_hist_elems(int T, int E);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out, void* ws,
+                         cudaStream_t stream, bool pdl);
+cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
+                           cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode GEMV
+// Rows per CTA of the gate/up kernel and of the down kernel.
+constexpr int kGemvRowsGU = 32;
+constexpr int kGemvRowsDown = 16;
+
+// Tensor maps of one expert set for the GEMV kernels.
+struct GemvMaps {
+  CUtensorMap q_gate, q_up, q_down;     // codes, box (32 words, rows, 1), 128-byte swizzle
+  CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (rows, K/64, 1)
+};
+
+struct GemvArgs {
+  const uint16_t* X;   // [T][d] bf16
+  const int32_t* ids;  // [T][k]
+  const float* w;      // [T][k]
+  uint16_t* Y;         // [T][d] bf16
+  float* h_routed;     // [T*k][I] fp32
+  float* h_shared;     // [T][I_shared] fp32
+  uint32_t* status;
+  int T, d, I, k, I_shared, E;
+};
+
+cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMaps* shared, cudaStream_t stream,
+                        bool pdl);
+
+// ---------------------------------------------------------------- prefill GEMM
+constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)
+constexpr int kGemmBK = 64;    // K per stage = one quantisation group
+constexpr int kGemmBN = 128;   // max tokens per tile (MMA N)
+
+struct GemmMaps {
+  CUtensorMap q_gate, q_up, q_down;     // codes, box (8 words, 128 rows, 1), 32-byte swizzle
+  CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (128 rows, 1, 1)
+};
+
+struct GemmArgs {
+  const int32_t* perm;        // [A]
+  const int32_t* block_map;   // [nb][3]
+  const int32_t* num_blocks;  // [1]
+  const float* w;             // [A]
+  float* ypart;               // [T][k+1][d] fp32 weighted expert outputs
+  uint16_t* h_routed;         // [A][I] bf16
+  uint16_t* h_shared;         // [T][I_shared] bf16
+  uint16_t* Y;                // [T][d] bf16
+  uint32_t* status;
+  int T, d, I, k, I_shared, E, num_sms, max_blocks;
+};
+
+struct GemmActMaps {
+  CUtensorMap x;         // X [T][d] bf16, box (64, 1), 128-byte swizzle (gather4)
+  CUtensorMap h_routed;  // H [A][I] bf16, box (64, 16), 128-byte swizzle
+  CUtensorMap h_shared;  // H [T][I_shared] bf16, box (64, 16), 128-byte swizzle
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared,
+                        const GemmActMaps* act, cudaStream_t stream, bool pdl);
+
+}  // namespace bm

@@ -1,0 +1,289 @@
+// GPU-resident routing in one launch: top-k, histogram, exclusive scan, stable
+// scatter and tile block map, with no host round trip ("Perplexity's Lily
+// Beats MLX-LM on MacBook M5", section "Prefill: keep routing on the GPU,
+// dequantize in flight": histogram, prefix scan, scatter and block map after
+// every top-8 selection, kept inside one GPU submission).
+//
+// Each CTA routes a chunk of 32 tokens (one warp per token at a time): k rounds
+// of a warp-wide arg-max over the lane-strided logits.  It then writes its
+// per-expert counts and, for every assignment, the rank among the chunk's
+// assignments to the same expert (computed in assignment order, so the result
+// is stable).  The last CTA to finish (an atomic ticket, no spin wait) reduces
+// the chunk counts into counts/offsets, turns them into per-chunk bases, places
+// every assignment, and writes the block map.
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bm {
+
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+struct BestKV {
+  float v;
+  int i;  // -1 = none
+};
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  if (bi < 0) return i >= 0;
+  if (i < 0) return false;
+  return v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                              int k, int block_rows, RouteOut out,
+                                                              WsHeader* hdr, int32_t* __restrict__ chunk_hist,
+                                                              int32_t* __restrict__ local_rank) {
+  __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
+  __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int s_is_last;
+
+  pdl_wait();  // the previous kernel on the stream may still own our outputs
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kRouteTokensPerCta;
+  const int ntok = max(0, min(kRouteTokensPerCta, T - t0));
+  const int per_lane = (E + 31) >> 5;
+
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
+
+  // ---- top-k, one warp per token
+  for (int tl = warp; tl < ntok; tl += kRouteWarps) {
+    const int t = t0 + tl;
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[kMaxE / 32];
+    uint32_t taken = 0;
+    bool finite = true;
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) {
+      const int e = lane + 32 * c;
+      v[c] = (c < per_lane && e < E) ? __ldg(row + e) : 0.0f;
+      if (c < per_lane && e < E) finite &= isfinite(v[c]);
+      if (!(c < per_lane && e < E)) taken |= 1u << c;
+    }
+    if (!__all_sync(0xffffffffu, finite)) record_status(&hdr->status, MOE_ERR_NONFINITE);
+
+    float sel_v = 0.0f;  // lane j keeps the j-th selected logit
+    int sel_i = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = 0.0f;
+      int bi = -1;
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c) {
+        if (c < per_lane && !((taken >> c) & 1u)) {
+          const int e = lane + 32 * c;
+          if (better(v[c], e, bv, bi)) {
+            bv = v[c];
+            bi = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      // bi is now identical in every lane
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        sel_v = bv;
+        sel_i = bi;
+      }
+    }
+    // weights: exp(l_j - l_max) in fp64, summed in selection order, one rounding to fp32
+    const float top = __shfl_sync(0xffffffffu, sel_v, 0);
+    const double ex = (lane < k) ? exp(static_cast<double>(sel_v) - static_cast<double>(top)) : 0.0;
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+      out.ids[static_cast<size_t>(t) * k + lane] = sel_i;
+      out.w[static_cast<size_t>(t) * k + lane] = static_cast<float>(ex / sum);
+      s_ids[tl * k + lane] = sel_i;
+    }
+  }
+  __syncthreads();
+
+  // ---- stable per-chunk ranks: one warp walks the chunk's assignments in order
+  const int na = ntok * k;
+  if (warp == 0) {
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int base = 0; base < na; base += 32) {
+      const int a = base + lane;
+      const bool valid = a < na;
+      const int e = valid ? s_ids[a] : -1 - lane;  // distinct dummy keys for idle lanes
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int before = __popc(peers & lt_mask);
+      int cnt_before = 0;
+      if (valid) cnt_before = s_cnt[e];
+      __syncwarp();
+      if (valid) {
+        local_rank[static_cast<size_t>(t0) * k + a] = cnt_before + before;
+        if (before == 0) s_cnt[e] = cnt_before + __popc(peers);  // group leader publishes
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) chunk_hist[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
+
+  // ---- last CTA to arrive finishes the layout
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned ticket = atomicAdd(&hdr->ticket, 1u);
+    s_is_last = (ticket == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_is_last) return;
+  __threadfence();
+
+  const int nchunks = gridDim.x;
+  const int A = T * k;
+  // counts[e] and the per-chunk exclusive bases (in place over chunk_hist)
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const size_t idx = static_cast<size_t>(c) * E + e;
+      const int h = __ldcg(chunk_hist + idx);
+      chunk_hist[idx] = run;
+      run += h;
+    }
+    s_cnt[e] = run;
+    out.counts[e] = run;
+  }
+  __syncthreads();
+
+  // exclusive scans over experts: offsets (rows) and block offsets (tiles);
+  // E <= 1024 values, one thread walks a contiguous slice, then a warp scan
+  __shared__ int32_t s_off[kMaxE + 1];
+  __shared__ int32_t s_boff[kMaxE + 1];
+  __shared__ int32_t s_part[2][kRouteThreads];
+  {
+    const int per = (E + kRouteThreads - 1) / kRouteThreads;
+    const int lo = threadIdx.x * per;
+    const int hi = min(E, lo + per);
+    int rs = 0, bs = 0;
+    for (int e = lo; e < hi; ++e) {
+      rs += s_cnt[e];
+      bs += (s_cnt[e] + block_rows - 1) / block_rows;
+    }
+    s_part[0][threadIdx.x] = rs;
+    s_part[1][threadIdx.x] = bs;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int r = 0, b = 0;
+      for (int i = 0; i < kRouteThreads; ++i) {
+        const int tr = s_part[0][i], tb = s_part[1][i];
+        s_part[0][i] = r;
+        s_part[1][i] = b;
+        r += tr;
+        b += tb;
+      }
+      s_off[E] = r;
+      s_boff[E] = b;
+    }
+    __syncthreads();
+    rs = s_part[0][threadIdx.x];
+    bs = s_part[1][threadIdx.x];
+    for (int e = lo; e < hi; ++e) {
+      s_off[e] = rs;
+      s_boff[e] = bs;
+      rs += s_cnt[e];
+      bs += (s_cnt[e] + block_rows - 1) / block_rows;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kRouteThreads) out.offsets[e] = s_off[e];
+  if (threadIdx.x == 0) *out.num_blocks = s_boff[E];
+
+  // block map
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+    const int cnt = s_cnt[e];
+    int b = s_boff[e];
+    for (int r = 0; r < cnt; r += block_rows, ++b) {
+      out.block_map[3 * b + 0] = e;
+      out.block_map[3 * b + 1] = s_off[e] + r;
+      out.block_map[3 * b + 2] = min(block_rows, cnt - r);
+    }
+  }
+
+  // scatter: position = offsets[e] + base of the chunk for e + rank within the chunk
+  for (int a = threadIdx.x; a < A; a += kRouteThreads) {
+    const int e = __ldcg(out.ids + a);
+    const int c = (a / k) / kRouteTokensPerCta;
+    const int pos = s_off[e] + __ldcg(chunk_hist + static_cast<size_t>(c) * E + e) + __ldcg(local_rank + a);
+    out.perm[pos] = a;
+    out.inv_perm[a] = pos;
+  }
+  if (threadIdx.x == 0) hdr->ticket = 0;  // ready for the next call
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out,
+                         void* ws, cudaStream_t stream, bool pdl) {
+  WsHeader* hdr = static_cast<WsHeader*>(ws);
+  const int nchunks = T > 0 ? (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta : 1;
+  int32_t* chunk_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
+  int32_t* local_rank = chunk_hist + route_hist_elems(T, E);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nchunks);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_kernel, logits, T, E, k, block_rows, out, hdr, chunk_hist, local_rank);
+}
+
+size_t route_hist_elems(int T, int E) {
+  const int nchunks = T > 0 ? (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta : 1;
+  const size_t n = static_cast<size_t>(nchunks) * E;
+  return (n + 63) & ~static_cast<size_t>(63);
+}
+
+// ------------------------------------------------------------------ prepack
+namespace {
+__global__ void prepack_kernel(const uint16_t* __restrict__ scale, const uint16_t* __restrict__ bias, int E,
+                               int N, int G, uint32_t* __restrict__ sb) {
+  // output index o = ((e*G + g)*N + n); input index i = ((e*N + n)*G + g)
+  const size_t total = static_cast<size_t>(E) * G * N;
+  for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
+       o += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(o % N);
+    const size_t eg = o / N;
+    const int g = static_cast<int>(eg % G);
+    const int e = static_cast<int>(eg / G);
+    const size_t i = (static_cast<size_t>(e) * N + n) * G + g;
+    sb[o] = static_cast<uint32_t>(scale[i]) | (static_cast<uint32_t>(bias[i]) << 16);
+  }
+}
+}  // namespace
+
+cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
+                           cudaStream_t stream) {
+  const int G = K / 64;
+  const size_t total = static_cast<size_t>(E) * G * N;
+  const int threads = 256;
+  const size_t blocks = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
+  prepack_kernel<<<grid, threads, 0, stream>>>(scale, bias, E, N, G, sb);
+  return cudaGetLastError();
+}
+
+}  // namespace bm

@@ -1,0 +1,181 @@
+/*
+ * bit_moe_expert_gb300 -- C ABI of a GB300 (sm_103a) mixture-of-experts layer
+ * whose expert weights are 4-bit groupwise-affine quantised.
+ *
+ * The operation (sources: the web pages "Perplexity's Lily Beats MLX-LM on
+ * MacBook M5. Because It Only Runs One Model." -- sections "Why
+ * Qwen3.6-35B-A3B is a weird workload", "Prefill: keep routing on the GPU,
+ * dequantize in flight" and "Decode: minimize bytes per token" -- and
+ * "Perplexity builds a custom engine for Qwen on M5 Macs"):
+ *
+ *   routing   for each token t, the k experts with the largest router logits
+ *             (ties to the lower expert index) and weights w = softmax over
+ *             the experts renormalised over the selected k;
+ *   layout    a histogram of assignments per expert, its exclusive prefix
+ *             scan, a stable scatter that groups each expert's rows together
+ *             and a tile block map, all on the GPU with no host round trip;
+ *   experts   Y[t] = sum_j w[t][j] * FFN_{e(t,j)}(x_t) + FFN_shared(x_t), with
+ *             FFN(x) = (silu(x Wg^T) * (x Wu^T)) Wd^T and every weight
+ *             w = q * scale + bias, q a 4-bit code, one bf16 scale and one
+ *             bf16 bias per group of 64 consecutive weights along K.
+ *
+ * Conventions for every entry point
+ *   - All array pointers are DEVICE pointers, owned by the caller, and must be
+ *     16-byte aligned.  The library never allocates, frees or synchronises on
+ *     these paths (moe_check_status is the one synchronising call).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL means the legacy
+ *     default stream) and may be captured into a CUDA graph.
+ *   - Argument checks happen on the host before anything is launched; a failed
+ *     check returns a status and launches nothing.  Errors that only the device
+ *     can see (a non-finite logit, a bounded wait that expired) are recorded in
+ *     a status word at the start of the workspace and read by moe_check_status.
+ *   - Integers in device arrays are int32 (no int64 anywhere).
+ *   - bf16 values travel as uint16_t bit patterns.
+ */
+#ifndef BIT_MOE_EXPERT_GB300_MOE_H
+#define BIT_MOE_EXPERT_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Identical to cudaStream_t. */
+typedef struct CUstream_st* moe_stream;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a size, pointer or alignment precondition failed */
+  MOE_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels implement */
+  MOE_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or smaller than queried */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired (device status word) */
+  MOE_ERR_NONFINITE = 6    /* a router logit was NaN or infinite (device status word) */
+} moe_status;
+
+/* Human-readable name of a status.  Never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* ------------------------------------------------------------------ weights
+ * One stacked packed matrix of E experts with N rows and K columns (K a
+ * multiple of 64):
+ *   q   uint32 [E][N][K/8]   the code of column k sits in bits 4*(k%8) of word
+ *                            k/8 of its row (low nibble = lowest k);
+ *   sb  uint32 [E][K/64][N]  the group parameters, transposed so one group of
+ *                            many rows is contiguous: bits 0..15 hold the bf16
+ *                            scale and bits 16..31 the bf16 bias of rows n,
+ *                            columns 64g .. 64g+63.  Build it once per weight
+ *                            set with moe_prepack_scales.
+ * Gate and up projections have N = I, K = d; the down projection has N = d,
+ * K = I.
+ */
+typedef struct {
+  const uint32_t* q;
+  const uint32_t* sb;
+} moe_qmat;
+
+typedef struct {
+  moe_qmat gate;
+  moe_qmat up;
+  moe_qmat down;
+  int n_experts;
+} moe_experts;
+
+/* Bytes of the sb array for E experts of an N x K matrix: E * (K/64) * N * 4. */
+size_t moe_prepack_bytes(int E, int N, int K);
+
+/* Transpose and interleave per-group bf16 scale and bias, both laid out
+ * [E][N][K/64] as in the checkpoint, into sb [E][K/64][N] (see above).  A pure
+ * data movement; bit-exact.  Sizes: E >= 1, N >= 1, K a positive multiple of
+ * 64.  Returns MOE_ERR_INVALID_ARG on a bad size or pointer. */
+moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E, int N, int K,
+                              uint32_t* sb, moe_stream stream);
+
+/* ------------------------------------------------------------------ routing
+ * Output arrays of moe_route, all caller-owned device memory:
+ *   ids        int32 [T][k]  selected experts, descending logit, lower index
+ *                            first among equal logits
+ *   w          float [T][k]  renormalised routing weights: exp(l - l_max) summed
+ *                            over the selection in fp64, rounded once to fp32
+ *   counts     int32 [E]     assignments per expert (sum = T*k)
+ *   offsets    int32 [E+1]   exclusive prefix sum of counts; offsets[E] = T*k
+ *   perm       int32 [T*k]   permuted row p holds assignment a = t*k + j;
+ *                            rows of one expert are contiguous
+ *                            ([offsets[e], offsets[e+1])) and in ascending a
+ *   inv_perm   int32 [T*k]   inv_perm[perm[p]] = p
+ *   block_map  int32 [moe_route_max_blocks(...)][3]  one entry per tile:
+ *                            (expert, first permuted row, rows <= block_rows),
+ *                            experts ascending, tiles of an expert in order
+ *   num_blocks int32 [1]     number of valid block_map entries
+ * block_rows records the tile height moe_route was called with; moe_forward
+ * reads it.
+ */
+typedef struct {
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* block_map;
+  int32_t* num_blocks;
+  int block_rows;
+} moe_routing;
+
+/* Upper bound on num_blocks: ceil(T*k / block_rows) + E. */
+int moe_route_max_blocks(int T, int E, int k, int block_rows);
+
+/* Workspace bytes moe_route needs.  A workspace is caller-owned device memory,
+ * 256-byte aligned, zero-filled ONCE before its first use; every call leaves it
+ * ready for the next.  Calls sharing a workspace must be stream-ordered. */
+size_t moe_route_workspace_bytes(int T, int E, int k);
+
+/* fp32 router logits [T][E] (row-major) -> all arrays of *out.  One kernel
+ * launch, no host synchronisation.  Preconditions: T >= 0 (T = 0 writes zero
+ * counts, offsets and num_blocks), 1 <= E <= 1024, 1 <= k <= min(E, 32),
+ * 1 <= block_rows <= 128.  Logits must be finite: a NaN or infinity leaves a
+ * deterministic but meaningless selection and records MOE_ERR_NONFINITE in
+ * the workspace status word.  Sets out->block_rows. */
+moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
+                     void* ws, size_t ws_bytes, moe_stream stream);
+
+/* ------------------------------------------------------------------ experts
+ * Workspace bytes moe_forward needs for these sizes (I_shared = 0: no shared
+ * expert).  Same rules as the routing workspace: zero-filled once before first
+ * use, 256-byte aligned, one in-flight call per workspace. */
+size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shared);
+
+/* bf16 X [T][d] (row-major) -> bf16 Y [T][d].
+ *   routed   E = routed->n_experts experts, I columns of intermediate
+ *   shared   NULL, or one always-on expert (n_experts = 1) with I_shared
+ *   r        the routing written by moe_route for the same T, E, k on this
+ *            stream (block_rows <= 128)
+ * Preconditions: T >= 0 (T = 0 does nothing), d, I and I_shared multiples of
+ * 64 (I_shared = 0 iff shared is NULL), 1 <= k <= min(E, 32), E <= 1024.
+ * Path: T <= 4 runs the decode kernels (CUDA-core GEMV, every active expert's
+ * bytes streamed once); larger T runs the grouped tensor-core GEMM (tcgen05,
+ * dequantisation fused, SwiGLU and the weighted combine fused).  The
+ * environment variable MOE_PATH=gemv|gemm overrides the choice (for A/B
+ * measurements and tests).  Arithmetic: fp32 accumulation; on the GEMM path the
+ * dequantised weights and the SwiGLU output are rounded to bf16 as tensor-core
+ * operands; Y is rounded to bf16 once. */
+moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
+                       const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y,
+                       void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Synchronises `stream`, returns the status recorded in the workspace of a
+ * previous moe_route or moe_forward call (MOE_OK if none) and clears it.  For
+ * tests and debugging; never needed on the hot path. */
+moe_status moe_check_status(void* ws, moe_stream stream);
+
+/* Number of streaming multiprocessors the library sizes its persistent grids
+ * for on the current device (0 if no device).  Informational. */
+int moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
