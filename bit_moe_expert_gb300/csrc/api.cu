@@ -59,12 +59,12 @@ bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cu
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// bf16 activations [rows][cols], 128-byte swizzle, box (64, box_rows)
+// fp16 activations [rows][cols], 128-byte swizzle, box (64, box_rows)
 bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols, cuuint32_t box_rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   const cuuint32_t box[2] = {64, box_rows};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -95,7 +95,7 @@ enum class Path { kGemv, kGemm };
 // Forward workspace: header, then one region used by either path.
 struct FwdLayout {
   size_t gemv_h_routed, gemv_h_shared;              // fp32
-  size_t gemm_h_routed, gemm_h_shared, gemm_ypart;  // bf16, bf16, fp32
+  size_t gemm_h_routed, gemm_h_shared, gemm_ypart, gemm_xh;  // fp16, fp16, fp32, fp16
   size_t total;
 };
 
@@ -116,6 +116,8 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
   o = round256(o + static_cast<size_t>(T) * I_shared * 2);
   L.gemm_ypart = o;
   o = round256(o + static_cast<size_t>(T) * (k + 1) * d * 4);
+  L.gemm_xh = o;
+  o = round256(o + static_cast<size_t>(T) * d * 2);
   L.total = o > gemv_end ? o : gemv_end;
   return L;
 }
@@ -183,9 +185,9 @@ moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, m
   if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
   if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(T) * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
-  if ((T > 0 && !logits) || !out->ids || !out->w || !out->counts || !out->offsets || !out->perm ||
-      !out->inv_perm || !out->block_map || !out->num_blocks)
-    return MOE_ERR_INVALID_ARG;
+  // arrays of length T*k may be null when T = 0
+  if (!out->counts || !out->offsets || !out->block_map || !out->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !out->ids || !out->w || !out->perm || !out->inv_perm)) return MOE_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < moe_route_workspace_bytes(T, E, k))
     return MOE_ERR_WORKSPACE;
   out->block_rows = block_rows;
@@ -211,11 +213,12 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     return MOE_ERR_INVALID_ARG;
   const int E = routed->n_experts;
   if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
-  if (!r || !r->ids || !r->w || !r->perm || !r->block_map || !r->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (!r) return MOE_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
       ws_bytes < moe_forward_workspace_bytes(T, d, I, E, k, I_shared))
     return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
+  if (!r->ids || !r->w || !r->perm || !r->block_map || !r->num_blocks) return MOE_ERR_INVALID_ARG;
   if (!X || !Y || !aligned16(X) || !aligned16(Y)) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
   if (!get_encoder()) return MOE_ERR_CUDA;
@@ -277,13 +280,14 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   GemmActMaps act;
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
   bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
             encode_codes(&mr.q_up, routed->up.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
             encode_codes(&mr.q_down, routed->down.q, E, d, I, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
-            encode_act(&act.x, X, T, d, 1) && encode_act(&act.h_routed, hr, A, I, 16);
+            encode_act(&act.x, xh, T, d, 1) && encode_act(&act.h_routed, hr, A, I, 16);
   if (ok && shared)
     ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
          encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
@@ -303,6 +307,8 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   a.ypart = reinterpret_cast<float*>(wsb + L.gemm_ypart);
   a.h_routed = hr;
   a.h_shared = hs;
+  a.X = X;
+  a.Xh = xh;
   a.Y = Y;
   a.status = status;
   a.T = T;

@@ -6,17 +6,21 @@
 // weights; the expert input projections are fused with the gate activation and
 // the output projection with the routing scores and the shared expert).
 //
+// Operands are fp16 (the pages' Metal kernels use bf16): fp16 holds the
+// dequantised weights of this format exactly and rounds h and X 8x more finely,
+// at the same tensor-core rate; X is converted once per call.
+//
 // sm_103a design ("swap AB"): the weights are the M = 128 operand and an
 // expert's tokens the N operand (16..128, a multiple of 16), so an expert with
 // few tokens still streams its weight tile exactly once.  The dequantised
 // weight tile never touches shared memory: dequantisation warps turn the TMA-
-// loaded codes into bf16 and store them with tcgen05.st straight into tensor
+// loaded codes into fp16 and store them with tcgen05.st straight into tensor
 // memory, where tcgen05.mma reads them as its A operand; shared memory carries
 // only the packed codes, the group parameters and the token tile (TMA gather4
 // of the expert's token rows).  Accumulators live in tensor memory.
 //
 // Roles (14 warps, one persistent CTA per SM):
-//   warps 0-7   dequantise codes -> bf16 A tiles in TMEM
+//   warps 0-7   dequantise codes -> fp16 A tiles in TMEM
 //   warps 8-11  epilogue: TMEM -> registers -> SwiGLU (gate/up) or weighted
 //               scatter of expert outputs (down)
 //   warp 12     TMA producer (codes, group parameters, token rows)
@@ -24,6 +28,7 @@
 // Synchronisation is by mbarriers; every wait is bounded (2 s) and records
 // MOE_ERR_TIMEOUT instead of hanging.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -43,12 +48,12 @@ struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
   static constexpr int kStages = kGateUp ? 6 : 8;
   static constexpr int kAStages = kGateUp ? 4 : 8;
-  static constexpr int kACols = 32 * kMats;  // 64 bf16 per lane per matrix = 32 columns
+  static constexpr int kACols = 32 * kMats;  // 64 fp16 per lane per matrix = 32 columns
   static constexpr int kAccCols = kMats * kGemmBN;
   static constexpr int kAccBufs = kGateUp ? 1 : 2;
   static constexpr int kABase = kAccBufs * kAccCols;
   static_assert(kABase + kAStages * kACols <= static_cast<int>(kTmemCols), "TMEM budget");
-  static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to 128 rows x 64 bf16 (128-byte swizzle)
+  static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to 128 rows x 64 fp16 (128-byte swizzle)
   static constexpr int kQBytes = kGemmBM * 32;   // 128 rows x 8 code words (32-byte swizzle)
   static constexpr int kSBBytes = kGemmBM * 4;
   static constexpr int kStageBytes = ((kBBytes + kMats * (kQBytes + kSBBytes)) + 1023) / 1024 * 1024;
@@ -93,17 +98,23 @@ __device__ __forceinline__ Item get_item(const GemmArgs& a, const Sched& s, int 
 
 __device__ __forceinline__ int tile_n(int rows) { return max(16, (rows + 15) & ~15); }
 
-// Eight 4-bit codes (one word, k ascending from the low nibble) -> four bf16x2
+// Eight 4-bit codes (one word, k ascending from the low nibble) -> four f16x2
 // values of q*scale + bias, adjacent columns paired (low half = lower k).
+// fp16 carries 11 significant bits, so q*scale + bias is exact whenever it fits
+// them (always when bias = -8*scale: |q-8| <= 8 adds at most 3 bits to the
+// 8-bit bf16 scale); otherwise it is rounded once.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* out) {
   const uint32_t w4 = w >> 4;
-  const uint32_t magic = 0x43004300u;  // bf16 pair (128, 128): a code in the low mantissa bits reads 128 + q
+  const uint32_t magic = 0x64006400u;      // f16 pair (1024, 1024): a code in the low mantissa bits reads 1024 + q
+  const uint32_t one = 0x3C003C00u;        // f16 pair (1, 1)
+  const uint32_t minus_magic = 0xE400E400u;  // f16 pair (-1024, -1024)
   const uint32_t sel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const uint32_t t = prmt(w, w4, sel[m]);               // low nibbles: byte 0 = q_2m, byte 2 = q_2m+1
-    const uint32_t v = lop3_and_or(t, 0x000F000Fu, magic);  // (128 + q_2m, 128 + q_2m+1)
-    out[m] = bf16x2_fma(bf16x2_sub(v, magic), s2, b2);    // q*scale + bias, one rounding
+    const uint32_t t = prmt(w, w4, sel[m]);                 // low nibbles: byte 0 = q_2m, byte 2 = q_2m+1
+    const uint32_t v = lop3_and_or(t, 0x000F000Fu, magic);  // (1024 + q_2m, 1024 + q_2m+1)
+    const uint32_t q = f16x2_fma(v, one, minus_magic);      // (q_2m, q_2m+1), exact
+    out[m] = f16x2_fma(q, s2, b2);                          // q*scale + bias, one rounding
   }
 }
 
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
       const int bn = tile_n(m.rows);
-      const uint32_t idesc = idesc_bf16_f32(kGemmBM, bn);
+      const uint32_t idesc = idesc_f16_f32(kGemmBM, bn);
       const int ab = kGateUp ? 0 : accb;
       if (!mbar_wait(&acc_empty[ab], accphase ^ 1, abort_flag)) {
         fail();
@@ -343,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes;
         const uint32_t sbv =
             *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes + mat * C::kSBBytes + row * 4);
-        const uint32_t s2 = prmt(sbv, 0u, 0x1010u);
-        const uint32_t b2 = prmt(sbv, 0u, 0x3232u);
+        const float sf = __uint_as_float(sbv << 16);          // bf16 -> fp32 is exact
+        const float bf = __uint_as_float(sbv & 0xFFFF0000u);
+        const uint32_t s2 = f32x2_to_f16x2(sf, sf);
+        const uint32_t b2 = f32x2_to_f16x2(bf, bf);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols;
         if constexpr (kGateUp) {
           const uint4 wa = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((0 ^ swz) * 16));
@@ -422,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float gv = __uint_as_float(g[c]);
                 const float uv = __uint_as_float(u[c]);
                 const float h = gv / (1.0f + expf(-gv)) * uv;
-                H[static_cast<size_t>(m.row0 + c0 + c) * Icur + n] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+                if (!(fabsf(h) <= 65504.0f)) record_status(a.status, MOE_ERR_UNSUPPORTED);
+                H[static_cast<size_t>(m.row0 + c0 + c) * Icur + n] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }
@@ -473,6 +487,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// X (bf16) -> fp16 copy used as the tensor-core operand.  Values outside the
+// fp16 range are recorded as MOE_ERR_UNSUPPORTED.
+__global__ void x_to_f16_kernel(const uint16_t* __restrict__ X, size_t n8, uint16_t* __restrict__ Xh,
+                                uint32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  bool range_ok = true;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(X)[i];
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(in[j] << 16);
+      const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
+      range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
+      out[j] = f32x2_to_f16x2(lo, hi);
+    }
+    reinterpret_cast<uint4*>(Xh)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  if (!range_ok) record_status(status, MOE_ERR_UNSUPPORTED);
 }
 
 // Y[t] = bf16( sum over the k routed slots and the shared slot )
@@ -530,6 +568,16 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.gridDim = dim3(a.num_sms);
   cfg.blockDim = dim3(kThreads);
 
+  {
+    cudaLaunchConfig_t c2 = cfg;
+    c2.gridDim = dim3(a.num_sms * 2);
+    c2.blockDim = dim3(256);
+    c2.dynamicSmemBytes = 0;
+    const size_t n8 = static_cast<size_t>(a.T) * a.d / 8;
+    cudaError_t e = cudaLaunchKernelEx(&c2, x_to_f16_kernel, a.X, n8, a.Xh, a.status);
+    if (e != cudaSuccess) return e;
+  }
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CG::kSmemBytes;
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
                                        routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);

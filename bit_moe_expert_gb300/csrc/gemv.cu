@@ -111,7 +111,7 @@ __host__ __device__ inline GUSmem gu_layout(int K) {
   size_t o = 0;
   L.q_off = o;
   o += 2ull * L.nbox * kGemvRowsGU * 128;  // gate then up
-  L.sb_off = o;
+  L.sb_off = o;  // 1024-aligned; the up matrix's block starts KB*128 bytes later (128-aligned)
   o += 2ull * L.KB * kGemvRowsGU * 4;
   L.x_off = o;
   o += static_cast<size_t>(K) * 4;
@@ -225,9 +225,14 @@ __global__ void __launch_bounds__(kGUThreads, 1)
 
 struct DownSmem {
   int nbox_r, nbox_s, KB_r, KB_s, nexp, Imax;
+  size_t sb_slot_r;  // bytes per routed expert's group parameters, rounded to 128 (TMA destination)
   size_t q_off, q_s_off, sb_off, sb_s_off, h_off, sx_off, w_off, red_off, bar_off, total;
 };
 
+__host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Every TMA destination starts on a 1024-byte boundary (128-byte swizzled code
+// boxes) or a 128-byte boundary (group parameters).
 __host__ __device__ inline DownSmem down_layout(int I, int I_shared, int k) {
   DownSmem L;
   L.KB_r = I / 64;
@@ -236,6 +241,7 @@ __host__ __device__ inline DownSmem down_layout(int I, int I_shared, int k) {
   L.nbox_s = I_shared > 0 ? div_up(I_shared / 8, kBoxWords) : 0;
   L.nexp = k + (I_shared > 0 ? 1 : 0);
   L.Imax = I > I_shared ? I : I_shared;
+  L.sb_slot_r = round_up(static_cast<size_t>(L.KB_r) * kGemvRowsDown * 4, 128);
   const size_t box = kGemvRowsDown * 128;
   size_t o = 0;
   L.q_off = o;
@@ -243,16 +249,16 @@ __host__ __device__ inline DownSmem down_layout(int I, int I_shared, int k) {
   L.q_s_off = o;
   o += static_cast<size_t>(L.nbox_s) * box;
   L.sb_off = o;
-  o += static_cast<size_t>(k) * L.KB_r * kGemvRowsDown * 4;
+  o += static_cast<size_t>(k) * L.sb_slot_r;
   L.sb_s_off = o;
-  o += static_cast<size_t>(L.KB_s) * kGemvRowsDown * 4;
+  o += round_up(static_cast<size_t>(L.KB_s) * kGemvRowsDown * 4, 128);
   L.h_off = o;
   o += static_cast<size_t>(L.nexp) * L.Imax * 4;
   L.sx_off = o;
   o += static_cast<size_t>(L.nexp) * (L.Imax / 64) * 4;
   L.w_off = o;
   o += static_cast<size_t>(L.nexp) * 4;
-  o = (o + 15) & ~static_cast<size_t>(15);
+  o = round_up(o, 16);
   L.red_off = o;
   o += static_cast<size_t>(kDownSlices) * kGemvRowsDown * 4;
   L.bar_off = o;
@@ -276,7 +282,6 @@ __global__ void __launch_bounds__(kDownThreads, 1)
 
   uint8_t* q_r = smem + L.q_off;
   uint8_t* q_s = smem + L.q_s_off;
-  uint32_t* sb_r = reinterpret_cast<uint32_t*>(smem + L.sb_off);
   uint32_t* sb_s = reinterpret_cast<uint32_t*>(smem + L.sb_s_off);
   float* hs = reinterpret_cast<float*>(smem + L.h_off);
   float* sxs = reinterpret_cast<float*>(smem + L.sx_off);
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
         e = 0;
       }
       uint8_t* qj = q_r + static_cast<size_t>(j) * L.nbox_r * box;
-      uint32_t* sbj = sb_r + static_cast<size_t>(j) * L.KB_r * kGemvRowsDown;
+      uint32_t* sbj = reinterpret_cast<uint32_t*>(smem + L.sb_off + static_cast<size_t>(j) * L.sb_slot_r);
       mbar_arrive_expect_tx(&bars[j], static_cast<uint32_t>(L.nbox_r * box + L.KB_r * kGemvRowsDown * 4));
       tma_load_3d(sbj, &sbd_r, &bars[j], n0, 0, e);
       for (int b = 0; b < L.nbox_r; ++b) tma_load_3d(qj + b * box, &qd_r, &bars[j], b * kBoxWords, n0, e);
@@ -363,7 +368,8 @@ __global__ void __launch_bounds__(kDownThreads, 1)
     uint32_t sbv;
     if (j < k) {
       tile = q_r + (static_cast<size_t>(j) * L.nbox_r + kb / kBoxKB) * box;
-      sbv = sb_r[(static_cast<size_t>(j) * L.KB_r + kb) * kGemvRowsDown + r];
+      sbv = reinterpret_cast<const uint32_t*>(smem + L.sb_off + static_cast<size_t>(j) * L.sb_slot_r)
+          [kb * kGemvRowsDown + r];
     } else {
       tile = q_s + static_cast<size_t>(kb / kBoxKB) * box;
       sbv = sb_s[kb * kGemvRowsDown + r];
@@ -395,6 +401,13 @@ cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMap
                         bool pdl) {
   const GUSmem Lg = gu_layout(a.d);
   const DownSmem Ld = down_layout(a.I, a.I_shared, a.k);
+  // TMA destinations: swizzled code boxes on 1024 bytes, group parameters on 128
+  const bool aligned = Lg.q_off % 1024 == 0 && (static_cast<size_t>(Lg.nbox) * kGemvRowsGU * 128) % 1024 == 0 &&
+                       Lg.sb_off % 128 == 0 && (static_cast<size_t>(Lg.KB) * kGemvRowsGU * 4) % 128 == 0 &&
+                       Ld.q_off % 1024 == 0 && Ld.q_s_off % 1024 == 0 && Ld.sb_off % 128 == 0 &&
+                       Ld.sb_slot_r % 128 == 0 && Ld.sb_s_off % 128 == 0 && Lg.bar_off % 8 == 0 &&
+                       Ld.bar_off % 8 == 0;
+  if (!aligned) return cudaErrorInvalidValue;
   if (!g_attr_set) {
     cudaError_t e1 = cudaFuncSetAttribute(gemv_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaError_t e2 = cudaFuncSetAttribute(gemv_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);

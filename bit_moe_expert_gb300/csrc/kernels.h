@@ -69,17 +69,19 @@ struct GemmArgs {
   const int32_t* num_blocks;  // [1]
   const float* w;             // [A]
   float* ypart;               // [T][k+1][d] fp32 weighted expert outputs
-  uint16_t* h_routed;         // [A][I] bf16
-  uint16_t* h_shared;         // [T][I_shared] bf16
+  uint16_t* h_routed;         // [A][I] fp16
+  uint16_t* h_shared;         // [T][I_shared] fp16
+  const uint16_t* X;          // [T][d] bf16 input
+  uint16_t* Xh;               // [T][d] fp16 copy (tensor-core operand)
   uint16_t* Y;                // [T][d] bf16
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms, max_blocks;
 };
 
 struct GemmActMaps {
-  CUtensorMap x;         // X [T][d] bf16, box (64, 1), 128-byte swizzle (gather4)
-  CUtensorMap h_routed;  // H [A][I] bf16, box (64, 16), 128-byte swizzle
-  CUtensorMap h_shared;  // H [T][I_shared] bf16, box (64, 16), 128-byte swizzle
+  CUtensorMap x;         // Xh [T][d] fp16, box (64, 1), 128-byte swizzle (gather4)
+  CUtensorMap h_routed;  // H [A][I] fp16, box (64, 16), 128-byte swizzle
+  CUtensorMap h_shared;  // H [T][I_shared] fp16, box (64, 16), 128-byte swizzle
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared,

@@ -124,7 +124,7 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 operands, fp32 accumulate).
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (16-bit operands, fp32 accumulate).
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -180,11 +180,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t start_addr) 
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor, kind::f16: fp16 A and B (format code 0), fp32 D,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4)                                 // D format: f32
-         | (1u << 7)                               // A format: bf16
-         | (1u << 10)                              // B format: bf16
+         | (0u << 7)                               // A format: f16
+         | (0u << 10)                              // B format: f16
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
@@ -203,19 +204,16 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
   return r;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
   return r;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+// Two fp32 values -> one f16x2 (round to nearest even); lo lands in bits 0..15.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   uint32_t r;
-  // a - b as a*1 + (-b): exact here (small integers)
-  asm("{\n\t.reg .b32 one;\n\tmov.b32 one, 0x3F803F80;\n\t"
-      "fma.rn.bf16x2 %0, %2, one, %1;\n\t}"
-      : "=r"(r)
-      : "r"(b ^ 0x80008000u), "r"(a));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

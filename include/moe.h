@@ -111,7 +111,7 @@ moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E
  *                            experts ascending, tiles of an expert in order
  *   num_blocks int32 [1]     number of valid block_map entries
  * block_rows records the tile height moe_route was called with; moe_forward
- * reads it.
+ * reads it.  When T = 0 the arrays of length T*k may be NULL.
  */
 typedef struct {
   int32_t* ids;

@@ -81,6 +81,8 @@ def test_route_rejects_bad_arguments(L):
     assert call(16, 16, 2, 16, logits=0) == INVALID
     r0 = bm._Routing(*([fake] * 7), 0, 0)                          # num_blocks missing
     assert L.moe_route(fake, 16, 16, 2, 16, C.byref(r0), fake, ws_ok, None) == INVALID
+    r1 = bm._Routing(0, *([fake] * 7), 0)                          # ids missing with T > 0
+    assert L.moe_route(fake, 16, 16, 2, 16, C.byref(r1), fake, ws_ok, None) == INVALID
 
 
 def test_forward_rejects_bad_arguments(L):
