@@ -1,0 +1,687 @@
+#!/usr/bin/env python3
+"""Benchmark of the 4-bit groupwise-affine MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill4096|prefill512|canvas|tiny] [--no-secondary]
+
+Prints ONE JSON line.  Headline workload: batch-1 decode through 40 distinct
+chained MoE layers (T=1, d=2048, E=256, top-8 + shared expert, I=512); a step
+is the 40-layer pass, captured in a CUDA graph.  The line also carries the
+T=4096 long prefill (four chunks of 1024 tokens, Zipf-skewed routing) measured
+the same way.  `value` is tokens per second through one MoE layer: layer
+invocations x tokens / time.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer has no exchange step on one node); value sums the ranks' tokens
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from bit_moe_expert_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s at T=1 decode (40 distinct chained layers); T=4096 prefill reported alongside"
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+class Dist:
+    def __init__(self):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        import torch
+        if torch.cuda.is_available():
+            torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+        if torch.cuda.is_available():
+            torch.cuda.synchronize()
+
+    def reduce(self, x: float, op: str) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX if op == "max" else self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks (NVML via ctypes)
+
+class ClockSampler:
+    """Samples SM clock, max clock, power and throttle reasons every few ms while
+    active.  Uses the driver's NVML library directly; falls back to nvidia-smi."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle",
+               0x2: "applications_clocks_setting", 0x100: "display_clock_setting"}
+
+    def __init__(self, gpu_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(h)) == 0:
+                    self.nvml, self.handle = nv, h
+                    m = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(m)) == 0:  # 1 = SM
+                        self.max_mhz = m.value
+        except OSError:
+            self.nvml = None
+
+    def _sample(self):
+        nv, h = self.nvml, self.handle
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(clk))
+        nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+        nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs))
+        self.samples.append((clk.value, pw.value / 1000.0, rs.value))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        self.samples = []
+        self._stop.clear()
+        if self.nvml is not None:
+            self._sample()
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+
+    def stop(self) -> dict:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._sample()
+        return self.summary()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return self._smi_snapshot()
+        mhz = [s[0] for s in self.samples]
+        reasons = 0
+        for s in self.samples:
+            reasons |= s[2]
+        names = sorted({n for bit, n in self.REASONS.items() if reasons & bit})
+        return {"sm_mhz": statistics.median(mhz), "sm_min_mhz": min(mhz), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(s[1] for s in self.samples), "reasons": names,
+                "samples": len(self.samples), "source": "nvml"}
+
+    def _smi_snapshot(self) -> dict:
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            out = subprocess.run(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits"],
+                                 capture_output=True, text=True, timeout=20).stdout.strip().splitlines()[0]
+            f = [x.strip() for x in out.split(",")]
+            names = [n for n, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                        "sw_power_cap"], f[3:]) if v.lower() == "active"]
+            return {"sm_mhz": float(f[0]), "sm_max_mhz": float(f[1]), "reasons": names, "samples": 1,
+                    "source": "nvidia-smi after the timed region"}
+        except Exception as e:  # pragma: no cover - diagnostic only
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": f"unavailable: {e}"}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class Workload:
+    """One benchmark workload on one GPU (our arm)."""
+    name = ""
+    tokens_per_step = 0        # token-layer invocations per step
+    dtype = ""
+
+    def step(self):
+        raise NotImplementedError
+
+    def e2e_step(self):
+        raise NotImplementedError
+
+
+def _dev_layer(cfg, layer, dev, with_shared=True):
+    import bit_moe_expert_gb300 as bm
+    rex = synth.draw_experts_torch(cfg, layer, dev)
+    sex = synth.draw_experts_torch(cfg, layer, dev, E=1, I=cfg.I_shared, tag=20) if (cfg.I_shared and with_shared) \
+        else None
+    routed = bm.prepare_experts(rex, dev)
+    shared = bm.prepare_experts(sex, dev) if sex is not None else None
+    return rex, sex, routed, shared
+
+
+class DecodeWorkload(Workload):
+    name = "decode"
+    dtype = "f32"
+
+    def __init__(self, dev, layers=None):
+        import torch
+        import bit_moe_expert_gb300 as bm
+        self.bm = bm
+        self.cfg = cfg = synth.CONFIGS["decode"]
+        self.L = layers or cfg.layers
+        self.T = cfg.T
+        self.dev = dev
+        self.raw, self.routed, self.shared, self.X, self.logits = [], [], [], [], []
+        self.X_host, self.logits_host = [], []
+        for l in range(self.L):
+            rex, sex, routed, shared = _dev_layer(cfg, l, dev)
+            self.raw.append((rex, sex))
+            self.routed.append(routed)
+            self.shared.append(shared)
+            xh = synth.draw_x(cfg, self.T, l)
+            lh = synth.draw_logits(cfg, self.T, l)
+            self.X_host.append(xh)
+            self.logits_host.append(lh)
+            self.X.append(torch.from_numpy(xh.view(np.int16)).to(dev))
+            self.logits.append(torch.from_numpy(lh).to(dev))
+        self.block_rows = 128
+        self.r = bm.Routing.empty(self.T, cfg.E, cfg.k, self.block_rows, dev)
+        self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(self.T, cfg.E, cfg.k), dev)
+        self.ws_f = bm.workspace(bm.moe_forward_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
+        self.Y = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16, device=dev)
+        self.tokens_per_step = self.L * self.T
+        # pinned host buffers for the end-to-end measurement
+        self.X_pin = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in self.X_host]
+        self.lg_pin = [torch.from_numpy(x).pin_memory() for x in self.logits_host]
+        self.Y_pin = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16).pin_memory()
+        self.X_e2e = torch.empty_like(self.X[0])
+        self.lg_e2e = torch.empty_like(self.logits[0])
+        self.h2d_bytes = self.L * (self.X_host[0].nbytes + self.logits_host[0].nbytes)
+        self.d2h_bytes = self.L * self.T * cfg.d * 2
+
+    def launches_per_step(self):
+        return self.L * 3  # route, gate/up GEMV, down GEMV
+
+    def step(self):
+        bm, cfg = self.bm, self.cfg
+        for l in range(self.L):
+            bm.moe_route(self.logits[l], cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X[l], self.routed[l], self.shared[l], self.r, self.Y[l], self.ws_f)
+
+    def e2e_step(self):
+        bm, cfg = self.bm, self.cfg
+        for l in range(self.L):
+            self.X_e2e.copy_(self.X_pin[l], non_blocking=True)
+            self.lg_e2e.copy_(self.lg_pin[l], non_blocking=True)
+            bm.moe_route(self.lg_e2e, cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X_e2e, self.routed[l], self.shared[l], self.r, self.Y[l], self.ws_f)
+            self.Y_pin[l].copy_(self.Y[l], non_blocking=True)
+
+    # algorithmic work
+    def bytes_per_step(self):
+        cfg = self.cfg
+        return self.L * (cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared))
+
+    def dominant(self):
+        cfg = self.cfg
+        per_launch = (cfg.k * 2 * synth.expert_bytes(cfg.I, cfg.d) + 2 * synth.expert_bytes(cfg.I_shared, cfg.d))
+        return "gemv_gateup", "hbm", per_launch, (
+            f"{cfg.k}+1 experts x gate+up x ({cfg.I} rows x {cfg.d // 2} B codes + {cfg.d // 64 * 4} B scale/bias) "
+            f"= {per_launch} B per launch")
+
+    def workload_desc(self):
+        c = self.cfg
+        return (f"decode: T={c.T}, d={c.d}, E={c.E}, top-{c.k} + shared expert, I={c.I}; {self.L} distinct chained "
+                f"layers per step (CUDA graph); 4-bit codes + bf16 scale/bias per 64")
+
+    def cpu_sample(self, budget_s):
+        """Oracle (routing + layer) on the host for the first layers until the budget is spent."""
+        import oracle
+        done, t_used = 0, 0.0
+        while t_used < budget_s and done < self.L:
+            routed, shared, ids, w = self._host_subset(done)
+            t0 = time.perf_counter()
+            r = oracle.route(self.logits_host[done], self.cfg.k, self.block_rows)
+            oracle.forward(self.X_host[done], routed, shared, self._remap(r["ids"], ids), r["w"])
+            t_used += time.perf_counter() - t0
+            done += 1
+        return done * self.T, t_used, f"{done} decode layer(s) of 1 token (routing + layer), single-threaded oracle"
+
+    def _host_subset(self, l):
+        """Host copies of the experts layer l's token selects (the oracle reads only those)."""
+        import oracle
+        r = oracle.route(self.logits_host[l], self.cfg.k, self.block_rows)
+        sel = sorted(set(int(e) for e in r["ids"].reshape(-1)))
+        rex, sex = self.raw[l]
+        idx = __import__("torch").tensor(sel, device=self.dev)
+
+        def host(ex, index=None):
+            out = {}
+            for m, (q, s, b) in ex.items():
+                if index is not None:
+                    q, s, b = q.index_select(0, index), s.index_select(0, index), b.index_select(0, index)
+                out[m] = (q.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint16),
+                          b.cpu().numpy().view(np.uint16))
+            return out
+        return host(rex, idx), host(sex) if sex is not None else None, sel, r["w"]
+
+    @staticmethod
+    def _remap(ids, sel):
+        lut = {e: i for i, e in enumerate(sel)}
+        return np.vectorize(lambda e: lut[int(e)])(ids).astype(np.int32)
+
+
+class PrefillWorkload(Workload):
+    """Chunked prefill: T tokens as chunks, each chunk through a different weight set."""
+    dtype = "f16 MMA, f32 accumulate"
+
+    def __init__(self, dev, name="prefill4096", sets=None):
+        import torch
+        import bit_moe_expert_gb300 as bm
+        self.bm = bm
+        self.name = name
+        self.cfg = cfg = synth.CONFIGS[name]
+        self.dev = dev
+        self.chunk = cfg.tokens_per_call
+        self.nchunks = cfg.T // self.chunk
+        self.sets = sets or max(self.nchunks, 4)
+        self.raw, self.routed, self.shared = [], [], []
+        for l in range(self.sets):
+            rex, sex, routed, shared = _dev_layer(cfg, l, dev)
+            self.raw.append((rex, sex))
+            self.routed.append(routed)
+            self.shared.append(shared)
+        # one prompt: X and logits for all T tokens (logits per weight set, as a real layer would produce)
+        self.X_host = synth.draw_x(cfg, cfg.T, 0)
+        self.logits_host = [synth.draw_logits(cfg, cfg.T, l) for l in range(self.sets)]
+        self.X = torch.from_numpy(self.X_host.view(np.int16)).to(dev)
+        self.logits = [torch.from_numpy(x).to(dev) for x in self.logits_host]
+        self.block_rows = 128
+        C = self.chunk
+        self.r = bm.Routing.empty(C, cfg.E, cfg.k, self.block_rows, dev)
+        self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(C, cfg.E, cfg.k), dev)
+        self.ws_f = bm.workspace(bm.moe_forward_workspace_bytes(C, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
+        self.Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
+        self.tokens_per_step = cfg.T
+        self.X_pin = torch.from_numpy(self.X_host.view(np.int16)).pin_memory()
+        self.lg_pin = [torch.from_numpy(x).pin_memory() for x in self.logits_host]
+        self.Y_pin = torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory()
+        self.X_e2e = torch.empty((C, cfg.d), dtype=torch.int16, device=dev)
+        self.lg_e2e = torch.empty((C, cfg.E), dtype=torch.float32, device=dev)
+        self.h2d_bytes = self.X_host.nbytes + self.nchunks * C * cfg.E * 4
+        self.d2h_bytes = cfg.T * cfg.d * 2
+        self._flops = None
+
+    def launches_per_step(self):
+        return self.nchunks * 5  # route, X->fp16, gate/up GEMM, down GEMM, combine
+
+    def _set(self, c):
+        return c % self.sets
+
+    def step(self):
+        bm, cfg, C = self.bm, self.cfg, self.chunk
+        for c in range(self.nchunks):
+            s = self._set(c)
+            bm.moe_route(self.logits[s][c * C:(c + 1) * C], cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X[c * C:(c + 1) * C], self.routed[s], self.shared[s], self.r,
+                           self.Y[c * C:(c + 1) * C], self.ws_f)
+
+    def e2e_step(self):
+        bm, cfg, C = self.bm, self.cfg, self.chunk
+        for c in range(self.nchunks):
+            s = self._set(c)
+            self.X_e2e.copy_(self.X_pin[c * C:(c + 1) * C], non_blocking=True)
+            self.lg_e2e.copy_(self.lg_pin[s][c * C:(c + 1) * C], non_blocking=True)
+            bm.moe_route(self.lg_e2e, cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X_e2e, self.routed[s], self.shared[s], self.r, self.Y[c * C:(c + 1) * C], self.ws_f)
+            self.Y_pin[c * C:(c + 1) * C].copy_(self.Y[c * C:(c + 1) * C], non_blocking=True)
+
+    def flops_per_step(self):
+        cfg = self.cfg
+        per_tok_expert = 6 * cfg.d * cfg.I
+        shared = 6 * cfg.d * cfg.I_shared
+        return cfg.T * (cfg.k * per_tok_expert + shared)
+
+    def dominant(self):
+        cfg = self.cfg
+        per_launch = self.chunk * (cfg.k * 4 * cfg.d * cfg.I + 4 * cfg.d * cfg.I_shared)
+        return "gemm_gateup", "tensor", per_launch, (
+            f"{self.chunk} tokens x ({cfg.k} routed + shared) x 2 matrices x 2*{cfg.d}*{cfg.I} FLOP "
+            f"= {per_launch / 1e9:.2f} GFLOP per launch")
+
+    def workload_desc(self):
+        c = self.cfg
+        return (f"{self.name}: T={c.T} as {self.nchunks} chunk(s) of {self.chunk}, d={c.d}, E={c.E}, top-{c.k}"
+                f"{' + shared' if c.I_shared else ''}, I={c.I}{', Zipf-skewed routing' if c.zipf else ''}; "
+                f"chunk c uses weight set c ({self.sets} sets x "
+                f"{(c.E * synth.ffn_bytes(c.d, c.I)) / 1e6:.0f} MB)")
+
+    def cpu_sample(self, budget_s):
+        import oracle
+        cfg, C = self.cfg, self.chunk
+        lg = self.logits_host[0][:C]
+        r = oracle.route(lg, cfg.k, self.block_rows)
+        rex, sex = self.raw[0]
+        routed = {m: (q.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint16), b.cpu().numpy().view(np.uint16))
+                  for m, (q, s, b) in rex.items()}
+        shared = ({m: (q.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint16),
+                       b.cpu().numpy().view(np.uint16)) for m, (q, s, b) in sex.items()} if sex else None)
+        X = self.X_host[:C]
+        done, t_used = 0, 0.0
+        while t_used < budget_s and done < C:
+            t0 = time.perf_counter()
+            oracle.forward(X, routed, shared, r["ids"], r["w"], done, done + 1)
+            t_used += time.perf_counter() - t0
+            done += 1
+        return done, t_used, f"{done} token(s) of chunk 0 through the layer, single-threaded oracle"
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_graph(wl, steps, warmup, dist, clocks=None):
+    import torch
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            wl.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        wl.step()
+    torch.cuda.synchronize()
+    for _ in range(max(warmup, 3)):
+        g.replay()
+    dist.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    stop.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    dist.barrier()
+    ms = start.elapsed_time(stop)
+    return ms, clk
+
+
+def time_e2e(wl, steps, warmup, dist):
+    import torch
+    for _ in range(max(warmup, 3)):
+        wl.e2e_step()
+    dist.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        wl.e2e_step()
+    stop.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return start.elapsed_time(stop)
+
+
+def time_kernels(wl, steps):
+    """Per-kernel device time: the library brackets each launch with events on
+    its own stream (a separate pass; events between kernels remove overlap)."""
+    import torch
+    bm = wl.bm
+    bm.moe_profile_reset()
+    bm.moe_profile_enable(True)
+    try:
+        for _ in range(steps):
+            wl.step()
+        torch.cuda.synchronize()
+        return bm.moe_profile_read()
+    finally:
+        bm.moe_profile_enable(False)
+        bm.moe_profile_reset()
+
+
+def run_workload(wl, args, dist, peaks, clocks):
+    ms, clk = time_graph(wl, args.steps, args.warmup, dist, clocks)
+    ms = dist.reduce(ms, "max")
+    tok = dist.reduce(float(wl.tokens_per_step * args.steps), "sum")
+    value = tok / (ms / 1e3)
+    ms_e2e = dist.reduce(time_e2e(wl, args.steps, args.warmup, dist), "max")
+    e2e = {"value": tok / (ms_e2e / 1e3), "unit": "tok/s", "h2d_bytes_per_step": wl.h2d_bytes,
+           "d2h_bytes_per_step": wl.d2h_bytes, "ms_per_step": ms_e2e / args.steps,
+           "note": "public API per call (moe_route + moe_forward), inputs copied from pinned host memory and Y "
+                   "copied back every step, no CUDA graph"}
+    kt = time_kernels(wl, min(args.steps, 200))
+    kname, bound, work, work_desc = wl.dominant()
+    kms, kn = kt[kname]
+    avg_s = (kms / max(kn, 1)) / 1e3
+    if bound == "hbm":
+        achieved = work / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        achieved = work / avg_s / 1e12
+        peak = peaks["bf16_tflops"]  # fp16 dense rate = bf16 dense rate (nominal ratio 1)
+        unit = "TFLOP/s"
+    total_k = sum(v[0] for v in kt.values())
+    shares = {k: {"launches": v[1], "avg_us": (v[0] / max(v[1], 1)) * 1e3,
+                  "share": (v[0] / total_k if total_k else 0.0)} for k, v in kt.items() if v[1]}
+    roof = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": None, "algorithmic_work_per_launch": work_desc,
+            "avg_launch_us": avg_s * 1e6, "peak_source": peaks["source"] + (
+                " copy bandwidth" if bound == "hbm" else " cuBLAS bf16 GEMM (burst); fp16 MMA has the same rate")}
+    out = {"value": value, "ms_per_step": ms / args.steps, "e2e": e2e, "roofline": roof, "kernels": shares,
+           "clocks": clk, "dtype": wl.dtype}
+    if isinstance(wl, DecodeWorkload):
+        t_layer = (ms / args.steps) / wl.L / 1e3
+        gbs = wl.bytes_per_step() / wl.L / t_layer / 1e9
+        out["layer_roofline"] = {"bound": "hbm", "active_bytes_per_layer": wl.bytes_per_step() // wl.L,
+                                 "us_per_layer": t_layer * 1e6, "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                 "note": "whole layer (routing + both GEMV kernels) inside the 40-layer graph"}
+    else:
+        fl = wl.flops_per_step() / ((ms / args.steps) / 1e3) / 1e12
+        out["step_roofline"] = {"bound": "tensor", "flops_per_step": wl.flops_per_step(), "achieved": fl,
+                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": fl / peaks["bf16_tflops"],
+                                "note": "whole step (routing, conversion, both GEMMs, combine), algorithmic FLOPs"}
+    return out
+
+
+def cpu_baseline(wl, budget_s):
+    tokens, secs, desc = wl.cpu_sample(budget_s)
+    return {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
+            "seconds": secs}
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+def _host_experts(ex, index=None):
+    out = {}
+    for m, (q, sc, bi) in ex.items():
+        if index is not None:
+            q, sc, bi = q.index_select(0, index), sc.index_select(0, index), bi.index_select(0, index)
+        out[m] = (q.cpu().numpy().view(np.uint32), sc.cpu().numpy().view(np.uint16), bi.cpu().numpy().view(np.uint16))
+    return out
+
+
+def reference_arm(args, dist):
+    """The oracle, as it stands, timed on the host cores: each step one bounded
+    sample of the headline workload (routing + layer for the decode token of
+    each sampled layer).  The device only draws the synthetic weights (torch's
+    generator, the same bytes as the GPU arm); nothing of the CUDA library runs."""
+    if dist.rank != 0:
+        return None
+    if args.workload != "decode":
+        return {"impl": "reference", "unavailable": "reference arm is defined for the decode headline workload"}
+    import torch
+    import oracle
+    dev = torch.device("cuda", dist.local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    cfg = synth.CONFIGS["decode"]
+    n_layers = 8
+    layers = []
+    for l in range(n_layers):
+        logits = synth.draw_logits(cfg, cfg.T, l)
+        X = synth.draw_x(cfg, cfg.T, l)
+        ids, _ = oracle.topk(logits, cfg.k)
+        sel = sorted(set(int(e) for e in ids.reshape(-1)))
+        rex = synth.draw_experts_torch(cfg, l, dev)
+        sex = synth.draw_experts_torch(cfg, l, dev, E=1, I=cfg.I_shared, tag=20)
+        routed = _host_experts(rex, torch.tensor(sel, device=dev))
+        shared = _host_experts(sex)
+        del rex, sex
+        lut = {e: i for i, e in enumerate(sel)}
+        layers.append((logits, X, routed, shared, lut))
+
+    def one_layer(l):
+        logits, X, routed, shared, lut = layers[l]
+        r = oracle.route(logits, cfg.k, 128)
+        ids = np.vectorize(lambda e: lut[int(e)])(r["ids"]).astype(np.int32)
+        oracle.forward(X, routed, shared, ids, r["w"])
+
+    t0 = time.perf_counter()
+    one_layer(0)
+    t_layer = time.perf_counter() - t0
+    budget = 120.0  # seconds for the whole --steps/--warmup run
+    per_step = max(1, min(n_layers, int(budget / max(args.steps + args.warmup, 1) / t_layer)))
+
+    def step():
+        for l in range(per_step):
+            one_layer(l)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    value = per_step * cfg.T * args.steps / secs
+    sample = f"{per_step} decode layer(s) of 1 token per step (routing + layer)"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": f"decode: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k} + shared expert, "
+                                   f"I={cfg.I}; CPU oracle", "reference_sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-secondary", action="store_true", help="skip the T=4096 prefill object")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    dist = Dist()
+    if args.impl == "reference":
+        res = reference_arm(args, dist)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        dist.close()
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    clocks = ClockSampler(dist.local_rank)
+
+    if args.workload == "decode":
+        wl = DecodeWorkload(dev)
+    elif args.workload in ("prefill4096", "prefill512", "canvas", "tiny"):
+        wl = PrefillWorkload(dev, args.workload)
+    main_res = run_workload(wl, args, dist, peaks, clocks)
+    cpu = cpu_baseline(wl, args.cpu_budget) if dist.rank == 0 else None
+    desc = wl.workload_desc()
+    launches = wl.launches_per_step() * args.steps
+    del wl
+    torch.cuda.empty_cache()
+
+    secondary = None
+    if args.workload == "decode" and not args.no_secondary:
+        wl2 = PrefillWorkload(dev, "prefill4096")
+        steps2 = max(3, min(args.steps, 200))
+        a2 = argparse.Namespace(**vars(args))
+        a2.steps = steps2
+        r2 = run_workload(wl2, a2, dist, peaks, ClockSampler(dist.local_rank))
+        r2["cpu_baseline"] = cpu_baseline(wl2, args.cpu_budget) if dist.rank == 0 else None
+        r2["workload"] = wl2.workload_desc()
+        r2["steps"] = steps2
+        r2["gpu_launches"] = wl2.launches_per_step() * steps2
+        secondary = r2
+        del wl2
+        torch.cuda.empty_cache()
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": main_res["value"], "unit": "tok/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": main_res["dtype"],
+            "data": "synthetic (seeded; random 4-bit codes, bf16 scale/bias, N(0,1) X and logits)",
+            "config": {"workload": desc, "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU",
+                       "l2": "inputs larger than L2 (decode: 40 distinct layers, 18.2 GB of weights; prefill: "
+                             "each chunk on its own 455 MB weight set)"},
+            "e2e": main_res["e2e"], "roofline": main_res["roofline"], "cpu_baseline": cpu,
+            "clocks": main_res["clocks"], "gpu_launches": launches, "kernels": main_res["kernels"],
+        }
+        for key in ("layer_roofline", "step_roofline"):
+            if key in main_res:
+                line[key] = main_res[key]
+        if secondary is not None:
+            line["prefill4096"] = secondary
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

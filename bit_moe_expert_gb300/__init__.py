@@ -19,10 +19,11 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NONFINITE"}
 
-# Every symbol include/moe.h declares.
+# Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_forward_workspace_bytes",
-            "moe_forward", "moe_check_status")
+            "moe_forward", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
+            "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
 
 
 class MoeError(RuntimeError):
@@ -78,6 +79,14 @@ def lib(path: Optional[str] = None):
                                   C.c_size_t, C.c_void_p]
         L.moe_check_status.restype = C.c_int
         L.moe_check_status.argtypes = [C.c_void_p, C.c_void_p]
+        L.moe_profile_enable.restype = C.c_int
+        L.moe_profile_enable.argtypes = [C.c_int]
+        L.moe_profile_kernel_count.restype = C.c_int
+        L.moe_profile_kernel_name.restype = C.c_char_p
+        L.moe_profile_kernel_name.argtypes = [C.c_int]
+        L.moe_profile_read.restype = C.c_int
+        L.moe_profile_read.argtypes = [C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_longlong)]
+        L.moe_profile_reset.restype = None
         _lib_handle = L
     return _lib_handle
 
@@ -219,6 +228,26 @@ def moe_forward(X, routed: Experts, shared: Optional[Experts], routing: Routing,
 
 def moe_check_status(ws, stream=None) -> int:
     return int(lib().moe_check_status(_ptr(ws), _stream(stream)))
+
+
+def moe_profile_enable(on: bool) -> bool:
+    return bool(lib().moe_profile_enable(1 if on else 0))
+
+
+def moe_profile_reset() -> None:
+    lib().moe_profile_reset()
+
+
+def moe_profile_read() -> dict:
+    """{kernel name: (total device ms, launches)} for every kernel kind timed since the last reset."""
+    L = lib()
+    out = {}
+    for i in range(L.moe_profile_kernel_count()):
+        ms = C.c_double()
+        n = C.c_longlong()
+        _check("moe_profile_read", L.moe_profile_read(i, C.byref(ms), C.byref(n)))
+        out[L.moe_profile_kernel_name(i).decode()] = (ms.value, n.value)
+    return out
 
 
 # ----------------------------------------------------------------------- weight preparation

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libbitmoe.so")
-SOURCES = ["api.cu", "route.cu", "gemv.cu", "gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "gemv.cu", "gemm.cu", "profile.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,7 +30,7 @@ def nvcc() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "moe.h"))
+    files += [os.path.join(INCLUDE, "moe.h"), os.path.join(INCLUDE, "moe_profile.h")]
     return files
 
 

@@ -574,28 +574,36 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
     c2.blockDim = dim3(256);
     c2.dynamicSmemBytes = 0;
     const size_t n8 = static_cast<size_t>(a.T) * a.d / 8;
+    timer_begin(kKToF16, stream);
     cudaError_t e = cudaLaunchKernelEx(&c2, x_to_f16_kernel, a.X, n8, a.Xh, a.status);
+    timer_end(kKToF16, stream);
     if (e != cudaSuccess) return e;
   }
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CG::kSmemBytes;
+  timer_begin(kKGemmGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
                                        routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
+  timer_end(kKGemmGateUp, stream);
   if (err != cudaSuccess) return err;
 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CD::kSmemBytes;
+  timer_begin(kKGemmDown, stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false>, routed->q_down, routed->q_down, routed->sb_down,
                            routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
                            act->h_shared, a);
+  timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 
   cfg.gridDim = dim3(a.num_sms * 4);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   const int slots = a.k + (a.I_shared > 0 ? 1 : 0);
-  return cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.ypart), a.T, a.d, a.k + 1, slots,
-                            a.Y);
+  timer_begin(kKCombine, stream);
+  err = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.ypart), a.T, a.d, a.k + 1, slots, a.Y);
+  timer_end(kKCombine, stream);
+  return err;
 }
 
 }  // namespace bm

@@ -428,15 +428,20 @@ cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMap
   cfg.gridDim = dim3(div_up(Imax, kGemvRowsGU), a.T * a.k + (a.I_shared > 0 ? a.T : 0));
   cfg.blockDim = dim3(kGUThreads);
   cfg.dynamicSmemBytes = Lg.total;
+  timer_begin(kKGemvGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, gemv_gateup_kernel, routed->q_gate, routed->q_up, routed->sb_gate,
                                        routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, a);
+  timer_end(kKGemvGateUp, stream);
   if (err != cudaSuccess) return err;
 
   cfg.gridDim = dim3(a.d / kGemvRowsDown, a.T);
   cfg.blockDim = dim3(kDownThreads);
   cfg.dynamicSmemBytes = Ld.total;
   attr[0].val.programmaticStreamSerializationAllowed = 1;  // always chained to the gate/up kernel
-  return cudaLaunchKernelEx(&cfg, gemv_down_kernel, routed->q_down, routed->sb_down, sh->q_down, sh->sb_down, a);
+  timer_begin(kKGemvDown, stream);
+  err = cudaLaunchKernelEx(&cfg, gemv_down_kernel, routed->q_down, routed->sb_down, sh->q_down, sh->sb_down, a);
+  timer_end(kKGemvDown, stream);
+  return err;
 }
 
 }  // namespace bm

@@ -11,6 +11,21 @@
 
 namespace bm {
 
+// Kernel kinds for the optional per-kernel timing (moe_profile.h).
+enum KernelKind {
+  kKRoute = 0,
+  kKGemvGateUp,
+  kKGemvDown,
+  kKToF16,
+  kKGemmGateUp,
+  kKGemmDown,
+  kKCombine,
+  kKPrepack,
+  kKernelKinds
+};
+void timer_begin(int id, cudaStream_t s);
+void timer_end(int id, cudaStream_t s);
+
 struct RouteOut {
   int32_t* ids;
   float* w;

@@ -248,7 +248,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_kernel, logits, T, E, k, block_rows, out, hdr, chunk_hist, local_rank);
+  timer_begin(kKRoute, stream);
+  const cudaError_t err =
+      cudaLaunchKernelEx(&cfg, route_kernel, logits, T, E, k, block_rows, out, hdr, chunk_hist, local_rank);
+  timer_end(kKRoute, stream);
+  return err;
 }
 
 size_t route_hist_elems(int T, int E) {
@@ -282,8 +286,11 @@ cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, i
   const int threads = 256;
   const size_t blocks = (total + threads - 1) / threads;
   const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
+  timer_begin(kKPrepack, stream);
   prepack_kernel<<<grid, threads, 0, stream>>>(scale, bias, E, N, G, sb);
-  return cudaGetLastError();
+  const cudaError_t err = cudaGetLastError();
+  timer_end(kKPrepack, stream);
+  return err;
 }
 
 }  // namespace bm

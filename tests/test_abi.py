@@ -12,7 +12,7 @@ import bit_moe_expert_gb300 as bm
 from bit_moe_expert_gb300 import build as bbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
 
@@ -24,9 +24,12 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_and_binding_agree():
@@ -39,6 +42,14 @@ def test_every_declared_symbol_is_exported(L):
     for name in declared_functions():
         assert name in exported, name
         assert hasattr(L, name)
+
+
+def test_profile_surface_without_gpu(L):
+    names = [L.moe_profile_kernel_name(i).decode() for i in range(L.moe_profile_kernel_count())]
+    assert "gemv_gateup" in names and "gemm_gateup" in names and "route" in names
+    assert L.moe_profile_kernel_name(-1) is None
+    assert L.moe_profile_enable(0) == 0
+    assert L.moe_profile_read(-1, C.byref(C.c_double()), C.byref(C.c_longlong())) == INVALID
 
 
 def test_status_strings(L):
