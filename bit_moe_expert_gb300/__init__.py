@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_scales",
-            "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_forward_workspace_bytes",
+            "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
+            "moe_forward_workspace_bytes",
             "moe_forward", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
             "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
 
@@ -71,6 +72,9 @@ def lib(path: Optional[str] = None):
         L.moe_route.restype = C.c_int
         L.moe_route.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                 C.c_void_p, C.c_size_t, C.c_void_p]
+        L.moe_route_noalloc.restype = C.c_int
+        L.moe_route_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
+                                        C.c_void_p]
         L.moe_forward_workspace_bytes.restype = C.c_size_t
         L.moe_forward_workspace_bytes.argtypes = [C.c_int] * 6
         L.moe_forward.restype = C.c_int
@@ -207,6 +211,17 @@ def moe_route(logits, k: int, block_rows: int, out: Routing, ws, stream=None) ->
     r = out._c()
     _check("moe_route", lib().moe_route(_ptr(logits), T, E, k, block_rows, C.byref(r), _ptr(ws), ws.numel(),
                                         _stream(stream)))
+    out.block_rows = r.block_rows
+
+
+def moe_route_noalloc(logits, k: int, block_rows: int, out: Routing, stream=None) -> None:
+    """moe_route without a workspace (for callers that cannot allocate device
+    memory): uses the library's built-in scratch array; calls must not overlap
+    on the GPU."""
+    T, E = logits.shape
+    r = out._c()
+    _check("moe_route_noalloc", lib().moe_route_noalloc(_ptr(logits), T, E, k, block_rows, C.byref(r),
+                                                        _stream(stream)))
     out.block_rows = r.block_rows
 
 

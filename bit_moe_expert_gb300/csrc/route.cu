@@ -13,6 +13,8 @@
 // every assignment, and writes the block map.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -294,3 +296,53 @@ cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, i
 }
 
 }  // namespace bm
+
+// ------------------------------------------------------------------ routing without a workspace
+// The scratch of moe_route_noalloc: one file-scope device array, loaded with
+// the module on every device that uses the library.  Host code must not pass
+// the name itself to a kernel (on the host it is only a stand-in); the device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+namespace bm {
+namespace {
+
+static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+}  // namespace bm
+
+extern "C" moe_status moe_route_noalloc(const float* logits, int T, int E, int k, int block_rows,
+                                        moe_routing* out, moe_stream stream) {
+  using namespace bm;
+  if (!out || T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * k > MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS ||
+      route_hist_elems(T, E) > static_cast<size_t>(MOE_ROUTE_NOALLOC_MAX_HIST))
+    return MOE_ERR_UNSUPPORTED;
+  if (!out->counts || !out->offsets || !out->block_map || !out->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !out->ids || !out->w || !out->perm || !out->inv_perm)) return MOE_ERR_INVALID_ARG;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+      g_scratch_addr[dev] = p;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the arrival ticket and the status word must start at zero
+  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+  out->block_rows = block_rows;
+  RouteOut o{out->ids, out->w, out->counts, out->offsets, out->perm, out->inv_perm, out->block_map, out->num_blocks};
+  if (launch_route(logits, T, E, k, block_rows, o, scratch, st, false) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -142,6 +142,37 @@ size_t moe_route_workspace_bytes(int T, int E, int k);
 moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
                      void* ws, size_t ws_bytes, moe_stream stream);
 
+/* ------------------------------------------------------------------ routing without a workspace
+ * moe_route_noalloc: no counterpart on the source pages.  It computes exactly
+ * what moe_route computes, into the same caller-owned output arrays, for
+ * callers that cannot allocate device memory -- for example code hosted by a
+ * framework that owns all device memory and forbids cudaMalloc once it has
+ * started, or code that runs while a stream is being captured into a CUDA
+ * graph, where allocating is not allowed.  Instead of a workspace it uses one
+ * scratch array compiled into the library: MOE_ROUTE_NOALLOC_SCRATCH_BYTES of
+ * device memory on every GPU that loads the library, held until the process
+ * exits.
+ *   - Limits: T*k <= MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS and
+ *     ceil(T/32)*E <= MOE_ROUTE_NOALLOC_MAX_HIST; larger sizes return
+ *     MOE_ERR_UNSUPPORTED and launch nothing.  Other preconditions and errors
+ *     as for moe_route.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (with that device current).  Make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array and leaves its contents behind; each call
+ *     first clears the part that must start at zero (cudaMemsetAsync on
+ *     `stream`).  Calls that overlap on the GPU -- on different streams or from
+ *     different host threads -- race and produce wrong results: keep them
+ *     ordered on one stream.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - A non-finite logit is not reported (there is no workspace status word);
+ *     use moe_route with a workspace and moe_check_status to detect it. */
+#define MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS 65536
+#define MOE_ROUTE_NOALLOC_MAX_HIST 65536
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (256 + 4 * (MOE_ROUTE_NOALLOC_MAX_HIST + MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS))
+moe_status moe_route_noalloc(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
+                             moe_stream stream);
+
 /* ------------------------------------------------------------------ experts
  * Workspace bytes moe_forward needs for these sizes (I_shared = 0: no shared
  * expert).  Same rules as the routing workspace: zero-filled once before first
