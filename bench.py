@@ -617,6 +617,11 @@ def main():
     ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-secondary", action="store_true", help="skip the T=4096 prefill object")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="decode: layers per step; prefill: weight sets (default: the workload's own)")
+    ap.add_argument("--only-graph", action="store_true",
+                    help="time the graph only (no end-to-end pass, kernel-timing pass or CPU baseline): "
+                         "a small, quick case for profilers")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -637,9 +642,17 @@ def main():
     clocks = ClockSampler(dist.local_rank)
 
     if args.workload == "decode":
-        wl = DecodeWorkload(dev)
-    elif args.workload in ("prefill4096", "prefill512", "canvas", "tiny"):
-        wl = PrefillWorkload(dev, args.workload)
+        wl = DecodeWorkload(dev, layers=args.layers or None)
+    else:
+        wl = PrefillWorkload(dev, args.workload, sets=args.layers or None)
+    if args.only_graph:
+        ms, clk = time_graph(wl, args.steps, args.warmup, dist, clocks)
+        if dist.rank == 0:
+            print(json.dumps({"workload": wl.workload_desc(), "ms_per_step": ms / args.steps,
+                              "value": wl.tokens_per_step * args.steps / (ms / 1e3), "unit": "tok/s",
+                              "clocks": clk, "only_graph": True}), flush=True)
+        dist.close()
+        return
     main_res = run_workload(wl, args, dist, peaks, clocks)
     cpu = cpu_baseline(wl, args.cpu_budget) if dist.rank == 0 else None
     desc = wl.workload_desc()

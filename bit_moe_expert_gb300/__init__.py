@@ -51,10 +51,11 @@ _lib_handle = None
 
 
 def lib(path: Optional[str] = None):
-    """Loads the CUDA library (raises if it has not been built)."""
+    """Loads the CUDA library (raises if it has not been built).  The environment
+    variable BITMOE_LIB may name another build of it (for A/B comparisons)."""
     global _lib_handle
     if _lib_handle is None:
-        p = path or LIB_PATH
+        p = path or os.environ.get("BITMOE_LIB") or LIB_PATH
         if not os.path.exists(p):
             raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
         L = C.CDLL(p)

@@ -214,44 +214,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* msb0 = m.shared ? &sb0_s : &sb0_r;
       const CUtensorMap* msb1 = m.shared ? &sb1_s : &sb1_r;
       const CUtensorMap* mact = m.shared ? &act_s : &act_r;
+      // Token rows of the tile, loaded once per item: lane g owns rows 4g..4g+3
+      // (the gather coordinates; rows past the tile read row T, out of range,
+      // which TMA zero-fills).
+      int tok[4] = {a.T, a.T, a.T, a.T};
+      if (kGateUp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = lane * 4 + i;
+          if (p < m.rows) tok[i] = m.shared ? m.row0 + p : __ldg(a.perm + m.row0 + p) / a.k;
+        }
+      }
+      const uint32_t bytes = C::kMats * (C::kQBytes + C::kSBBytes) + bn * 128;
       for (int kb = 0; kb < m.nk && ok; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
+        uint8_t* st = stages + stage * C::kStageBytes;
+        uint8_t* b_tile = st;
+        uint8_t* q_tile = st + C::kBBytes;
+        uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
         if (lane == 0) {
-          uint8_t* st = stages + stage * C::kStageBytes;
-          uint8_t* b_tile = st;
-          uint8_t* q_tile = st + C::kBBytes;
-          uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
-          const uint32_t bytes = C::kMats * (C::kQBytes + C::kSBBytes) + bn * 128;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_3d(q_tile, mq0, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
             tma_load_3d(q_tile + C::kQBytes, mq1, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
             tma_load_3d(sb_tile + C::kSBBytes, msb1, &full[stage], m.mt * kGemmBM, kb, m.e);
-            // token rows of the tile; rows past the tile read out of range
-            // (row T) and are zero-filled
-            for (int g = 0; g < bn / 4; ++g) {
-              int r[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int p = g * 4 + i;
-                if (p < m.rows)
-                  r[i] = m.shared ? m.row0 + p : __ldg(a.perm + m.row0 + p) / a.k;
-                else
-                  r[i] = a.T;
-              }
-              tma_gather4(b_tile + g * 512, mact, &full[stage], kb * 64, r[0], r[1], r[2], r[3]);
-            }
-          } else {
-            for (int g = 0; g < bn / 16; ++g)
-              tma_load_2d(b_tile + g * 2048, mact, &full[stage], kb * 64, m.row0 + g * 16);
           }
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        }
+        __syncwarp();  // the expected byte count is registered before any row load can complete
+        if (kGateUp) {
+          if (lane < bn / 4)
+            tma_gather4(b_tile + lane * 512, mact, &full[stage], kb * 64, tok[0], tok[1], tok[2], tok[3]);
+        } else {
+          if (lane < bn / 16) tma_load_2d(b_tile + lane * 2048, mact, &full[stage], kb * 64, m.row0 + lane * 16);
         }
         __syncwarp();
         if (++stage == C::kStages) {
@@ -442,32 +443,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        // destination slot and routing weight of each column, loaded once per
+        // item: lane L owns columns L, L+32, L+64, L+96
+        int slot[4];
+        float wt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = lane + 32 * i;
+          slot[i] = -1;
+          wt[i] = 0.0f;
+          if (c < m.rows) {
+            const int p = m.row0 + c;
+            if (m.shared) {
+              slot[i] = p * (a.k + 1) + a.k;
+              wt[i] = 1.0f;
+            } else {
+              const int asg = __ldg(a.perm + p);
+              if (asg >= 0 && asg < a.T * a.k) {
+                slot[i] = asg + asg / a.k;
+                wt[i] = __ldg(a.w + asg);
+              } else {
+                record_status(a.status, MOE_ERR_INVALID_ARG);
+              }
+            }
+          }
+        }
         for (int c0 = 0; c0 < bn; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tbase + c0, v);
           tc_wait_ld();
-          if (n < a.d) {
+          const int grp = c0 >> 5;  // which register holds these columns (uniform in the warp)
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              if (c0 + c < m.rows) {
-                const int p = m.row0 + c0 + c;
-                size_t slot;
-                float wt;
-                if (m.shared) {
-                  slot = static_cast<size_t>(p) * (a.k + 1) + a.k;
-                  wt = 1.0f;
-                } else {
-                  const int asg = __ldg(a.perm + p);
-                  if (asg < 0 || asg >= a.T * a.k) {
-                    record_status(a.status, MOE_ERR_INVALID_ARG);
-                    continue;
-                  }
-                  slot = static_cast<size_t>(asg) + asg / a.k;
-                  wt = __ldg(a.w + asg);
-                }
-                a.ypart[slot * a.d + n] = wt * __uint_as_float(v[c]);
-              }
+          for (int c = 0; c < 16; ++c) {
+            const int col = c0 + c;
+            const int src = col & 31;
+            int sl;
+            float wv;
+            if (grp == 0) {
+              sl = __shfl_sync(0xffffffffu, slot[0], src);
+              wv = __shfl_sync(0xffffffffu, wt[0], src);
+            } else if (grp == 1) {
+              sl = __shfl_sync(0xffffffffu, slot[1], src);
+              wv = __shfl_sync(0xffffffffu, wt[1], src);
+            } else if (grp == 2) {
+              sl = __shfl_sync(0xffffffffu, slot[2], src);
+              wv = __shfl_sync(0xffffffffu, wt[2], src);
+            } else {
+              sl = __shfl_sync(0xffffffffu, slot[3], src);
+              wv = __shfl_sync(0xffffffffu, wt[3], src);
             }
+            if (n < a.d && sl >= 0) a.ypart[static_cast<size_t>(sl) * a.d + n] = wv * __uint_as_float(v[c]);
           }
         }
       }

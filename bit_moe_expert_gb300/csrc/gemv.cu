@@ -165,22 +165,26 @@ __global__ void __launch_bounds__(kGUThreads, 1)
   }
   __syncthreads();
 
+  // Lane b < nbox of warp 0 loads code box b of both matrices; lane nbox the
+  // group parameters.
   auto issue_loads = [&](int e) {
     const uint32_t box_bytes = kGemvRowsGU * 128;
-    mbar_arrive_expect_tx(&bars[L.nbox], 2u * L.KB * kGemvRowsGU * 4);
-    tma_load_3d(sbg, msbg, &bars[L.nbox], n0, 0, e);
-    tma_load_3d(sbu, msbu, &bars[L.nbox], n0, 0, e);
-    for (int b = 0; b < L.nbox; ++b) {
+    const int b = threadIdx.x;
+    if (b < L.nbox) {
       mbar_arrive_expect_tx(&bars[b], 2 * box_bytes);
       tma_load_3d(qg + static_cast<size_t>(b) * box_bytes, mqg, &bars[b], b * kBoxWords, n0, e);
       tma_load_3d(qu + static_cast<size_t>(b) * box_bytes, mqu, &bars[b], b * kBoxWords, n0, e);
+    } else if (b == L.nbox) {
+      mbar_arrive_expect_tx(&bars[L.nbox], 2u * L.KB * kGemvRowsGU * 4);
+      tma_load_3d(sbg, msbg, &bars[L.nbox], n0, 0, e);
+      tma_load_3d(sbu, msbu, &bars[L.nbox], n0, 0, e);
     }
   };
 
   // The shared expert's weights do not depend on the previous kernel.
-  if (threadIdx.x == 0 && is_shared) issue_loads(0);
+  if (threadIdx.x <= L.nbox && is_shared) issue_loads(0);
   pdl_wait();
-  if (threadIdx.x == 0 && !is_shared) {
+  if (threadIdx.x <= L.nbox && !is_shared) {
     int e = a.ids[pair];
     if (e < 0 || e >= a.E) {
       record_status(a.status, MOE_ERR_INVALID_ARG);
@@ -295,15 +299,17 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   }
   __syncthreads();
 
-  if (threadIdx.x == 0) {
-    if (has_shared) {
+  // Lane j of warp 0 loads expert j's codes and group parameters (lane k: the
+  // shared expert).  The routing was complete before the gate/up kernel
+  // released this grid, so the expert ids can be read before waiting on that
+  // kernel; only h needs the wait.
+  if (threadIdx.x < L.nexp) {
+    const int j = threadIdx.x;
+    if (j == k) {
       mbar_arrive_expect_tx(&bars[k], static_cast<uint32_t>(L.nbox_s * box + L.KB_s * kGemvRowsDown * 4));
       tma_load_3d(sb_s, &sbd_s, &bars[k], n0, 0, 0);
       for (int b = 0; b < L.nbox_s; ++b) tma_load_3d(q_s + b * box, &qd_s, &bars[k], b * kBoxWords, n0, 0);
-    }
-    // The routing was complete before the gate/up kernel released this grid,
-    // so the expert ids can be read before waiting on that kernel.
-    for (int j = 0; j < k; ++j) {
+    } else {
       int e = a.ids[static_cast<size_t>(t) * k + j];
       if (e < 0 || e >= a.E) {
         record_status(a.status, MOE_ERR_INVALID_ARG);

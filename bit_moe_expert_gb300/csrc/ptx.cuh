@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void record_status(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
@@ -54,19 +48,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp sleeps in hardware until the
+// phase completes or about `hint_ns` elapse, instead of polling (a polling
+// warp takes issue slots from the warps doing the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // A wait that gives up: after kWaitLimitNs, or as soon as *abort (a flag in
 // shared memory that another role of the CTA raised) is non-zero.  Returns
 // false when it gave up; the caller records MOE_ERR_TIMEOUT and unwinds.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+// The limit is counted in SM clock cycles (clock64 is cheap to read, unlike
+// the global nanosecond timer): 4e9 cycles is about 2 s at the maximum clock.
+constexpr long long kWaitLimitCycles = 4000000000ll;
+constexpr uint32_t kSleepHintNs = 20000;  // re-check the abort flag and the limit this often
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (abort && *abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 

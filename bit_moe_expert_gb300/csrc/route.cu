@@ -22,13 +22,9 @@ namespace bm {
 
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
-
-struct BestKV {
-  float v;
-  int i;  // -1 = none
-};
+constexpr int kBasesSmemLimit = 96 * 1024;  // per-chunk bases kept in shared memory up to this size
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   if (bi < 0) return i >= 0;
@@ -36,12 +32,19 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// kPL: logits per lane (E <= 32 * kPL).
+template <int kPL>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E,
                                                               int k, int block_rows, RouteOut out,
                                                               WsHeader* hdr, int32_t* __restrict__ chunk_hist,
-                                                              int32_t* __restrict__ local_rank) {
+                                                              int32_t* __restrict__ local_rank, int bases_in_smem) {
+  extern __shared__ int32_t s_bases[];  // [nchunks][E] exclusive per-chunk bases (last CTA, when they fit)
   __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
+  __shared__ int32_t s_rank[kRouteTokensPerCta * kMaxK];
   __shared__ int32_t s_cnt[kMaxE];
+  __shared__ int32_t s_off[kMaxE + 1];
+  __shared__ int32_t s_boff[kMaxE + 1];
+  __shared__ int32_t s_part[2][kRouteThreads];
   __shared__ int s_is_last;
 
   pdl_wait();  // the previous kernel on the stream may still own our outputs
@@ -50,25 +53,27 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
+  const int nchunks = gridDim.x;
   const int t0 = chunk * kRouteTokensPerCta;
   const int ntok = max(0, min(kRouteTokensPerCta, T - t0));
-  const int per_lane = (E + 31) >> 5;
+  const int A = T * k;
 
   for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
 
-  // ---- top-k, one warp per token
+  // ---- top-k, one warp per token: k rounds of a warp-wide arg-max
   for (int tl = warp; tl < ntok; tl += kRouteWarps) {
     const int t = t0 + tl;
     const float* row = logits + static_cast<size_t>(t) * E;
-    float v[kMaxE / 32];
+    float v[kPL];
     uint32_t taken = 0;
     bool finite = true;
 #pragma unroll
-    for (int c = 0; c < kMaxE / 32; ++c) {
+    for (int c = 0; c < kPL; ++c) {
       const int e = lane + 32 * c;
-      v[c] = (c < per_lane && e < E) ? __ldg(row + e) : 0.0f;
-      if (c < per_lane && e < E) finite &= isfinite(v[c]);
-      if (!(c < per_lane && e < E)) taken |= 1u << c;
+      const bool in = e < E;
+      v[c] = in ? __ldg(row + e) : 0.0f;
+      finite &= !in || isfinite(v[c]);
+      if (!in) taken |= 1u << c;
     }
     if (!__all_sync(0xffffffffu, finite)) record_status(&hdr->status, MOE_ERR_NONFINITE);
 
@@ -78,8 +83,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
       float bv = 0.0f;
       int bi = -1;
 #pragma unroll
-      for (int c = 0; c < kMaxE / 32; ++c) {
-        if (c < per_lane && !((taken >> c) & 1u)) {
+      for (int c = 0; c < kPL; ++c) {
+        if (!((taken >> c) & 1u)) {
           const int e = lane + 32 * c;
           if (better(v[c], e, bv, bi)) {
             bv = v[c];
@@ -130,47 +135,53 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
       if (valid) cnt_before = s_cnt[e];
       __syncwarp();
       if (valid) {
-        local_rank[static_cast<size_t>(t0) * k + a] = cnt_before + before;
+        s_rank[a] = cnt_before + before;
         if (before == 0) s_cnt[e] = cnt_before + __popc(peers);  // group leader publishes
       }
       __syncwarp();
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) chunk_hist[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
 
-  // ---- last CTA to arrive finishes the layout
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned ticket = atomicAdd(&hdr->ticket, 1u);
-    s_is_last = (ticket == gridDim.x - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_is_last) return;
-  __threadfence();
-
-  const int nchunks = gridDim.x;
-  const int A = T * k;
-  // counts[e] and the per-chunk exclusive bases (in place over chunk_hist)
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
-    int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const size_t idx = static_cast<size_t>(c) * E + e;
-      const int h = __ldcg(chunk_hist + idx);
-      chunk_hist[idx] = run;
-      run += h;
+  if (nchunks > 1) {
+    // publish this chunk's counts and ranks, then the last CTA finishes
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) chunk_hist[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
+    for (int a = threadIdx.x; a < na; a += kRouteThreads) local_rank[static_cast<size_t>(t0) * k + a] = s_rank[a];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned ticket = atomicAdd(&hdr->ticket, 1u);
+      s_is_last = (ticket == gridDim.x - 1) ? 1 : 0;
     }
-    s_cnt[e] = run;
-    out.counts[e] = run;
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+    // counts and exclusive per-chunk bases; loads batched so they overlap
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+      int run = 0;
+      for (int c0 = 0; c0 < nchunks; c0 += 8) {
+        int h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          h[i] = (c0 + i < nchunks) ? __ldcg(chunk_hist + static_cast<size_t>(c0 + i) * E + e) : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i < nchunks) {
+            if (bases_in_smem)
+              s_bases[(c0 + i) * E + e] = run;
+            else
+              chunk_hist[static_cast<size_t>(c0 + i) * E + e] = run;
+          }
+          run += h[i];
+        }
+      }
+      s_cnt[e] = run;
+    }
+    __syncthreads();
   }
-  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) out.counts[e] = s_cnt[e];
 
-  // exclusive scans over experts: offsets (rows) and block offsets (tiles);
-  // E <= 1024 values, one thread walks a contiguous slice, then a warp scan
-  __shared__ int32_t s_off[kMaxE + 1];
-  __shared__ int32_t s_boff[kMaxE + 1];
-  __shared__ int32_t s_part[2][kRouteThreads];
+  // ---- exclusive scans over experts: row offsets and tile offsets
   {
     const int per = (E + kRouteThreads - 1) / kRouteThreads;
     const int lo = threadIdx.x * per;
@@ -180,36 +191,60 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
       rs += s_cnt[e];
       bs += (s_cnt[e] + block_rows - 1) / block_rows;
     }
-    s_part[0][threadIdx.x] = rs;
-    s_part[1][threadIdx.x] = bs;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int r = 0, b = 0;
-      for (int i = 0; i < kRouteThreads; ++i) {
-        const int tr = s_part[0][i], tb = s_part[1][i];
-        s_part[0][i] = r;
-        s_part[1][i] = b;
-        r += tr;
-        b += tb;
+    // warp-level inclusive scans of the per-thread sums, then across warps
+    int ir = rs, ib = bs;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int r2 = __shfl_up_sync(0xffffffffu, ir, off);
+      const int b2 = __shfl_up_sync(0xffffffffu, ib, off);
+      if (lane >= off) {
+        ir += r2;
+        ib += b2;
       }
-      s_off[E] = r;
-      s_boff[E] = b;
+    }
+    if (lane == 31) {
+      s_part[0][warp] = ir;
+      s_part[1][warp] = ib;
     }
     __syncthreads();
-    rs = s_part[0][threadIdx.x];
-    bs = s_part[1][threadIdx.x];
+    if (warp == 0) {
+      int wr = lane < kRouteWarps ? s_part[0][lane] : 0;
+      int wb = lane < kRouteWarps ? s_part[1][lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int r2 = __shfl_up_sync(0xffffffffu, wr, off);
+        const int b2 = __shfl_up_sync(0xffffffffu, wb, off);
+        if (lane >= off) {
+          wr += r2;
+          wb += b2;
+        }
+      }
+      if (lane < kRouteWarps) {
+        s_part[0][kRouteWarps + lane] = wr;  // inclusive totals per warp
+        s_part[1][kRouteWarps + lane] = wb;
+      }
+    }
+    __syncthreads();
+    const int wbase_r = warp > 0 ? s_part[0][kRouteWarps + warp - 1] : 0;
+    const int wbase_b = warp > 0 ? s_part[1][kRouteWarps + warp - 1] : 0;
+    rs = wbase_r + ir - rs;  // exclusive prefix of this thread's slice
+    bs = wbase_b + ib - bs;
     for (int e = lo; e < hi; ++e) {
       s_off[e] = rs;
       s_boff[e] = bs;
       rs += s_cnt[e];
       bs += (s_cnt[e] + block_rows - 1) / block_rows;
     }
+    if (threadIdx.x == kRouteThreads - 1) {
+      s_off[E] = s_part[0][2 * kRouteWarps - 1];
+      s_boff[E] = s_part[1][2 * kRouteWarps - 1];
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += kRouteThreads) out.offsets[e] = s_off[e];
   if (threadIdx.x == 0) *out.num_blocks = s_boff[E];
 
-  // block map
+  // ---- block map
   for (int e = threadIdx.x; e < E; e += kRouteThreads) {
     const int cnt = s_cnt[e];
     int b = s_boff[e];
@@ -220,15 +255,38 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     }
   }
 
-  // scatter: position = offsets[e] + base of the chunk for e + rank within the chunk
-  for (int a = threadIdx.x; a < A; a += kRouteThreads) {
-    const int e = __ldcg(out.ids + a);
-    const int c = (a / k) / kRouteTokensPerCta;
-    const int pos = s_off[e] + __ldcg(chunk_hist + static_cast<size_t>(c) * E + e) + __ldcg(local_rank + a);
-    out.perm[pos] = a;
-    out.inv_perm[a] = pos;
+  // ---- scatter: position = offsets[e] + base of the chunk for e + rank within the chunk
+  if (nchunks == 1) {
+    for (int a = threadIdx.x; a < na; a += kRouteThreads) {
+      const int pos = s_off[s_ids[a]] + s_rank[a];
+      out.perm[pos] = a;
+      out.inv_perm[a] = pos;
+    }
+  } else {
+    constexpr int kU = 8;
+    for (int a0 = threadIdx.x; a0 < A; a0 += kRouteThreads * kU) {
+      int e[kU], rk[kU];
+#pragma unroll
+      for (int i = 0; i < kU; ++i) {
+        const int a = a0 + i * kRouteThreads;
+        e[i] = a < A ? __ldcg(out.ids + a) : 0;
+        rk[i] = a < A ? __ldcg(local_rank + a) : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < kU; ++i) {
+        const int a = a0 + i * kRouteThreads;
+        if (a < A) {
+          const int c = (a / k) / kRouteTokensPerCta;
+          const int base = bases_in_smem ? s_bases[c * E + e[i]]
+                                         : __ldcg(chunk_hist + static_cast<size_t>(c) * E + e[i]);
+          const int pos = s_off[e[i]] + base + rk[i];
+          out.perm[pos] = a;
+          out.inv_perm[a] = pos;
+        }
+      }
+    }
+    if (threadIdx.x == 0) hdr->ticket = 0;  // ready for the next call
   }
-  if (threadIdx.x == 0) hdr->ticket = 0;  // ready for the next call
 }
 
 }  // namespace
@@ -239,11 +297,21 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   const int nchunks = T > 0 ? (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta : 1;
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
   int32_t* local_rank = chunk_hist + route_hist_elems(T, E);
+  const size_t bases_bytes = nchunks > 1 ? static_cast<size_t>(nchunks) * E * 4 : 0;
+  const int bases_in_smem = (nchunks > 1 && bases_bytes <= static_cast<size_t>(kBasesSmemLimit)) ? 1 : 0;
 
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e1 = cudaFuncSetAttribute(route_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
+    cudaError_t e2 = cudaFuncSetAttribute(route_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
+    if (e1 != cudaSuccess) return e1;
+    if (e2 != cudaSuccess) return e2;
+    attr_set = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunks);
   cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = bases_in_smem ? bases_bytes : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -252,7 +320,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   cfg.numAttrs = 1;
   timer_begin(kKRoute, stream);
   const cudaError_t err =
-      cudaLaunchKernelEx(&cfg, route_kernel, logits, T, E, k, block_rows, out, hdr, chunk_hist, local_rank);
+      E <= 256 ? cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, T, E, k, block_rows, out, hdr, chunk_hist,
+                                    local_rank, bases_in_smem)
+               : cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, T, E, k, block_rows, out, hdr, chunk_hist,
+                                    local_rank, bases_in_smem);
   timer_end(kKRoute, stream);
   return err;
 }
