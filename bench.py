@@ -240,7 +240,7 @@ class DecodeWorkload(Workload):
         self.d2h_bytes = self.L * self.T * cfg.d * 2
 
     def launches_per_step(self):
-        return self.L * 3  # route, gate/up GEMV, down GEMV
+        return self.L * 2  # route, fused decode kernel
 
     def step(self):
         bm, cfg = self.bm, self.cfg
@@ -264,9 +264,9 @@ class DecodeWorkload(Workload):
 
     def dominant(self):
         cfg = self.cfg
-        per_launch = (cfg.k * 2 * synth.expert_bytes(cfg.I, cfg.d) + 2 * synth.expert_bytes(cfg.I_shared, cfg.d))
-        return "gemv_gateup", "hbm", per_launch, (
-            f"{cfg.k}+1 experts x gate+up x ({cfg.I} rows x {cfg.d // 2} B codes + {cfg.d // 64 * 4} B scale/bias) "
+        per_launch = cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared)
+        return "decode", "hbm", per_launch, (
+            f"({cfg.k} routed + 1 shared) experts x (gate+up+down) 4-bit codes and bf16 scale/bias "
             f"= {per_launch} B per launch")
 
     def workload_desc(self):

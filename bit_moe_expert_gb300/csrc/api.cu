@@ -130,8 +130,6 @@ bool experts_ok(const moe_experts* ex) {
 
 }  // namespace
 
-size_t gemv_smem_gateup(int d);
-size_t gemv_smem_down(int I, int I_shared, int k);
 
 }  // namespace bm
 
@@ -235,9 +233,7 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     if (!std::strcmp(p, "gemv")) path = Path::kGemv;
     if (!std::strcmp(p, "gemm")) path = Path::kGemm;
   }
-  const size_t smem_limit = 227 * 1024;
-  const bool gemv_fits = gemv_smem_gateup(d) <= smem_limit && gemv_smem_down(I, I_shared, k) <= smem_limit;
-  if (path == Path::kGemv && !gemv_fits) path = Path::kGemm;
+  if (path == Path::kGemv && !gemv_supported(d, I, I_shared, k)) path = Path::kGemm;
 
   if (path == Path::kGemv) {
     GemvMaps mr, ms;
@@ -270,7 +266,9 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     a.k = k;
     a.I_shared = I_shared;
     a.E = E;
-    if (launch_gemv(a, &mr, shared ? &ms : nullptr, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+    a.num_sms = sm_count();
+    if (a.num_sms <= 0) return MOE_ERR_CUDA;
+    if (launch_gemv(a, &mr, shared ? &ms : nullptr, ws, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
 

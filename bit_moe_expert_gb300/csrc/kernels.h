@@ -14,8 +14,8 @@ namespace bm {
 // Kernel kinds for the optional per-kernel timing (moe_profile.h).
 enum KernelKind {
   kKRoute = 0,
-  kKGemvGateUp,
-  kKGemvDown,
+  kKGemvGateUp,  // the fused decode kernel (gate/up + down)
+  kKGemvDown,    // reserved
   kKToF16,
   kKGemmGateUp,
   kKGemmDown,
@@ -62,11 +62,12 @@ struct GemvArgs {
   float* h_routed;     // [T*k][I] fp32
   float* h_shared;     // [T][I_shared] fp32
   uint32_t* status;
-  int T, d, I, k, I_shared, E;
+  int T, d, I, k, I_shared, E, num_sms;
 };
 
-cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMaps* shared, cudaStream_t stream,
-                        bool pdl);
+bool gemv_supported(int d, int I, int I_shared, int k);
+cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMaps* shared, void* ws,
+                        cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- prefill GEMM
 constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)

@@ -10,7 +10,7 @@
 namespace bm {
 namespace {
 
-const char* const kNames[kKernelKinds] = {"route", "gemv_gateup", "gemv_down", "x_to_f16",
+const char* const kNames[kKernelKinds] = {"route", "decode", "unused", "x_to_f16",
                                           "gemm_gateup", "gemm_down", "combine", "prepack"};
 
 struct Pending {

@@ -26,12 +26,6 @@ constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kBasesSmemLimit = 96 * 1024;  // per-chunk bases kept in shared memory up to this size
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  if (bi < 0) return i >= 0;
-  if (i < 0) return false;
-  return v > bv || (v == bv && i < bi);
-}
-
 // kPL: logits per lane (E <= 32 * kPL).
 template <int kPL>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E,
@@ -64,50 +58,50 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   for (int tl = warp; tl < ntok; tl += kRouteWarps) {
     const int t = t0 + tl;
     const float* row = logits + static_cast<size_t>(t) * E;
-    float v[kPL];
+    // Monotone 32-bit keys: a larger float gives a larger unsigned key.  -0.0
+    // becomes +0.0 first, so equal floats always get equal keys and the tie
+    // goes to the lower expert index, as with a float comparison.
+    uint32_t key[kPL];
     uint32_t taken = 0;
     bool finite = true;
 #pragma unroll
     for (int c = 0; c < kPL; ++c) {
       const int e = lane + 32 * c;
       const bool in = e < E;
-      v[c] = in ? __ldg(row + e) : 0.0f;
-      finite &= !in || isfinite(v[c]);
+      float v = in ? __ldg(row + e) : 0.0f;
+      finite &= !in || isfinite(v);
+      if (v == 0.0f) v = 0.0f;
+      const uint32_t u = __float_as_uint(v);
+      key[c] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
       if (!in) taken |= 1u << c;
     }
     if (!__all_sync(0xffffffffu, finite)) record_status(&hdr->status, MOE_ERR_NONFINITE);
 
-    float sel_v = 0.0f;  // lane j keeps the j-th selected logit
+    uint32_t sel_key = 0;  // lane j keeps the j-th selected key
     int sel_i = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = 0.0f;
-      int bi = -1;
+      // lane-local best: largest key, lowest index among equal keys
+      uint32_t bk = 0;
+      int bi = 0x7FFFFFFF;
 #pragma unroll
       for (int c = 0; c < kPL; ++c) {
-        if (!((taken >> c) & 1u)) {
-          const int e = lane + 32 * c;
-          if (better(v[c], e, bv, bi)) {
-            bv = v[c];
-            bi = e;
-          }
+        if (!((taken >> c) & 1u) && (key[c] > bk || bi == 0x7FFFFFFF)) {
+          bk = key[c];
+          bi = lane + 32 * c;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (better(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      // bi is now identical in every lane
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi == 0x7FFFFFFF ? 0u : bk);
+      const int win = static_cast<int>(
+          __reduce_min_sync(0xffffffffu, (bi != 0x7FFFFFFF && bk == kmax) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu));
+      if ((win & 31) == lane) taken |= 1u << (win >> 5);
       if (lane == j) {
-        sel_v = bv;
-        sel_i = bi;
+        sel_key = kmax;
+        sel_i = win;
       }
     }
+    // back from key to float
+    const uint32_t su = (sel_key & 0x80000000u) ? (sel_key & 0x7FFFFFFFu) : ~sel_key;
+    const float sel_v = __uint_as_float(su);
     // weights: exp(l_j - l_max) in fp64, summed in selection order, one rounding to fp32
     const float top = __shfl_sync(0xffffffffu, sel_v, 0);
     const double ex = (lane < k) ? exp(static_cast<double>(sel_v) - static_cast<double>(top)) : 0.0;

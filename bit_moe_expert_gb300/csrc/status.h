@@ -10,9 +10,11 @@ namespace bm {
 // Every workspace starts with this header (256 bytes, so what follows stays
 // 256-byte aligned).
 struct WsHeader {
-  uint32_t status;  // first device-side error (moe_status), 0 = none
-  uint32_t ticket;  // arrival counter of the routing kernel; reset by its last CTA
-  uint32_t pad[62];
+  uint32_t status;     // first device-side error (moe_status), 0 = none
+  uint32_t ticket;     // arrival counter of the routing kernel; reset by its last CTA
+  uint32_t bar_count;  // grid barrier of the decode kernel: arrivals in this round
+  uint32_t bar_gen;    // grid barrier of the decode kernel: completed rounds
+  uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 
