@@ -224,7 +224,7 @@ class DecodeWorkload(Workload):
             self.logits_host.append(lh)
             self.X.append(torch.from_numpy(xh.view(np.int16)).to(dev))
             self.logits.append(torch.from_numpy(lh).to(dev))
-        self.block_rows = 128
+        self.block_rows = 96
         self.r = bm.Routing.empty(self.T, cfg.E, cfg.k, self.block_rows, dev)
         self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(self.T, cfg.E, cfg.k), dev)
         self.ws_f = bm.workspace(bm.moe_forward_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
@@ -336,7 +336,7 @@ class PrefillWorkload(Workload):
         self.logits_host = [synth.draw_logits(cfg, cfg.T, l) for l in range(self.sets)]
         self.X = torch.from_numpy(self.X_host.view(np.int16)).to(dev)
         self.logits = [torch.from_numpy(x).to(dev) for x in self.logits_host]
-        self.block_rows = 128
+        self.block_rows = 96
         C = self.chunk
         self.r = bm.Routing.empty(C, cfg.E, cfg.k, self.block_rows, dev)
         self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(C, cfg.E, cfg.k), dev)

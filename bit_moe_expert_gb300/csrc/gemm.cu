@@ -38,26 +38,37 @@ namespace bm {
 
 namespace {
 
-constexpr int kThreads = 448;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+// Warp roles (27 warps).
+constexpr int kProducerWarp = 0;   // TMA of codes and group parameters; cp.async gather of the token tile
+constexpr int kMmaWarp0 = 1;       // two MMA issuers (warps 1 and 2)
+constexpr int kEpiWarp0 = 3;       // eight epilogue warps (3..10)
+constexpr int kEpiWarps = 8;
+constexpr int kDqWarp0 = 11;       // sixteen dequantisation warps (11..26)
+constexpr int kDqWarps = 16;
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 
 template <bool kGateUp>
 struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
   static constexpr int kStages = kGateUp ? 6 : 8;
-  static constexpr int kAStages = kGateUp ? 4 : 8;
+  static constexpr int kAStages = kGateUp ? 2 : 4;
   static constexpr int kACols = 32 * kMats;  // 64 fp16 per lane per matrix = 32 columns
-  static constexpr int kAccCols = kMats * kGemmBN;
-  static constexpr int kAccBufs = kGateUp ? 1 : 2;
-  static constexpr int kABase = kAccBufs * kAccCols;
+  // two accumulator buffers of two halves each: gate|up (gate/up GEMM) or the
+  // even|odd k-block partial sums (down GEMM)
+  static constexpr int kAccBufCols = 2 * kGemmBN;
+  static constexpr int kABase = 2 * kAccBufCols;
   static_assert(kABase + kAStages * kACols <= static_cast<int>(kTmemCols), "TMEM budget");
-  static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to 128 rows x 64 fp16 (128-byte swizzle)
+  // the down GEMM splits stages between its two issuers by parity; the stage
+  // and A-stage rings must then agree on parity
+  static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "stage rings must have even length");
+  static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to kGemmBN rows x 64 fp16 (128-byte swizzle)
   static constexpr int kQBytes = kGemmBM * 32;   // 128 rows x 8 code words (32-byte swizzle)
   static constexpr int kSBBytes = kGemmBM * 4;
   static constexpr int kStageBytes = ((kBBytes + kMats * (kQBytes + kSBBytes)) + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
+  static constexpr int kEmptyArrivals = kDqWarps + (kGateUp ? 2 : 1);  // dequant warps + MMA commits
+  static constexpr int kAEmptyArrivals = kGateUp ? 2 : 1;
 };
 
 struct Item {
@@ -105,8 +116,8 @@ __device__ __forceinline__ int tile_n(int rows) { return max(16, (rows + 15) & ~
 // 8-bit bf16 scale); otherwise it is rounded once.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* out) {
   const uint32_t w4 = w >> 4;
-  const uint32_t magic = 0x64006400u;      // f16 pair (1024, 1024): a code in the low mantissa bits reads 1024 + q
-  const uint32_t one = 0x3C003C00u;        // f16 pair (1, 1)
+  const uint32_t magic = 0x64006400u;        // f16 pair (1024, 1024): a code in the low mantissa bits reads 1024 + q
+  const uint32_t one = 0x3C003C00u;          // f16 pair (1, 1)
   const uint32_t minus_magic = 0xE400E400u;  // f16 pair (-1024, -1024)
   const uint32_t sel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};
 #pragma unroll
@@ -124,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap sb0_r, const __grid_constant__ CUtensorMap sb1_r,
                     const __grid_constant__ CUtensorMap q0_s, const __grid_constant__ CUtensorMap q1_s,
                     const __grid_constant__ CUtensorMap sb0_s, const __grid_constant__ CUtensorMap sb1_s,
-                    const __grid_constant__ CUtensorMap act_r, const __grid_constant__ CUtensorMap act_s,
                     GemmArgs a) {
   using C = Cfg<kGateUp>;
   extern __shared__ uint8_t smem_raw[];
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = a_empty + C::kAStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -146,31 +156,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 8 + 1);  // 8 dequantisation warps + the MMA commit
+      mbar_init(&full[i], 1 + 32);  // the producer's expect_tx arrival + one cp.async arrival per lane
+      mbar_init(&empty[i], C::kEmptyArrivals);
     }
     for (int i = 0; i < C::kAStages; ++i) {
-      mbar_init(&a_full[i], 8);
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_full[i], kDqWarps);
+      mbar_init(&a_empty[i], C::kAEmptyArrivals);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_full[i], 2);  // one commit per MMA issuer
+      mbar_init(&acc_empty[i], kEpiWarps);
     }
-    mbar_init(done, 1);
+    mbar_init(&done[0], 1);
+    mbar_init(&done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&q0_r);
     tma_prefetch_desc(&sb0_r);
-    tma_prefetch_desc(&act_r);
     if (kGateUp) {
       tma_prefetch_desc(&q1_r);
       tma_prefetch_desc(&sb1_r);
     }
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -179,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  pdl_wait();  // routing and (for the down GEMM) h come from earlier kernels
+  pdl_wait();  // routing, X (and for the down GEMM, h) come from earlier kernels
   pdl_launch_dependents();
 
   Sched s;
@@ -213,19 +223,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mq1 = m.shared ? &q1_s : &q1_r;
       const CUtensorMap* msb0 = m.shared ? &sb0_s : &sb0_r;
       const CUtensorMap* msb1 = m.shared ? &sb1_s : &sb1_r;
-      const CUtensorMap* mact = m.shared ? &act_s : &act_r;
-      // Token rows of the tile, loaded once per item: lane g owns rows 4g..4g+3
-      // (the gather coordinates; rows past the tile read row T, out of range,
-      // which TMA zero-fills).
-      int tok[4] = {a.T, a.T, a.T, a.T};
-      if (kGateUp) {
+      // Token tile rows owned by this lane: L, L+32, L+64.  Source row base
+      // addresses, or null for a padding row (zero-filled).
+      const uint16_t* act = kGateUp ? a.Xh : (m.shared ? a.h_shared : a.h_routed);
+      const int act_cols = kGateUp ? a.d : (m.shared ? a.I_shared : a.I);
+      const uint8_t* src_row[kGemmBN / 32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = lane * 4 + i;
-          if (p < m.rows) tok[i] = m.shared ? m.row0 + p : __ldg(a.perm + m.row0 + p) / a.k;
+      for (int i = 0; i < kGemmBN / 32; ++i) {
+        const int r = lane + 32 * i;
+        src_row[i] = nullptr;
+        if (r < m.rows) {
+          int row;
+          if (kGateUp)
+            row = m.shared ? m.row0 + r : __ldg(a.perm + m.row0 + r) / a.k;
+          else
+            row = m.row0 + r;
+          src_row[i] = reinterpret_cast<const uint8_t*>(act + static_cast<size_t>(row) * act_cols);
         }
       }
-      const uint32_t bytes = C::kMats * (C::kQBytes + C::kSBBytes) + bn * 128;
+      const uint32_t tma_bytes = C::kMats * (C::kQBytes + C::kSBBytes);
       for (int kb = 0; kb < m.nk && ok; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           fail();
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* q_tile = st + C::kBBytes;
         uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], bytes);
+          mbar_arrive_expect_tx(&full[stage], tma_bytes);
           tma_load_3d(q_tile, mq0, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
@@ -247,14 +263,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         }
-        __syncwarp();  // the expected byte count is registered before any row load can complete
-        if (kGateUp) {
-          if (lane < bn / 4)
-            tma_gather4(b_tile + lane * 512, mact, &full[stage], kb * 64, tok[0], tok[1], tok[2], tok[3]);
-        } else {
-          if (lane < bn / 16) tma_load_2d(b_tile + lane * 2048, mact, &full[stage], kb * 64, m.row0 + lane * 16);
+        // token tile: 128-byte rows (64 fp16 of this k-block), 16-byte chunks
+        // placed with the 128-byte swizzle the MMA descriptor expects
+#pragma unroll
+        for (int i = 0; i < kGemmBN / 32; ++i) {
+          const int r = lane + 32 * i;
+          if (r < bn) {
+            uint8_t* drow = b_tile + r * 128;
+            const uint8_t* srow = src_row[i] ? src_row[i] + kb * 128 : reinterpret_cast<const uint8_t*>(act);
+            const uint32_t nbytes = src_row[i] ? 16u : 0u;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cp_async16(drow + ((c ^ (r & 7)) << 4), srow + c * 16, nbytes);
+          }
         }
-        __syncwarp();
+        cp_async_arrive(&full[stage]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
@@ -268,8 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&full[i], (last_parity >> i) & 1u, nullptr)) record_status(a.status, MOE_ERR_TIMEOUT);
         }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+    __syncwarp();
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    // ------------------------------------------------------------ MMA issuers
+    // gate/up: issuer 0 multiplies the gate tile, issuer 1 the up tile, both
+    // over every stage.  down: each issuer owns the stages (and A stages) of
+    // one parity and accumulates its k-blocks into its own half of the buffer;
+    // a fixed stage-to-issuer map means every issuer waits on every phase of
+    // the barriers it uses, so no wait can mistake an old phase for the next.
+    const int who = warp - kMmaWarp0;
     int stage = 0, astage = 0, accb = 0;
     uint32_t phase = 0, aphase = 0, accphase = 0;
     bool ok = true;
@@ -278,34 +307,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!m.ok) continue;
       const int bn = tile_n(m.rows);
       const uint32_t idesc = idesc_f16_f32(kGemmBM, bn);
-      const int ab = kGateUp ? 0 : accb;
-      if (!mbar_wait(&acc_empty[ab], accphase ^ 1, abort_flag)) {
+      if (!mbar_wait(&acc_empty[accb], accphase ^ 1, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after();
-      const uint32_t d0 = tmem + ab * C::kAccCols;
+      const uint32_t d = tmem + accb * C::kAccBufCols + who * kGemmBN;
+      bool first = true;
       for (int kb = 0; kb < m.nk; ++kb) {
-        if (!mbar_wait(&a_full[astage], aphase, abort_flag) || !mbar_wait(&full[stage], phase, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t b_addr = smem_u32(stages + stage * C::kStageBytes);
-          const uint32_t a0 = tmem + C::kABase + astage * C::kACols;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128_kmajor(b_addr + kk * 32);
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_ts(d0, a0 + kk * 8, bdesc, idesc, acc);
-            if (kGateUp) tc_mma_ts(d0 + kGemmBN, a0 + 32 + kk * 8, bdesc, idesc, acc);
+        const bool mine = kGateUp || ((stage & 1) == who);
+        if (mine) {
+          if (!mbar_wait(&a_full[astage], aphase, abort_flag) || !mbar_wait(&full[stage], phase, abort_flag)) {
+            fail();
+            ok = false;
+            break;
           }
-          tc_commit(&empty[stage]);
-          tc_commit(&a_empty[astage]);
+          fence_proxy_async_smem();  // the token tile was written by cp.async (generic proxy)
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t b_addr = smem_u32(stages + stage * C::kStageBytes);
+            const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 : 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              tc_mma_ts(d, a0 + kk * 8, smem_desc_sw128_kmajor(b_addr + kk * 32), idesc,
+                        (first && kk == 0) ? 0u : 1u);
+            }
+            tc_commit(&empty[stage]);
+            tc_commit(&a_empty[astage]);
+          }
+          __syncwarp();
+          first = false;
         }
-        __syncwarp();
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
@@ -316,31 +348,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&acc_full[ab]);
+      if (lane == 0) tc_commit(&acc_full[accb]);  // arrives at once if this issuer had no k-block
       __syncwarp();
-      if (kGateUp) {
-        accphase ^= 1;
-      } else if (++accb == 2) {
+      if (++accb == 2) {
         accb = 0;
         accphase ^= 1;
       }
     }
     // all MMAs issued by this thread have completed before TMEM is released
     if (lane == 0) {
-      tc_commit(done);
-      if (!mbar_wait(done, 0, nullptr)) record_status(a.status, MOE_ERR_TIMEOUT);
+      tc_commit(&done[who]);
+      if (!mbar_wait(&done[who], 0, nullptr)) record_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp >= kDqWarp0) {
     // ------------------------------------------------------------ dequantisation
+    const int dq = warp - kDqWarp0;
     const int lanegrp = warp & 3;
-    const int row = lanegrp * 32 + lane;             // weight row inside the tile = TMEM lane
-    const int mat = kGateUp ? (warp >> 2) : 0;       // gate/up: which matrix
-    const int half = warp >> 2;                      // down: which 32 columns of the group
+    const int row = lanegrp * 32 + lane;  // weight row inside the tile = TMEM lane
+    const int part = dq >> 2;             // gate/up: (matrix, 32-column half); down: 16-column quarter
+    const int mat = kGateUp ? (part >> 1) : 0;
+    const int swz = (row >> 2) & 1;
     int stage = 0, astage = 0;
     uint32_t phase = 0, aphase = 0;
     bool ok = true;
-    const int swz = (row >> 2) & 1;
     for (int it = blockIdx.x; it < s.n_total && ok; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
@@ -355,33 +386,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes;
         const uint32_t sbv =
             *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes + mat * C::kSBBytes + row * 4);
-        const float sf = __uint_as_float(sbv << 16);          // bf16 -> fp32 is exact
+        const float sf = __uint_as_float(sbv << 16);  // bf16 -> fp32 is exact
         const float bf = __uint_as_float(sbv & 0xFFFF0000u);
         const uint32_t s2 = f32x2_to_f16x2(sf, sf);
         const uint32_t b2 = f32x2_to_f16x2(bf, bf);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols;
         if constexpr (kGateUp) {
-          const uint4 wa = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((0 ^ swz) * 16));
-          const uint4 wb = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((1 ^ swz) * 16));
+          const int half = part & 1;  // words 4*half .. 4*half+3 = columns 32*half .. 32*half+31
+          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((half ^ swz) << 4));
           uint32_t v[16];
-          dequant_word(wa.x, s2, b2, v + 0);
-          dequant_word(wa.y, s2, b2, v + 4);
-          dequant_word(wa.z, s2, b2, v + 8);
-          dequant_word(wa.w, s2, b2, v + 12);
-          tmem_st16(taddr + mat * 32, v);
-          dequant_word(wb.x, s2, b2, v + 0);
-          dequant_word(wb.y, s2, b2, v + 4);
-          dequant_word(wb.z, s2, b2, v + 8);
-          dequant_word(wb.w, s2, b2, v + 12);
-          tmem_st16(taddr + mat * 32 + 16, v);
+          dequant_word(w.x, s2, b2, v + 0);
+          dequant_word(w.y, s2, b2, v + 4);
+          dequant_word(w.z, s2, b2, v + 8);
+          dequant_word(w.w, s2, b2, v + 12);
+          tmem_st16(taddr + mat * 32 + half * 16, v);
         } else {
-          const uint4 wv = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((half ^ swz) * 16));
-          uint32_t v[16];
-          dequant_word(wv.x, s2, b2, v + 0);
-          dequant_word(wv.y, s2, b2, v + 4);
-          dequant_word(wv.z, s2, b2, v + 8);
-          dequant_word(wv.w, s2, b2, v + 12);
-          tmem_st16(taddr + half * 16, v);
+          const int quarter = part;  // words 2q, 2q+1 = columns 16q .. 16q+15
+          const uint2 w = *reinterpret_cast<const uint2*>(q_tile + row * 32 + (((quarter >> 1) ^ swz) << 4) +
+                                                          ((quarter & 1) << 3));
+          uint32_t v[8];
+          dequant_word(w.x, s2, b2, v + 0);
+          dequant_word(w.y, s2, b2, v + 4);
+          tmem_st8(taddr + quarter * 8, v);
         }
         tc_wait_st();
         tc_fence_before();
@@ -402,10 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ep = warp - kEpiWarp0;
     const int lanegrp = warp & 3;
+    const int colhalf = ep >> 2;  // this warp handles columns [48*colhalf, 48*colhalf + 48)
     const int row = lanegrp * 32 + lane;
     int accb = 0;
     uint32_t accphase = 0;
+    uint32_t kcount = 0;  // k-blocks of the items before this one (sets which issuer took a lone k-block)
     for (int it = blockIdx.x; it < s.n_total; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) {
@@ -413,18 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int bn = tile_n(m.rows);
-      const int ab = kGateUp ? 0 : accb;
-      if (!mbar_wait(&acc_full[ab], accphase, abort_flag)) {
+      const int c_begin = colhalf * (kGemmBN / 2);
+      const int c_end = min(bn, c_begin + kGemmBN / 2);
+      if (!mbar_wait(&acc_full[accb], accphase, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + ab * C::kAccCols;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + accb * C::kAccBufCols;
       const int n = m.mt * kGemmBM + row;
-      if (kGateUp) {
+      if constexpr (kGateUp) {
         const int Icur = m.shared ? a.I_shared : a.I;
         uint16_t* H = m.shared ? a.h_shared : a.h_routed;
-        for (int c0 = 0; c0 < bn; c0 += 16) {
+        bool range_ok = true;
+        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
           uint32_t g[16], u[16];
           tmem_ld16(tbase + c0, g);
           tmem_ld16(tbase + kGemmBN + c0, u);
@@ -434,25 +465,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 16; ++c) {
               if (c0 + c < m.rows) {
                 const float gv = __uint_as_float(g[c]);
-                const float uv = __uint_as_float(u[c]);
-                const float h = gv / (1.0f + expf(-gv)) * uv;
-                if (!(fabsf(h) <= 65504.0f)) record_status(a.status, MOE_ERR_UNSUPPORTED);
+                const float h = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
+                range_ok &= fabsf(h) <= 65504.0f;
                 H[static_cast<size_t>(m.row0 + c0 + c) * Icur + n] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }
         }
+        if (!range_ok) record_status(a.status, MOE_ERR_UNSUPPORTED);
       } else {
-        // destination slot and routing weight of each column, loaded once per
-        // item: lane L owns columns L, L+32, L+64, L+96
-        int slot[4];
-        float wt[4];
+        // destination slot and routing weight of this warp's columns, loaded
+        // once per item: lane L owns columns c_begin + L and c_begin + 32 + L
+        int slot[2];
+        float wt[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = lane + 32 * i;
+        for (int i = 0; i < 2; ++i) {
+          const int c = c_begin + lane + 32 * i;
           slot[i] = -1;
           wt[i] = 0.0f;
-          if (c < m.rows) {
+          if (c < c_end && c < m.rows) {
             const int p = m.row0 + c;
             if (m.shared) {
               slot[i] = p * (a.k + 1) + a.k;
@@ -468,40 +499,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        for (int c0 = 0; c0 < bn; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tbase + c0, v);
+        // both halves hold partial sums unless the item has one k-block, which
+        // the issuer of that stage parity took alone
+        const bool two = m.nk > 1;
+        const uint32_t h0 = two ? 0u : (kcount & 1u) * kGemmBN;
+        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tbase + h0 + c0, v0);
+          tmem_ld16(tbase + kGemmBN + c0, v1);
           tc_wait_ld();
-          const int grp = c0 >> 5;  // which register holds these columns (uniform in the warp)
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const int col = c0 + c;
-            const int src = col & 31;
-            int sl;
-            float wv;
-            if (grp == 0) {
-              sl = __shfl_sync(0xffffffffu, slot[0], src);
-              wv = __shfl_sync(0xffffffffu, wt[0], src);
-            } else if (grp == 1) {
-              sl = __shfl_sync(0xffffffffu, slot[1], src);
-              wv = __shfl_sync(0xffffffffu, wt[1], src);
-            } else if (grp == 2) {
-              sl = __shfl_sync(0xffffffffu, slot[2], src);
-              wv = __shfl_sync(0xffffffffu, wt[2], src);
-            } else {
-              sl = __shfl_sync(0xffffffffu, slot[3], src);
-              wv = __shfl_sync(0xffffffffu, wt[3], src);
-            }
-            if (n < a.d && sl >= 0) a.ypart[static_cast<size_t>(sl) * a.d + n] = wv * __uint_as_float(v[c]);
+            const int rel = c0 + c - c_begin;  // 0..47
+            const int src = rel & 31;
+            const int sl = rel < 32 ? __shfl_sync(0xffffffffu, slot[0], src) : __shfl_sync(0xffffffffu, slot[1], src);
+            const float wv = rel < 32 ? __shfl_sync(0xffffffffu, wt[0], src) : __shfl_sync(0xffffffffu, wt[1], src);
+            const float y = __uint_as_float(v0[c]) + (two ? __uint_as_float(v1[c]) : 0.0f);
+            if (n < a.d && sl >= 0) a.ypart[static_cast<size_t>(sl) * a.d + n] = wv * y;
           }
         }
       }
+      kcount += static_cast<uint32_t>(m.nk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
-      if (kGateUp) {
-        accphase ^= 1;
-      } else if (++accb == 2) {
+      if (lane == 0) mbar_arrive(&acc_empty[accb]);
+      if (++accb == 2) {
         accb = 0;
         accphase ^= 1;
       }
@@ -511,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // X (bf16) -> fp16 copy used as the tensor-core operand.  Values outside the
@@ -570,8 +592,8 @@ bool g_gemm_attr = false;
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
-                        cudaStream_t stream, bool pdl) {
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, cudaStream_t stream,
+                        bool pdl) {
   using CG = Cfg<true>;
   using CD = Cfg<false>;
   if (!g_gemm_attr) {
@@ -608,7 +630,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.dynamicSmemBytes = CG::kSmemBytes;
   timer_begin(kKGemmGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
-                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
+                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, a);
   timer_end(kKGemmGateUp, stream);
   if (err != cudaSuccess) return err;
 
@@ -616,8 +638,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.dynamicSmemBytes = CD::kSmemBytes;
   timer_begin(kKGemmDown, stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false>, routed->q_down, routed->q_down, routed->sb_down,
-                           routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
-                           act->h_shared, a);
+                           routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, a);
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 

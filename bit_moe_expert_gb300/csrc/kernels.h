@@ -72,7 +72,7 @@ cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMap
 // ---------------------------------------------------------------- prefill GEMM
 constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)
 constexpr int kGemmBK = 64;    // K per stage = one quantisation group
-constexpr int kGemmBN = 128;   // max tokens per tile (MMA N)
+constexpr int kGemmBN = 96;    // max tokens per tile (MMA N); two double-buffered accumulators fit TMEM
 
 struct GemmMaps {
   CUtensorMap q_gate, q_up, q_down;     // codes, box (8 words, 128 rows, 1), 32-byte swizzle
@@ -94,13 +94,7 @@ struct GemmArgs {
   int T, d, I, k, I_shared, E, num_sms, max_blocks;
 };
 
-struct GemmActMaps {
-  CUtensorMap x;         // Xh [T][d] fp16, box (64, 1), 128-byte swizzle (gather4)
-  CUtensorMap h_routed;  // H [A][I] fp16, box (64, 16), 128-byte swizzle
-  CUtensorMap h_shared;  // H [T][I_shared] fp16, box (64, 16), 128-byte swizzle
-};
-
-cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared,
-                        const GemmActMaps* act, cudaStream_t stream, bool pdl);
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, cudaStream_t stream,
+                        bool pdl);
 
 }  // namespace bm

@@ -183,16 +183,18 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  *   routed   E = routed->n_experts experts, I columns of intermediate
  *   shared   NULL, or one always-on expert (n_experts = 1) with I_shared
  *   r        the routing written by moe_route for the same T, E, k on this
- *            stream (block_rows <= 128)
+ *            stream; the tensor-core path (below) needs block_rows <= 96
+ *            and returns MOE_ERR_UNSUPPORTED otherwise
  * Preconditions: T >= 0 (T = 0 does nothing), d, I and I_shared multiples of
  * 64 (I_shared = 0 iff shared is NULL), 1 <= k <= min(E, 32), E <= 1024.
  * Path: T <= 4 runs the decode kernels (CUDA-core GEMV, every active expert's
  * bytes streamed once); larger T runs the grouped tensor-core GEMM (tcgen05,
  * dequantisation fused, SwiGLU and the weighted combine fused).  The
  * environment variable MOE_PATH=gemv|gemm overrides the choice (for A/B
- * measurements and tests).  Arithmetic: fp32 accumulation; on the GEMM path the
- * dequantised weights and the SwiGLU output are rounded to bf16 as tensor-core
- * operands; Y is rounded to bf16 once. */
+ * measurements and tests).  Arithmetic: fp32 accumulation; on the GEMM path X,
+ * the dequantised weights and the SwiGLU output are rounded to fp16 as
+ * tensor-core operands (a value outside the fp16 range is recorded as
+ * MOE_ERR_UNSUPPORTED); Y is rounded to bf16 once. */
 moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
                        const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y,
                        void* ws, size_t ws_bytes, moe_stream stream);

@@ -133,14 +133,14 @@ def test_forward_small(name, kw, path):
     cfg = synth.small_config(**kw)
     layer = synth.draw_layer(cfg)
     dl = G.DeviceLayer.from_host(layer)
-    r, _ = G.route_gpu(layer.logits, cfg.k, 128 if path == "gemm" else 32)
+    r, _ = G.route_gpu(layer.logits, cfg.k, 96 if path == "gemm" else 32)
     rh = G.routing_to_host(r)
     Y = dl.forward(r, path)
     Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, rh["ids"], rh["w"])
     G.assert_y_close(Y, Y64, f"{name}/{path}")
 
 
-@pytest.mark.parametrize("block_rows", [16, 32, 64, 100, 128])
+@pytest.mark.parametrize("block_rows", [1, 16, 32, 50, 64, 96])
 def test_forward_gemm_block_rows(block_rows):
     cfg = synth.small_config(T=200, d=256, E=8, k=2, I=128, I_shared=128)
     layer = synth.draw_layer(cfg)
@@ -150,6 +150,18 @@ def test_forward_gemm_block_rows(block_rows):
     Y = dl.forward(r, "gemm")
     Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, rh["ids"], rh["w"])
     G.assert_y_close(Y, Y64, f"block_rows={block_rows}")
+
+
+def test_forward_gemm_rejects_tiles_over_96_rows():
+    """The tensor-core path holds at most 96 tokens per tile; a routing made
+    with taller tiles is refused before any launch."""
+    cfg = synth.small_config(T=40, d=128, E=4, k=2, I=64, I_shared=0)
+    layer = synth.draw_layer(cfg)
+    dl = G.DeviceLayer.from_host(layer)
+    r, _ = G.route_gpu(layer.logits, cfg.k, 128)
+    with pytest.raises(bm.MoeError) as ei:
+        dl.forward(r, "gemm")
+    assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
 
 
 def test_forward_deterministic():
@@ -196,9 +208,9 @@ def test_forward_full_size_sampled(name):
     cfg = synth.CONFIGS[name]
     T = cfg.tokens_per_call
     dl = G.DeviceLayer.from_device_draw(cfg, 0, T)
-    r, _ = G.route_gpu(dl.logits, cfg.k, 128)
+    r, _ = G.route_gpu(dl.logits, cfg.k, 96)
     rh = G.routing_to_host(r)
-    G.assert_routing_equal(rh, oracle.route(dl.logits, cfg.k, 128))
+    G.assert_routing_equal(rh, oracle.route(dl.logits, cfg.k, 96))
     Y = dl.forward(r)  # the path moe_forward picks for this T
     sample = sorted({0, T - 1, T // 2, T // 3, (2 * T) // 3, 1 % T, 7 % T, 123 % T})
     for t in sample:
@@ -214,7 +226,7 @@ def test_full_size_gemv_and_gemm_agree(name):
     cfg = synth.CONFIGS[name]
     T = min(cfg.tokens_per_call, 4)
     dl = G.DeviceLayer.from_device_draw(cfg, 1, T)
-    r, _ = G.route_gpu(dl.logits, cfg.k, 128)
+    r, _ = G.route_gpu(dl.logits, cfg.k, 96)
     rh = G.routing_to_host(r)
     Yv = dl.forward(r, "gemv")
     Ym = dl.forward(r, "gemm")
