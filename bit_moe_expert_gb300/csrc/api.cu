@@ -50,6 +50,15 @@ bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuui
 }
 
 // group parameters sb [E][K/64][N] uint32
+// fp16 activations [rows][cols]: boxes of 64 columns (128 bytes) x kGemmBN
+// rows, 128-byte swizzle (the K-major operand layout of the tensor cores)
+bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kGemmBN)};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_rows,
                    cuuint32_t box_groups) {
   const int G = K / 64;
@@ -107,9 +116,9 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
   L.gemm_h_shared = o;
   o = round256(o + static_cast<size_t>(T) * I_shared * 2);
   L.gemm_ypart = o;
-  o = round256(o + static_cast<size_t>(T) * (k + 1) * d * 4);
+  o = round256(o + (A + static_cast<size_t>(T)) * d * 4);
   L.gemm_xh = o;
-  o = round256(o + static_cast<size_t>(T) * d * 2);
+  o = round256(o + (A + static_cast<size_t>(T)) * d * 2);
   L.total = o > gemv_end ? o : gemv_end;
   return L;
 }
@@ -265,7 +274,9 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   }
 
   if (r->block_rows < 1 || r->block_rows > kGemmBN) return MOE_ERR_UNSUPPORTED;
+  const int A = T * k;
   GemmMaps mr, ms;
+  GemmActMaps act;
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
   uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
@@ -274,18 +285,22 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
             encode_codes(&mr.q_down, routed->down.q, E, d, I, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
-            encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1);
+            encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
+            encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
   if (ok && shared)
     ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
          encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
          encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
          encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
-         encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1);
+         encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&
+         encode_act(&act.h_shared, hs, T, I_shared);
+  if (ok && !shared) act.h_shared = act.h_routed;  // never read without a shared expert
   if (!ok) return MOE_ERR_CUDA;
 
   GemmArgs a{};
   a.perm = r->perm;
+  a.inv_perm = r->inv_perm;
   a.block_map = r->block_map;
   a.num_blocks = r->num_blocks;
   a.w = r->w;
@@ -305,7 +320,7 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   a.num_sms = sm_count();
   a.max_blocks = moe_route_max_blocks(T, E, k, r->block_rows);
   if (a.num_sms <= 0) return MOE_ERR_CUDA;
-  if (launch_gemm(a, &mr, shared ? &ms : nullptr, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(a, &mr, shared ? &ms : nullptr, &act, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -46,6 +46,8 @@ constexpr int kEpiWarps = 8;
 constexpr int kDqWarp0 = 11;       // sixteen dequantisation warps (11..26)
 constexpr int kDqWarps = 16;
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr uint32_t kBarDequant = 1;   // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarEpilogue = 2;
 constexpr uint32_t kTmemCols = 512;
 
 template <bool kGateUp>
@@ -65,7 +67,8 @@ struct Cfg {
   static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to kGemmBN rows x 64 fp16 (128-byte swizzle)
   static constexpr int kQBytes = kGemmBM * 32;   // 128 rows x 8 code words (32-byte swizzle)
   static constexpr int kSBBytes = kGemmBM * 4;
-  static constexpr int kStageBytes = ((kBBytes + kMats * (kQBytes + kSBBytes)) + 1023) / 1024 * 1024;
+  static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
+  static constexpr int kStageBytes = (kStageTxBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
   static constexpr int kEmptyArrivals = kDqWarps + (kGateUp ? 2 : 1);  // dequant warps + MMA commits
   static constexpr int kAEmptyArrivals = kGateUp ? 2 : 1;
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap sb0_r, const __grid_constant__ CUtensorMap sb1_r,
                     const __grid_constant__ CUtensorMap q0_s, const __grid_constant__ CUtensorMap q1_s,
                     const __grid_constant__ CUtensorMap sb0_s, const __grid_constant__ CUtensorMap sb1_s,
-                    GemmArgs a) {
+                    const __grid_constant__ CUtensorMap act0, const __grid_constant__ CUtensorMap act1, GemmArgs a) {
   using C = Cfg<kGateUp>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1 + 32);  // the producer's expect_tx arrival + one cp.async arrival per lane
+      mbar_init(&full[i], 1);  // the producer's expect_tx arrival; the bytes complete the phase
       mbar_init(&empty[i], C::kEmptyArrivals);
     }
     for (int i = 0; i < C::kAStages; ++i) {
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&q0_r);
     tma_prefetch_desc(&sb0_r);
+    tma_prefetch_desc(&act0);
     if (kGateUp) {
       tma_prefetch_desc(&q1_r);
       tma_prefetch_desc(&sb1_r);
@@ -218,42 +222,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = blockIdx.x; it < s.n_total && ok; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
-      const int bn = tile_n(m.rows);
       const CUtensorMap* mq0 = m.shared ? &q0_s : &q0_r;
       const CUtensorMap* mq1 = m.shared ? &q1_s : &q1_r;
       const CUtensorMap* msb0 = m.shared ? &sb0_s : &sb0_r;
       const CUtensorMap* msb1 = m.shared ? &sb1_s : &sb1_r;
-      // Token tile rows owned by this lane: L, L+32, L+64.  Source row base
-      // addresses, or null for a padding row (zero-filled).
-      const uint16_t* act = kGateUp ? a.Xh : (m.shared ? a.h_shared : a.h_routed);
-      const int act_cols = kGateUp ? a.d : (m.shared ? a.I_shared : a.I);
-      const uint8_t* src_row[kGemmBN / 32];
-#pragma unroll
-      for (int i = 0; i < kGemmBN / 32; ++i) {
-        const int r = lane + 32 * i;
-        src_row[i] = nullptr;
-        if (r < m.rows) {
-          int row;
-          if (kGateUp)
-            row = m.shared ? m.row0 + r : __ldg(a.perm + m.row0 + r) / a.k;
-          else
-            row = m.row0 + r;
-          src_row[i] = reinterpret_cast<const uint8_t*>(act + static_cast<size_t>(row) * act_cols);
-        }
-      }
-      const uint32_t tma_bytes = C::kMats * (C::kQBytes + C::kSBBytes);
-      for (int kb = 0; kb < m.nk && ok; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        uint8_t* st = stages + stage * C::kStageBytes;
-        uint8_t* b_tile = st;
-        uint8_t* q_tile = st + C::kBBytes;
-        uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], tma_bytes);
+      // token tile: kGemmBN rows of the activation tensor from the item's
+      // first row (rows past the item belong to the next item or lie past the
+      // end of the tensor and are zero-filled; their MMA columns are ignored)
+      const CUtensorMap* mb = (!kGateUp && m.shared) ? &act1 : &act0;
+      const int brow = (kGateUp && m.shared) ? a.T * a.k + m.row0 : m.row0;
+      if (lane == 0) {
+        for (int kb = 0; kb < m.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          uint8_t* st = stages + stage * C::kStageBytes;
+          uint8_t* q_tile = st + C::kBBytes;
+          uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageTxBytes);
+          tma_load_2d(st, mb, &full[stage], kb * 64, brow);
           tma_load_3d(q_tile, mq0, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
@@ -262,26 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        }
-        // token tile: 128-byte rows (64 fp16 of this k-block), 16-byte chunks
-        // placed with the 128-byte swizzle the MMA descriptor expects
-#pragma unroll
-        for (int i = 0; i < kGemmBN / 32; ++i) {
-          const int r = lane + 32 * i;
-          if (r < bn) {
-            uint8_t* drow = b_tile + r * 128;
-            const uint8_t* srow = src_row[i] ? src_row[i] + kb * 128 : reinterpret_cast<const uint8_t*>(act);
-            const uint32_t nbytes = src_row[i] ? 16u : 0u;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) cp_async16(drow + ((c ^ (r & 7)) << 4), srow + c * 16, nbytes);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
           }
         }
-        cp_async_arrive(&full[stage]);
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     // never leave while a load into this CTA's shared memory may be in flight
     if (lane == 0) {
@@ -322,7 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          fence_proxy_async_smem();  // the token tile was written by cp.async (generic proxy)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t b_addr = smem_u32(stages + stage * C::kStageBytes);
@@ -376,8 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
       for (int kb = 0; kb < m.nk; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&a_empty[astage], aphase ^ 1, abort_flag)) {
-          fail();
+        // one warp polls the barriers; the other fifteen sleep in a named barrier
+        bool bad = false;
+        if (dq == 0) {
+          bad = !mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&a_empty[astage], aphase ^ 1, abort_flag);
+          if (bad && lane == 0) fail();
+        }
+        if (bar_sync_or(kBarDequant, kDqWarps * 32, bad)) {
           ok = false;
           break;
         }
@@ -444,78 +424,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bn = tile_n(m.rows);
       const int c_begin = colhalf * (kGemmBN / 2);
       const int c_end = min(bn, c_begin + kGemmBN / 2);
-      if (!mbar_wait(&acc_full[accb], accphase, abort_flag)) {
-        fail();
-        break;
+      bool bad = false;
+      if (ep == 0) {
+        bad = !mbar_wait(&acc_full[accb], accphase, abort_flag);
+        if (bad && lane == 0) fail();
       }
+      if (bar_sync_or(kBarEpilogue, kEpiWarps * 32, bad)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + accb * C::kAccBufCols;
       const int n = m.mt * kGemmBM + row;
       if constexpr (kGateUp) {
+        // h = SiLU(gate) * up, rounded to fp16 (the down GEMM's operand);
+        // rows of h follow the item's rows (permuted order, or token order for
+        // the shared expert)
         const int Icur = m.shared ? a.I_shared : a.I;
-        uint16_t* H = m.shared ? a.h_shared : a.h_routed;
+        uint16_t* H = (m.shared ? a.h_shared : a.h_routed) + static_cast<size_t>(m.row0) * Icur + n;
+        const int c_valid = min(c_end, m.rows);
         bool range_ok = true;
-        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tbase + c0, g);
-          tmem_ld16(tbase + kGemmBN + c0, u);
+        for (int c0 = c_begin; c0 < c_end; c0 += 8) {
+          uint32_t g[8], u[8];
+          tmem_ld8(tbase + c0, g);
+          tmem_ld8(tbase + kGemmBN + c0, u);
           tc_wait_ld();
           if (n < Icur) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              if (c0 + c < m.rows) {
+            for (int c = 0; c < 8; ++c) {
+              if (c0 + c < c_valid) {
                 const float gv = __uint_as_float(g[c]);
                 const float h = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
                 range_ok &= fabsf(h) <= 65504.0f;
-                H[static_cast<size_t>(m.row0 + c0 + c) * Icur + n] = __half_as_ushort(__float2half_rn(h));
+                H[static_cast<size_t>(c0 + c) * Icur] = __half_as_ushort(__float2half_rn(h));
               }
             }
           }
         }
         if (!range_ok) record_status(a.status, MOE_ERR_UNSUPPORTED);
       } else {
-        // destination slot and routing weight of this warp's columns, loaded
-        // once per item: lane L owns columns c_begin + L and c_begin + 32 + L
-        int slot[2];
-        float wt[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = c_begin + lane + 32 * i;
-          slot[i] = -1;
-          wt[i] = 0.0f;
-          if (c < c_end && c < m.rows) {
-            const int p = m.row0 + c;
-            if (m.shared) {
-              slot[i] = p * (a.k + 1) + a.k;
-              wt[i] = 1.0f;
-            } else {
-              const int asg = __ldg(a.perm + p);
-              if (asg >= 0 && asg < a.T * a.k) {
-                slot[i] = asg + asg / a.k;
-                wt[i] = __ldg(a.w + asg);
-              } else {
-                record_status(a.status, MOE_ERR_INVALID_ARG);
-              }
-            }
-          }
-        }
-        // both halves hold partial sums unless the item has one k-block, which
-        // the issuer of that stage parity took alone
-        const bool two = m.nk > 1;
+        // expert output rows: routed items in permuted order (row p of the
+        // routing), shared-expert items after them in token order; the combine
+        // kernel applies the routing weights and gathers rows back to tokens
+        const bool two = m.nk > 1;  // both halves hold partial sums unless the item has one k-block
         const uint32_t h0 = two ? 0u : (kcount & 1u) * kGemmBN;
-        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tbase + h0 + c0, v0);
-          tmem_ld16(tbase + kGemmBN + c0, v1);
+        const size_t row_base = (m.shared ? static_cast<size_t>(a.T) * a.k : 0) + m.row0;
+        float* Yp = a.ypart + row_base * a.d + n;
+        const int c_valid = min(c_end, m.rows);
+        for (int c0 = c_begin; c0 < c_end; c0 += 8) {
+          uint32_t v0[8], v1[8];
+          tmem_ld8(tbase + h0 + c0, v0);
+          tmem_ld8(tbase + kGemmBN + c0, v1);
           tc_wait_ld();
+          if (n < a.d) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int rel = c0 + c - c_begin;  // 0..47
-            const int src = rel & 31;
-            const int sl = rel < 32 ? __shfl_sync(0xffffffffu, slot[0], src) : __shfl_sync(0xffffffffu, slot[1], src);
-            const float wv = rel < 32 ? __shfl_sync(0xffffffffu, wt[0], src) : __shfl_sync(0xffffffffu, wt[1], src);
-            const float y = __uint_as_float(v0[c]) + (two ? __uint_as_float(v1[c]) : 0.0f);
-            if (n < a.d && sl >= 0) a.ypart[static_cast<size_t>(sl) * a.d + n] = wv * y;
+            for (int c = 0; c < 8; ++c)
+              if (c0 + c < c_valid)
+                Yp[static_cast<size_t>(c0 + c) * a.d] = __uint_as_float(v0[c]) + (two ? __uint_as_float(v1[c]) : 0.0f);
           }
         }
       }
@@ -536,45 +498,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// X (bf16) -> fp16 copy used as the tensor-core operand.  Values outside the
-// fp16 range are recorded as MOE_ERR_UNSUPPORTED.
-__global__ void x_to_f16_kernel(const uint16_t* __restrict__ X, size_t n8, uint16_t* __restrict__ Xh,
-                                uint32_t* status) {
+// The gate/up GEMM's token operand: fp16 rows of X in the routing's permuted
+// order (row p = X[perm[p] / k]), followed by the T rows of X in token order
+// when there is a shared expert.  Values outside the fp16 range are recorded
+// as MOE_ERR_UNSUPPORTED.  One warp per row, 16-byte loads and stores.
+__global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, int T, int d,
+                                int k, int rows, uint16_t* __restrict__ Xg, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
-  bool range_ok = true;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(X)[i];
-    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(in[j] << 16);
-      const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
-      range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
-      out[j] = f32x2_to_f16x2(lo, hi);
+  const int lane = threadIdx.x & 31;
+  const int A = T * k;
+  const int d8 = d / 8;
+  bool range_ok = true, idx_ok = true;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
+    int t = r - A;
+    if (r < A) t = __ldg(perm + r) / k;
+    if (t < 0 || t >= T) {
+      idx_ok = false;
+      continue;
     }
-    reinterpret_cast<uint4*>(Xh)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<size_t>(t) * d);
+    uint4* dst = reinterpret_cast<uint4*>(Xg + static_cast<size_t>(r) * d);
+    for (int c = lane; c < d8; c += 32) {
+      const uint4 v = src[c];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(in[j] << 16);
+        const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
+        range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
+        out[j] = f32x2_to_f16x2(lo, hi);
+      }
+      dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
   }
   if (!range_ok) record_status(status, MOE_ERR_UNSUPPORTED);
+  if (!idx_ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
 
-// Y[t] = bf16( sum over the k routed slots and the shared slot )
-__global__ void combine_kernel(const float* __restrict__ ypart, int T, int d, int stride_slots, int slots,
-                               uint16_t* __restrict__ Y) {
+// Y[t] = bf16( sum_j w[t][j] * yexp[inv_perm[t*k + j]] + yexp[A + t] ): the
+// weighted top-k combine plus the shared expert, summed in slot order.
+__global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ inv_perm,
+                               const float* __restrict__ w, int T, int d, int k, int has_shared,
+                               uint16_t* __restrict__ Y, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
-  const size_t total4 = static_cast<size_t>(T) * d / 4;
+  const size_t A = static_cast<size_t>(T) * k;
+  const int d4 = d / 4;
+  const size_t total4 = static_cast<size_t>(T) * d4;
+  bool ok = true;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total4;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t e = i * 4;
-    const size_t t = e / d;
-    const size_t n = e % d;
-    const float4* src = reinterpret_cast<const float4*>(ypart + t * stride_slots * d + n);
-    float4 acc = src[0];
-    for (int j = 1; j < slots; ++j) {
-      const float4 v = src[static_cast<size_t>(j) * d / 4];
+    const size_t t = i / d4;
+    const int n = static_cast<int>(i - t * d4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int p = __ldg(inv_perm + t * k + j);
+      const float wj = __ldg(w + t * k + j);
+      if (p < 0 || static_cast<size_t>(p) >= A) {
+        ok = false;
+        continue;
+      }
+      const float4 v = *reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d + n);
+      acc.x = fmaf(wj, v.x, acc.x);
+      acc.y = fmaf(wj, v.y, acc.y);
+      acc.z = fmaf(wj, v.z, acc.z);
+      acc.w = fmaf(wj, v.w, acc.w);
+    }
+    if (has_shared) {
+      const float4 v = *reinterpret_cast<const float4*>(ypart + (A + t) * d + n);
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -584,16 +577,17 @@ __global__ void combine_kernel(const float* __restrict__ ypart, int T, int d, in
                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
     const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
                         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(Y + e) = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(Y + t * d + n) = make_uint2(lo, hi);
   }
+  if (!ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
 
 bool g_gemm_attr = false;
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, cudaStream_t stream,
-                        bool pdl) {
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
+                        cudaStream_t stream, bool pdl) {
   using CG = Cfg<true>;
   using CD = Cfg<false>;
   if (!g_gemm_attr) {
@@ -620,17 +614,17 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
     c2.gridDim = dim3(a.num_sms * 2);
     c2.blockDim = dim3(256);
     c2.dynamicSmemBytes = 0;
-    const size_t n8 = static_cast<size_t>(a.T) * a.d / 8;
-    timer_begin(kKToF16, stream);
-    cudaError_t e = cudaLaunchKernelEx(&c2, x_to_f16_kernel, a.X, n8, a.Xh, a.status);
-    timer_end(kKToF16, stream);
+    const int rows = a.T * a.k + (a.I_shared > 0 ? a.T : 0);
+    timer_begin(kKXGather, stream);
+    cudaError_t e = cudaLaunchKernelEx(&c2, x_gather_kernel, a.X, a.perm, a.T, a.d, a.k, rows, a.Xh, a.status);
+    timer_end(kKXGather, stream);
     if (e != cudaSuccess) return e;
   }
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CG::kSmemBytes;
   timer_begin(kKGemmGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
-                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, a);
+                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
   timer_end(kKGemmGateUp, stream);
   if (err != cudaSuccess) return err;
 
@@ -638,16 +632,17 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.dynamicSmemBytes = CD::kSmemBytes;
   timer_begin(kKGemmDown, stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false>, routed->q_down, routed->q_down, routed->sb_down,
-                           routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, a);
+                           routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
+                           act->h_shared, a);
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 
   cfg.gridDim = dim3(a.num_sms * 4);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  const int slots = a.k + (a.I_shared > 0 ? 1 : 0);
   timer_begin(kKCombine, stream);
-  err = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.ypart), a.T, a.d, a.k + 1, slots, a.Y);
+  err = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.ypart), a.inv_perm, a.w, a.T, a.d, a.k,
+                           a.I_shared > 0 ? 1 : 0, a.Y, a.status);
   timer_end(kKCombine, stream);
   return err;
 }

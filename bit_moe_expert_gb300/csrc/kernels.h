@@ -16,7 +16,7 @@ enum KernelKind {
   kKRoute = 0,
   kKGemvGateUp,  // the fused decode kernel (gate/up + down)
   kKGemvDown,    // reserved
-  kKToF16,
+  kKXGather,
   kKGemmGateUp,
   kKGemmDown,
   kKCombine,
@@ -81,20 +81,27 @@ struct GemmMaps {
 
 struct GemmArgs {
   const int32_t* perm;        // [A]
+  const int32_t* inv_perm;    // [A]
   const int32_t* block_map;   // [nb][3]
   const int32_t* num_blocks;  // [1]
   const float* w;             // [A]
-  float* ypart;               // [T][k+1][d] fp32 weighted expert outputs
+  float* ypart;               // [A + T][d] fp32 expert outputs: routed rows in permuted order, then shared rows
   uint16_t* h_routed;         // [A][I] fp16
   uint16_t* h_shared;         // [T][I_shared] fp16
   const uint16_t* X;          // [T][d] bf16 input
-  uint16_t* Xh;               // [T][d] fp16 copy (tensor-core operand)
+  uint16_t* Xh;               // [A + T][d] fp16 gathered rows of X (tensor-core operand)
   uint16_t* Y;                // [T][d] bf16
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms, max_blocks;
 };
 
-cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, cudaStream_t stream,
-                        bool pdl);
+struct GemmActMaps {
+  CUtensorMap x;         // gathered X [A + T][d] fp16, box (64, kGemmBN), 128-byte swizzle
+  CUtensorMap h_routed;  // H [A][I] fp16, box (64, kGemmBN), 128-byte swizzle
+  CUtensorMap h_shared;  // H [T][I_shared] fp16, same box
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
+                        cudaStream_t stream, bool pdl);
 
 }  // namespace bm

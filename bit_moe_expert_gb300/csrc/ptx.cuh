@@ -74,11 +74,29 @@ constexpr uint32_t kSleepHintNs = 20000;  // re-check the abort flag and the lim
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
-    if (abort && *abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if ((i & 15u) == 0) {  // the flag and the clock cost issue slots: look every 16 polls
+      if (abort && *abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
   }
+}
+
+// Named barrier with an OR-reduction: every one of the `nthreads` threads
+// (whole warps) that reach barrier `id` gets the OR of their predicates.
+// Warps blocked here take no issue slots, unlike warps polling an mbarrier.
+__device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -112,18 +130,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
       : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared through L2; src_bytes = 0 writes
-// zeros (a padding row) without reading global memory.
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-// Arrives on the mbarrier once all of this thread's earlier cp.async copies
-// have completed (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ------------------------------------------------------------------ PDL
@@ -196,6 +202,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
         "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr)
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
