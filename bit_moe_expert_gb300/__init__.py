@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NONFINITE"}
 
 # Every symbol the headers in include/ declare.
-EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_scales",
+EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
             "moe_forward_workspace_bytes",
             "moe_forward", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
@@ -64,6 +64,8 @@ def lib(path: Optional[str] = None):
         L.moe_device_sm_count.restype = C.c_int
         L.moe_prepack_bytes.restype = C.c_size_t
         L.moe_prepack_bytes.argtypes = [C.c_int, C.c_int, C.c_int]
+        L.moe_prepack_codes.restype = C.c_int
+        L.moe_prepack_codes.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.moe_prepack_scales.restype = C.c_int
         L.moe_prepack_scales.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.moe_route_max_blocks.restype = C.c_int
@@ -115,7 +117,8 @@ def _ptr(t) -> int:
 
 @dataclasses.dataclass
 class QMat:
-    """One stacked packed matrix on the device: q int32 [E][N][K/8], sb int32 [E][K/64][N]."""
+    """One stacked packed matrix on the device: q int32 [E][K/64][N][8] (group-major codes),
+    sb int32 [E][K/64][N]."""
     q: "object"
     sb: "object"
 
@@ -131,11 +134,11 @@ class Experts:
 
     @property
     def n_experts(self) -> int:
-        return int(self.gate.q.shape[0])
+        return int(self.gate.sb.shape[0])
 
     @property
     def I(self) -> int:
-        return int(self.gate.q.shape[1])
+        return int(self.gate.sb.shape[2])
 
     def _c(self) -> _Experts:
         return _Experts(self.gate._c(), self.up._c(), self.down._c(), self.n_experts)
@@ -189,6 +192,12 @@ def moe_device_sm_count() -> int:
 
 def moe_prepack_bytes(E: int, N: int, K: int) -> int:
     return int(lib().moe_prepack_bytes(E, N, K))
+
+
+def moe_prepack_codes(q, qp, stream=None) -> None:
+    """q int32 [E][N][K/8] (row-major codes) -> qp int32 [E][K/64][N][8] (group-major)."""
+    E, N, K8 = q.shape
+    _check("moe_prepack_codes", lib().moe_prepack_codes(_ptr(q), E, N, K8 * 8, _ptr(qp), _stream(stream)))
 
 
 def moe_prepack_scales(scale, bias, sb, stream=None) -> None:
@@ -273,8 +282,9 @@ def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
 
     ex maps "gate", "up", "down" to (q, scale, bias): q uint32/int32 [E][N][K/8],
     scale and bias uint16/int16 bf16 bits [E][N][K/64], as NumPy arrays or
-    torch tensors.  The group parameters are converted once with
-    moe_prepack_scales (a one-time layout change, like loading a checkpoint).
+    torch tensors.  Codes and group parameters are reordered once with
+    moe_prepack_codes and moe_prepack_scales (a one-time layout change, like
+    loading a checkpoint).
     """
     import numpy as np
     import torch
@@ -293,5 +303,8 @@ def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
         E, N, G = sd.shape
         sb = torch.empty((E, G, N), dtype=torch.int32, device=device)
         moe_prepack_scales(sd, bd, sb, stream)
-        mats[name] = QMat(qd, sb)
+        qp = torch.empty((E, G, N, 8), dtype=torch.int32, device=device)
+        moe_prepack_codes(qd, qp, stream)
+        del qd
+        mats[name] = QMat(qp, sb)
     return Experts(**mats)

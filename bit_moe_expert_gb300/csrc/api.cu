@@ -39,17 +39,39 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
   return r == CUDA_SUCCESS;
 }
 
-// codes q [E][N][K/8] uint32
-bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_words,
-                  cuuint32_t box_rows, CUtensorMapSwizzle sw) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(E)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 8) * 4, static_cast<cuuint64_t>(K / 8) * 4 * N};
-  const cuuint32_t box[3] = {box_words, box_rows, 1};
+// codes q [E][K/64][N][8] uint32 (group-major, moe_prepack_codes), seen as
+// a 3-D tensor [E*K/64][N][8]; a box covers box_rows rows of box_groups
+// consecutive groups
+bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_rows,
+                  cuuint32_t box_groups, CUtensorMapSwizzle sw) {
+  const int G = K / 64;
+  const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E) * G};
+  const cuuint64_t strides[2] = {32, static_cast<cuuint64_t>(N) * 32};
+  const cuuint32_t box[3] = {8, box_rows, box_groups};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, sw);
 }
 
-// group parameters sb [E][K/64][N] uint32
+// The same codes seen as [E*K/64][N/4][32]: 128-byte super-rows of four
+// consecutive rows of one group (N a multiple of 4); a box covers box_sr
+// super-rows of one group
+bool encode_codes_sr(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_sr) {
+  const int G = K / 64;
+  const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(N / 4), static_cast<cuuint64_t>(E) * G};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(N) * 32};
+  const cuuint32_t box[3] = {32, box_sr, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// group parameters sb [E][K/64][N] seen as [E*K/64][N/4][4]: a box covers
+// 4 * box_sr consecutive rows of one group
+bool encode_groups_sr(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_sr) {
+  const int G = K / 64;
+  const cuuint64_t dims[3] = {4, static_cast<cuuint64_t>(N / 4), static_cast<cuuint64_t>(E) * G};
+  const cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(N) * 4};
+  const cuuint32_t box[3] = {4, box_sr, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // fp16 activations [rows][cols]: boxes of 64 columns (128 bytes) x kGemmBN
 // rows, 128-byte swizzle (the K-major operand layout of the tensor cores)
 bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols) {
@@ -59,6 +81,7 @@ bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols) {
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// group parameters sb [E][K/64][N] uint32
 bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_rows,
                    cuuint32_t box_groups) {
   const int G = K / 64;
@@ -95,7 +118,7 @@ enum class Path { kGemv, kGemm };
 
 // Forward workspace: header, then one region used by either path.
 struct FwdLayout {
-  size_t gemv_h_routed, gemv_h_shared;              // fp32
+  size_t dec_part;                                           // fp32 partial outputs of the decode kernel
   size_t gemm_h_routed, gemm_h_shared, gemm_ypart, gemm_xh;  // fp16, fp16, fp32, fp16
   size_t total;
 };
@@ -105,11 +128,9 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
   const size_t A = static_cast<size_t>(T) * k;
   size_t o = sizeof(WsHeader);
   const size_t base = o;
-  L.gemv_h_routed = o;
-  o = round256(o + A * I * 4);
-  L.gemv_h_shared = o;
-  o = round256(o + static_cast<size_t>(T) * I_shared * 4);
-  const size_t gemv_end = o;
+  L.dec_part = o;
+  o = round256(o + (T <= kGemvMaxT ? decode_partial_bytes(T, d) : 0));
+  const size_t dec_end = o;
   o = base;
   L.gemm_h_routed = o;
   o = round256(o + A * I * 2);
@@ -119,7 +140,7 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
   o = round256(o + (A + static_cast<size_t>(T)) * d * 4);
   L.gemm_xh = o;
   o = round256(o + (A + static_cast<size_t>(T)) * d * 2);
-  L.total = o > gemv_end ? o : gemv_end;
+  L.total = o > dec_end ? o : dec_end;
   return L;
 }
 
@@ -156,6 +177,14 @@ int moe_device_sm_count(void) { return sm_count(); }
 size_t moe_prepack_bytes(int E, int N, int K) {
   if (E < 1 || N < 1 || K < 64 || K % 64) return 0;
   return static_cast<size_t>(E) * (K / 64) * N * 4;
+}
+
+moe_status moe_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, moe_stream stream) {
+  if (!q || !qp || E < 1 || N < 1 || K < 64 || K % 64 != 0 || !aligned16(q) || !aligned16(qp))
+    return MOE_ERR_INVALID_ARG;
+  if (launch_prepack_codes(q, E, N, K, qp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
@@ -234,32 +263,35 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     if (!std::strcmp(p, "gemv")) path = Path::kGemv;
     if (!std::strcmp(p, "gemm")) path = Path::kGemm;
   }
-  if (path == Path::kGemv && !gemv_supported(d, I, I_shared, k)) path = Path::kGemm;
+  if (path == Path::kGemv && !decode_supported(T, d, I, I_shared, k)) {
+    if (T > kGemvMaxT) return MOE_ERR_UNSUPPORTED;  // the decode kernel takes at most kGemvMaxT tokens
+    path = Path::kGemm;
+  }
 
   if (path == Path::kGemv) {
-    GemvMaps mr, ms;
-    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_codes(&mr.q_up, routed->up.q, E, I, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_codes(&mr.q_down, routed->down.q, E, d, I, 32, kGemvRowsDown, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemvRowsGU, d / 64) &&
-              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemvRowsGU, d / 64) &&
-              encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemvRowsDown, I / 64);
+    DecodeMaps mr, ms;
+    const int KB1 = d / 64;
+    const cuuint32_t bsr = static_cast<cuuint32_t>(decode_box_superrows(d));
+    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_codes(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_codes_sr(&mr.q_down, routed->down.q, E, d, I, bsr) &&
+              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, KB1) &&
+              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, KB1) &&
+              encode_groups_sr(&mr.sb_down, routed->down.sb, E, d, I, bsr);
     if (ok && shared)
-      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 32, kGemvRowsGU, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, 32, kGemvRowsDown,
-                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemvRowsGU, d / 64) &&
-           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemvRowsGU, d / 64) &&
-           encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemvRowsDown, I_shared / 64);
+      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_codes_sr(&ms.q_down, shared->down.q, 1, d, I_shared, bsr) &&
+           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
+           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
+           encode_groups_sr(&ms.sb_down, shared->down.sb, 1, d, I_shared, bsr);
     if (!ok) return MOE_ERR_CUDA;
-    GemvArgs a{};
+    DecodeArgs a{};
     a.X = X;
     a.ids = r->ids;
     a.w = r->w;
     a.Y = Y;
-    a.h_routed = reinterpret_cast<float*>(wsb + L.gemv_h_routed);
-    a.h_shared = reinterpret_cast<float*>(wsb + L.gemv_h_shared);
+    a.part = reinterpret_cast<float*>(wsb + L.dec_part);
     a.status = status;
     a.T = T;
     a.d = d;
@@ -269,7 +301,7 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     a.E = E;
     a.num_sms = sm_count();
     if (a.num_sms <= 0) return MOE_ERR_CUDA;
-    if (launch_gemv(a, &mr, shared ? &ms : nullptr, ws, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_decode(a, &mr, shared ? &ms : nullptr, ws, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
 
@@ -280,17 +312,17 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
   uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
-  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            encode_codes(&mr.q_up, routed->up.q, E, I, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            encode_codes(&mr.q_down, routed->down.q, E, d, I, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            encode_codes(&mr.q_up, routed->up.q, E, I, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+            encode_codes(&mr.q_down, routed->down.q, E, d, I, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
             encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
   if (ok && shared)
-    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
-         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
-         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, 8, kGemmBM, CU_TENSOR_MAP_SWIZZLE_32B) &&
+    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
          encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&

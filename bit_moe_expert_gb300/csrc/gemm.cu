@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
           mbar_arrive_expect_tx(&full[stage], C::kStageTxBytes);
           tma_load_2d(st, mb, &full[stage], kb * 64, brow);
-          tma_load_3d(q_tile, mq0, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
+          tma_load_3d(q_tile, mq0, &full[stage], 0, m.mt * kGemmBM, m.e * m.nk + kb);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
-            tma_load_3d(q_tile + C::kQBytes, mq1, &full[stage], kb * 8, m.mt * kGemmBM, m.e);
+            tma_load_3d(q_tile + C::kQBytes, mq1, &full[stage], 0, m.mt * kGemmBM, m.e * m.nk + kb);
             tma_load_3d(sb_tile + C::kSBBytes, msb1, &full[stage], m.mt * kGemmBM, kb, m.e);
           }
           used_mask |= 1u << stage;

@@ -14,8 +14,8 @@ namespace bm {
 // Kernel kinds for the optional per-kernel timing (moe_profile.h).
 enum KernelKind {
   kKRoute = 0,
-  kKGemvGateUp,  // the fused decode kernel (gate/up + down)
-  kKGemvDown,    // reserved
+  kKDecode,    // the fused decode kernel (gate/up + down)
+  kKReserved,  // unused
   kKXGather,
   kKGemmGateUp,
   kKGemmDown,
@@ -40,34 +40,37 @@ struct RouteOut {
 size_t route_hist_elems(int T, int E);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out, void* ws,
                          cudaStream_t stream, bool pdl);
+cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream);
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream);
 
 // ---------------------------------------------------------------- decode GEMV
-// Rows per CTA of the gate/up kernel and of the down kernel.
-constexpr int kGemvRowsGU = 32;
-constexpr int kGemvRowsDown = 16;
+constexpr int kDecodeRowsGU = 32;        // gate/up rows per CTA and unit
+constexpr int kDecodeMaxClusters = 128;  // partial-output buffers in the workspace
 
-// Tensor maps of one expert set for the GEMV kernels.
-struct GemvMaps {
-  CUtensorMap q_gate, q_up, q_down;     // codes, box (32 words, rows, 1), 128-byte swizzle
-  CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (rows, K/64, 1)
+// Tensor maps of one expert set for the decode kernel.
+struct DecodeMaps {
+  CUtensorMap q_gate, q_up;    // codes, box (8 words, 32 rows, d/64 groups)
+  CUtensorMap sb_gate, sb_up;  // group parameters, box (32 rows, d/64, 1)
+  CUtensorMap q_down;          // codes as 128-byte super-rows, box (32 words, decode_box_superrows, 1 group)
+  CUtensorMap sb_down;         // group parameters as 4-row super-rows, same box rows
 };
 
-struct GemvArgs {
+struct DecodeArgs {
   const uint16_t* X;   // [T][d] bf16
   const int32_t* ids;  // [T][k]
   const float* w;      // [T][k]
   uint16_t* Y;         // [T][d] bf16
-  float* h_routed;     // [T*k][I] fp32
-  float* h_shared;     // [T][I_shared] fp32
+  float* part;         // [kDecodeMaxClusters][T][d] fp32 partial outputs
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms;
 };
 
-bool gemv_supported(int d, int I, int I_shared, int k);
-cudaError_t launch_gemv(const GemvArgs& a, const GemvMaps* routed, const GemvMaps* shared, void* ws,
-                        cudaStream_t stream, bool pdl);
+bool decode_supported(int T, int d, int I, int I_shared, int k);
+size_t decode_partial_bytes(int T, int d);
+int decode_box_superrows(int d);  // 128-byte super-rows per down-projection box
+cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
+                          cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- prefill GEMM
 constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)

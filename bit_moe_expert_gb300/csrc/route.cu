@@ -344,7 +344,38 @@ __global__ void prepack_kernel(const uint16_t* __restrict__ scale, const uint16_
     sb[o] = static_cast<uint32_t>(scale[i]) | (static_cast<uint32_t>(bias[i]) << 16);
   }
 }
+
+// codes [E][N][K/8] -> [E][K/64][N][8]: each row's 32-byte piece of one group
+// moves next to the same group's piece of the next row
+__global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, int G, uint4* __restrict__ qp) {
+  const size_t total = static_cast<size_t>(E) * G * N;  // 32-byte pieces
+  for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
+       o += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(o % N);
+    const size_t eg = o / N;
+    const int g = static_cast<int>(eg % G);
+    const int e = static_cast<int>(eg / G);
+    const size_t i = (static_cast<size_t>(e) * N + n) * G + g;
+    const uint4 a = q[2 * i], b = q[2 * i + 1];
+    qp[2 * o] = a;
+    qp[2 * o + 1] = b;
+  }
+}
 }  // namespace
+
+cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream) {
+  const int G = K / 64;
+  const size_t total = static_cast<size_t>(E) * G * N;
+  const int threads = 256;
+  const size_t blocks = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
+  timer_begin(kKPrepack, stream);
+  prepack_codes_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(q), E, N, G,
+                                                      reinterpret_cast<uint4*>(qp));
+  const cudaError_t err = cudaGetLastError();
+  timer_end(kKPrepack, stream);
+  return err;
+}
 
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream) {

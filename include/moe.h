@@ -62,8 +62,12 @@ const char* moe_status_string(moe_status s);
 /* ------------------------------------------------------------------ weights
  * One stacked packed matrix of E experts with N rows and K columns (K a
  * multiple of 64):
- *   q   uint32 [E][N][K/8]   the code of column k sits in bits 4*(k%8) of word
- *                            k/8 of its row (low nibble = lowest k);
+ *   q   uint32 [E][K/64][N][8]  the codes, group-major: the 8 words of row n,
+ *                            columns 64g .. 64g+63 sit at [e][g][n][0..7];
+ *                            inside a word the code of column k sits in bits
+ *                            4*(k%8) (low nibble = lowest k).  Build it once
+ *                            per weight set with moe_prepack_codes from the
+ *                            row-major [E][N][K/8] checkpoint layout;
  *   sb  uint32 [E][K/64][N]  the group parameters, transposed so one group of
  *                            many rows is contiguous: bits 0..15 hold the bf16
  *                            scale and bits 16..31 the bf16 bias of rows n,
@@ -86,6 +90,16 @@ typedef struct {
 
 /* Bytes of the sb array for E experts of an N x K matrix: E * (K/64) * N * 4. */
 size_t moe_prepack_bytes(int E, int N, int K);
+
+/* Reorder row-major codes q [E][N][K/8] (the checkpoint layout: row n holds
+ * its K/8 words) into the group-major layout qp [E][K/64][N][8] that
+ * moe_forward reads: the 32-byte piece of every row for one group of 64
+ * columns becomes contiguous, so one group of many rows is one contiguous
+ * block.  A pure data movement (same size, E*N*K/2 bytes); bit-exact.  Both
+ * pointers 16-byte aligned device memory, not overlapping.  Sizes: E >= 1,
+ * N >= 1, K a positive multiple of 64.  Returns MOE_ERR_INVALID_ARG on a bad
+ * size or pointer. */
+moe_status moe_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, moe_stream stream);
 
 /* Transpose and interleave per-group bf16 scale and bias, both laid out
  * [E][N][K/64] as in the checkpoint, into sb [E][K/64][N] (see above).  A pure
@@ -187,10 +201,11 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  *            and returns MOE_ERR_UNSUPPORTED otherwise
  * Preconditions: T >= 0 (T = 0 does nothing), d, I and I_shared multiples of
  * 64 (I_shared = 0 iff shared is NULL), 1 <= k <= min(E, 32), E <= 1024.
- * Path: T <= 4 runs the decode kernels (CUDA-core GEMV, every active expert's
- * bytes streamed once); larger T runs the grouped tensor-core GEMM (tcgen05,
- * dequantisation fused, SwiGLU and the weighted combine fused).  The
- * environment variable MOE_PATH=gemv|gemm overrides the choice (for A/B
+ * Path: T <= 4 runs the decode kernel (CUDA-core GEMV, every active expert's
+ * bytes streamed once, one launch); larger T runs the grouped tensor-core GEMM
+ * (tcgen05, dequantisation fused, SwiGLU and the weighted combine fused).  The
+ * environment variable MOE_PATH=gemv|gemm overrides the choice (gemv with
+ * T > 4 returns MOE_ERR_UNSUPPORTED; for A/B
  * measurements and tests).  Arithmetic: fp32 accumulation; on the GEMM path X,
  * the dequantised weights and the SwiGLU output are rounded to fp16 as
  * tensor-core operands (a value outside the fp16 range is recorded as

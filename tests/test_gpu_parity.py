@@ -44,6 +44,18 @@ def test_prepack_is_exact_transpose():
         np.testing.assert_array_equal(got, ref)
 
 
+def test_prepack_codes_is_exact_reordering():
+    rng = np.random.default_rng(1)
+    for (E, N, K) in [(3, 64, 128), (2, 704, 2816), (1, 2048, 512)]:
+        q = rng.integers(0, 2**32, size=(E, N, K // 8), dtype=np.uint32)
+        qd = torch.from_numpy(q.view(np.int32)).cuda()
+        qp = torch.empty((E, K // 64, N, 8), dtype=torch.int32, device="cuda")
+        bm.moe_prepack_codes(qd, qp)
+        got = qp.cpu().numpy().view(np.uint32)
+        ref = q.reshape(E, N, K // 64, 8).transpose(0, 2, 1, 3)
+        np.testing.assert_array_equal(got, ref)
+
+
 # ------------------------------------------------------------------ routing
 
 ROUTE_CASES = [
@@ -130,6 +142,8 @@ SMALL = [
 @pytest.mark.parametrize("path", ["gemv", "gemm"])
 @pytest.mark.parametrize("name,kw", SMALL, ids=[c[0] for c in SMALL])
 def test_forward_small(name, kw, path):
+    if path == "gemv":  # the decode kernel takes at most 4 tokens
+        kw = dict(kw, T=min(kw.get("T", synth.small_config().T), 4))
     cfg = synth.small_config(**kw)
     layer = synth.draw_layer(cfg)
     dl = G.DeviceLayer.from_host(layer)
@@ -152,6 +166,29 @@ def test_forward_gemm_block_rows(block_rows):
     G.assert_y_close(Y, Y64, f"block_rows={block_rows}")
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_forward_decode_token_counts(T):
+    """Every token count the decode kernel handles, on a layer shaped like the
+    decode workload but with fewer experts; tokens share some experts."""
+    cfg = synth.small_config(T=T, d=1024, E=12, k=8, I=256, I_shared=192)
+    layer = synth.draw_layer(cfg)
+    dl = G.DeviceLayer.from_host(layer)
+    r, _ = G.route_gpu(layer.logits, cfg.k, 32)
+    rh = G.routing_to_host(r)
+    Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, rh["ids"], rh["w"])
+    G.assert_y_close(dl.forward(r, "gemv"), Y64, f"T={T}")
+
+
+def test_forward_decode_rejects_more_than_4_tokens():
+    cfg = synth.small_config(T=5, d=128, E=4, k=2, I=64, I_shared=0)
+    layer = synth.draw_layer(cfg)
+    dl = G.DeviceLayer.from_host(layer)
+    r, _ = G.route_gpu(layer.logits, cfg.k, 32)
+    with pytest.raises(bm.MoeError) as ei:
+        dl.forward(r, "gemv")
+    assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
+
+
 def test_forward_gemm_rejects_tiles_over_96_rows():
     """The tensor-core path holds at most 96 tokens per tile; a routing made
     with taller tiles is refused before any launch."""
@@ -164,15 +201,15 @@ def test_forward_gemm_rejects_tiles_over_96_rows():
     assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
 
 
-def test_forward_deterministic():
-    cfg = synth.small_config(T=64, d=256, E=8, k=2, I=128, I_shared=128)
+@pytest.mark.parametrize("path,T", [("gemv", 1), ("gemv", 4), ("gemm", 64)])
+def test_forward_deterministic(path, T):
+    cfg = synth.small_config(T=T, d=256, E=8, k=2, I=128, I_shared=128)
     layer = synth.draw_layer(cfg)
     dl = G.DeviceLayer.from_host(layer)
     r, _ = G.route_gpu(layer.logits, cfg.k, 64)
-    for path in ("gemv", "gemm"):
-        a = dl.forward(r, path)
-        b = dl.forward(r, path)
-        np.testing.assert_array_equal(a, b)
+    first = dl.forward(r, path)
+    for _ in range(3):
+        np.testing.assert_array_equal(dl.forward(r, path), first)
 
 
 def test_forward_zero_tokens():
@@ -184,9 +221,10 @@ def test_forward_zero_tokens():
     assert dl.forward(r, "gemm").size == 0
 
 
-def test_forward_code8_experts_give_shared_only():
+@pytest.mark.parametrize("path,T", [("gemv", 3), ("gemm", 40)])
+def test_forward_code8_experts_give_shared_only(path, T):
     """All routed weights dequantise to exactly 0: Y is the shared expert alone."""
-    cfg = synth.small_config(T=40)
+    cfg = synth.small_config(T=T)
     layer = synth.draw_layer(cfg)
     layer.routed = {m: (np.full_like(q, 0x88888888), s, b) for m, (q, s, b) in layer.routed.items()}
     dl = G.DeviceLayer.from_host(layer)
@@ -194,8 +232,7 @@ def test_forward_code8_experts_give_shared_only():
     ids = np.zeros((cfg.T, cfg.k), np.int32)
     w = np.zeros((cfg.T, cfg.k), np.float32)
     Ysh, _ = oracle.forward(layer.X, layer.routed, layer.shared, ids, w)
-    for path in ("gemv", "gemm"):
-        G.assert_y_close(dl.forward(r, path), Ysh, path)
+    G.assert_y_close(dl.forward(r, path), Ysh, path)
 
 
 # ------------------------------------------------------------------ full-size workloads, sampled tokens
