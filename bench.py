@@ -202,6 +202,7 @@ def _dev_layer(cfg, layer, dev, with_shared=True):
 class DecodeWorkload(Workload):
     name = "decode"
     dtype = "f32"
+    api_desc = "moe_layer"
 
     def __init__(self, dev, layers=None):
         import torch
@@ -226,8 +227,7 @@ class DecodeWorkload(Workload):
             self.logits.append(torch.from_numpy(lh).to(dev))
         self.block_rows = 96
         self.r = bm.Routing.empty(self.T, cfg.E, cfg.k, self.block_rows, dev)
-        self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(self.T, cfg.E, cfg.k), dev)
-        self.ws_f = bm.workspace(bm.moe_forward_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
+        self.ws = bm.workspace(bm.moe_layer_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
         self.Y = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16, device=dev)
         self.tokens_per_step = self.L * self.T
         # pinned host buffers for the end-to-end measurement
@@ -240,21 +240,21 @@ class DecodeWorkload(Workload):
         self.d2h_bytes = self.L * self.T * cfg.d * 2
 
     def launches_per_step(self):
-        return self.L * 2  # route, fused decode kernel
+        return self.L  # moe_layer at T=1: one decode kernel that also routes
 
     def step(self):
         bm, cfg = self.bm, self.cfg
         for l in range(self.L):
-            bm.moe_route(self.logits[l], cfg.k, self.block_rows, self.r, self.ws_r)
-            bm.moe_forward(self.X[l], self.routed[l], self.shared[l], self.r, self.Y[l], self.ws_f)
+            bm.moe_layer(self.logits[l], self.X[l], self.routed[l], self.shared[l], cfg.k, self.block_rows, self.r,
+                         self.Y[l], self.ws)
 
     def e2e_step(self):
         bm, cfg = self.bm, self.cfg
         for l in range(self.L):
             self.X_e2e.copy_(self.X_pin[l], non_blocking=True)
             self.lg_e2e.copy_(self.lg_pin[l], non_blocking=True)
-            bm.moe_route(self.lg_e2e, cfg.k, self.block_rows, self.r, self.ws_r)
-            bm.moe_forward(self.X_e2e, self.routed[l], self.shared[l], self.r, self.Y[l], self.ws_f)
+            bm.moe_layer(self.lg_e2e, self.X_e2e, self.routed[l], self.shared[l], cfg.k, self.block_rows, self.r,
+                         self.Y[l], self.ws)
             self.Y_pin[l].copy_(self.Y[l], non_blocking=True)
 
     # algorithmic work
@@ -314,6 +314,7 @@ class DecodeWorkload(Workload):
 class PrefillWorkload(Workload):
     """Chunked prefill: T tokens as chunks, each chunk through a different weight set."""
     dtype = "f16 MMA, f32 accumulate"
+    api_desc = "moe_route + moe_forward"
 
     def __init__(self, dev, name="prefill4096", sets=None):
         import torch
@@ -489,7 +490,7 @@ def run_workload(wl, args, dist, peaks, clocks):
     ms_e2e = dist.reduce(time_e2e(wl, args.steps, args.warmup, dist), "max")
     e2e = {"value": tok / (ms_e2e / 1e3), "unit": "tok/s", "h2d_bytes_per_step": wl.h2d_bytes,
            "d2h_bytes_per_step": wl.d2h_bytes, "ms_per_step": ms_e2e / args.steps,
-           "note": "public API per call (moe_route + moe_forward), inputs copied from pinned host memory and Y "
+           "note": f"public API per call ({wl.api_desc}), inputs copied from pinned host memory and Y "
                    "copied back every step, no CUDA graph"}
     kt = time_kernels(wl, min(args.steps, 200))
     kname, bound, work, work_desc = wl.dominant()
@@ -518,7 +519,7 @@ def run_workload(wl, args, dist, peaks, clocks):
         out["layer_roofline"] = {"bound": "hbm", "active_bytes_per_layer": wl.bytes_per_step() // wl.L,
                                  "us_per_layer": t_layer * 1e6, "achieved": gbs, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                                 "note": "whole layer (routing + both GEMV kernels) inside the 40-layer graph"}
+                                 "note": "whole layer (moe_layer: routing and both projections in one launch) inside the 40-layer graph"}
     else:
         fl = wl.flops_per_step() / ((ms / args.steps) / 1e3) / 1e12
         out["step_roofline"] = {"bound": "tensor", "flops_per_step": wl.flops_per_step(), "achieved": fl,

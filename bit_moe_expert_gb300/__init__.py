@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
             "moe_forward_workspace_bytes",
-            "moe_forward", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
+            "moe_forward", "moe_layer_workspace_bytes", "moe_layer", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
             "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
 
 
@@ -84,6 +84,12 @@ def lib(path: Optional[str] = None):
         L.moe_forward.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Experts),
                                   C.POINTER(_Experts), C.c_int, C.POINTER(_Routing), C.c_void_p, C.c_void_p,
                                   C.c_size_t, C.c_void_p]
+        L.moe_layer_workspace_bytes.restype = C.c_size_t
+        L.moe_layer_workspace_bytes.argtypes = [C.c_int] * 6
+        L.moe_layer.restype = C.c_int
+        L.moe_layer.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                C.POINTER(_Experts), C.POINTER(_Experts), C.c_int, C.POINTER(_Routing), C.c_void_p,
+                                C.c_void_p, C.c_size_t, C.c_void_p]
         L.moe_check_status.restype = C.c_int
         L.moe_check_status.argtypes = [C.c_void_p, C.c_void_p]
         L.moe_profile_enable.restype = C.c_int
@@ -249,6 +255,24 @@ def moe_forward(X, routed: Experts, shared: Optional[Experts], routing: Routing,
     _check("moe_forward", lib().moe_forward(_ptr(X), T, d, routed.I, k, C.byref(re),
                                             C.byref(se) if se is not None else None, I_sh, C.byref(rr), _ptr(Y),
                                             _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_workspace_bytes(T: int, d: int, I: int, E: int, k: int, I_shared: int) -> int:
+    return int(lib().moe_layer_workspace_bytes(T, d, I, E, k, I_shared))
+
+
+def moe_layer(logits, X, routed: Experts, shared: Optional[Experts], k: int, block_rows: int, out: Routing, Y, ws,
+              stream=None) -> None:
+    """moe_route + moe_forward in one call (one launch on the decode path)."""
+    T, d = X.shape
+    re = routed._c()
+    se = shared._c() if shared is not None else None
+    I_sh = shared.I if shared is not None else 0
+    r = out._c()
+    _check("moe_layer", lib().moe_layer(_ptr(logits), _ptr(X), T, d, routed.I, k, block_rows, C.byref(re),
+                                        C.byref(se) if se is not None else None, I_sh, C.byref(r), _ptr(Y),
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+    out.block_rows = r.block_rows
 
 
 def moe_check_status(ws, stream=None) -> int:

@@ -231,9 +231,13 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
   return fwd_layout(T, d, I, k, I_shared).total;
 }
 
-moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
-                       const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y, void* ws,
-                       size_t ws_bytes, moe_stream stream) {
+namespace {
+
+// moe_forward; with `logits` set and T on the decode path, the decode kernel
+// also routes the tokens and writes every routing output to *r (moe_layer).
+moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
+                        const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y, void* ws,
+                        size_t ws_bytes, moe_stream stream, const float* logits) {
   if (T < 0 || d < 64 || I < 64 || k < 1 || I_shared < 0) return MOE_ERR_INVALID_ARG;
   if (d % 64 || I % 64 || I_shared % 64) return MOE_ERR_INVALID_ARG;
   if ((shared != nullptr) != (I_shared > 0)) return MOE_ERR_INVALID_ARG;
@@ -272,15 +276,17 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     DecodeMaps mr, ms;
     const int KB1 = d / 64;
     const cuuint32_t bsr = static_cast<cuuint32_t>(decode_box_superrows(d));
-    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              encode_codes(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              encode_codes(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, CU_TENSOR_MAP_SWIZZLE_NONE) &&
               encode_codes_sr(&mr.q_down, routed->down.q, E, d, I, bsr) &&
               encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, KB1) &&
               encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, KB1) &&
               encode_groups_sr(&mr.sb_down, routed->down.sb, E, d, I, bsr);
     if (ok && shared)
-      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, KB1, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
            encode_codes_sr(&ms.q_down, shared->down.q, 1, d, I_shared, bsr) &&
            encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
            encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
@@ -290,6 +296,9 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
     a.X = X;
     a.ids = r->ids;
     a.w = r->w;
+    a.logits = logits;
+    a.out = RouteOut{r->ids, r->w, r->counts, r->offsets, r->perm, r->inv_perm, r->block_map, r->num_blocks};
+    a.block_rows = r->block_rows;
     a.Y = Y;
     a.part = reinterpret_cast<float*>(wsb + L.dec_part);
     a.status = status;
@@ -354,6 +363,53 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
   if (a.num_sms <= 0) return MOE_ERR_CUDA;
   if (launch_gemm(a, &mr, shared ? &ms : nullptr, &act, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
+                       const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y, void* ws,
+                       size_t ws_bytes, moe_stream stream) {
+  return forward_impl(X, T, d, I, k, routed, shared, I_shared, r, Y, ws, ws_bytes, stream, nullptr);
+}
+
+size_t moe_layer_workspace_bytes(int T, int d, int I, int E, int k, int I_shared) {
+  const size_t f = moe_forward_workspace_bytes(T, d, I, E, k, I_shared);
+  const size_t r = moe_route_workspace_bytes(T, E, k);
+  if (!f || !r) return 0;
+  return round256(f) + r;
+}
+
+moe_status moe_layer(const float* logits, const uint16_t* X, int T, int d, int I, int k, int block_rows,
+                     const moe_experts* routed, const moe_experts* shared, int I_shared, moe_routing* r, uint16_t* Y,
+                     void* ws, size_t ws_bytes, moe_stream stream) {
+  if (!r || !experts_ok(routed) || T < 0 || k < 1) return MOE_ERR_INVALID_ARG;
+  const int E = routed->n_experts;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
+  if (!r->counts || !r->offsets || !r->block_map || !r->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !r->ids || !r->w || !r->perm || !r->inv_perm)) return MOE_ERR_INVALID_ARG;
+  const size_t fbytes = moe_forward_workspace_bytes(T, d, I, E, k, I_shared);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || fbytes == 0 ||
+      ws_bytes < moe_layer_workspace_bytes(T, d, I, E, k, I_shared))
+    return MOE_ERR_WORKSPACE;
+  // One launch when the decode kernel takes the call and can route it itself.
+  bool fused = T >= 1 && T <= kGemvMaxT && E <= 256 && decode_supported(T, d, I, I_shared, k);
+  if (const char* p = std::getenv("MOE_PATH"))
+    if (!std::strcmp(p, "gemm")) fused = false;
+  if (fused) {
+    r->block_rows = block_rows;
+    return forward_impl(X, T, d, I, k, routed, shared, I_shared, r, Y, ws, fbytes, stream, logits);
+  }
+  // Otherwise the routing kernel, then moe_forward; both report into the first header.
+  char* route_ws = static_cast<char*>(ws) + round256(fbytes);
+  r->block_rows = block_rows;
+  RouteOut o{r->ids, r->w, r->counts, r->offsets, r->perm, r->inv_perm, r->block_map, r->num_blocks};
+  const bool pdl = env_flag("MOE_PDL", true);
+  if (launch_route(logits, T, E, k, block_rows, o, route_ws, reinterpret_cast<cudaStream_t>(stream), pdl,
+                   &static_cast<WsHeader*>(ws)->status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return forward_impl(X, T, d, I, k, routed, shared, I_shared, r, Y, ws, fbytes, stream, nullptr);
 }
 
 moe_status moe_check_status(void* ws, moe_stream stream) {

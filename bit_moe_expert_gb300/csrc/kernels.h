@@ -38,36 +38,42 @@ struct RouteOut {
 };
 
 size_t route_hist_elems(int T, int E);
+// status: where device-side errors go (null: the workspace header's status word)
 cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out, void* ws,
-                         cudaStream_t stream, bool pdl);
+                         cudaStream_t stream, bool pdl, uint32_t* status = nullptr);
 cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream);
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream);
 
 // ---------------------------------------------------------------- decode GEMV
 constexpr int kDecodeRowsGU = 32;        // gate/up rows per CTA and unit
-constexpr int kDecodeMaxClusters = 128;  // partial-output buffers in the workspace
+constexpr int kDecodeChunkGroups = 8;    // 64-column groups per gate/up code box
+constexpr int kDecodeMaxClusters = 128;  // clusters per launch at most
 
 // Tensor maps of one expert set for the decode kernel.
 struct DecodeMaps {
-  CUtensorMap q_gate, q_up;    // codes, box (8 words, 32 rows, d/64 groups)
+  CUtensorMap q_gate, q_up;    // codes, box (8 words, 32 rows, kDecodeChunkGroups groups)
   CUtensorMap sb_gate, sb_up;  // group parameters, box (32 rows, d/64, 1)
   CUtensorMap q_down;          // codes as 128-byte super-rows, box (32 words, decode_box_superrows, 1 group)
   CUtensorMap sb_down;         // group parameters as 4-row super-rows, same box rows
 };
 
 struct DecodeArgs {
-  const uint16_t* X;   // [T][d] bf16
-  const int32_t* ids;  // [T][k]
-  const float* w;      // [T][k]
-  uint16_t* Y;         // [T][d] bf16
-  float* part;         // [kDecodeMaxClusters][T][d] fp32 partial outputs
+  const uint16_t* X;      // [T][d] bf16
+  const int32_t* ids;     // [T][k] (routing read from memory)
+  const float* w;         // [T][k]
+  const float* logits;    // [T][E]: when not null the kernel routes its own tokens (E <= 256) and one extra
+                          // cluster writes every routing output to `out`
+  RouteOut out;           // routing outputs written by the kernel (logits != null)
+  int block_rows;         // tile height of the block map it writes
+  uint16_t* Y;            // [T][d] bf16
+  float* part;            // [kDecodeMaxClusters][T][d] fp32 partial outputs
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms;
 };
 
 bool decode_supported(int T, int d, int I, int I_shared, int k);
-size_t decode_partial_bytes(int T, int d);
+size_t decode_partial_bytes(int T, int d);  // bytes of the partial outputs
 int decode_box_superrows(int d);  // 128-byte super-rows per down-projection box
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
                           cudaStream_t stream, bool pdl);

@@ -17,6 +17,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace bm {
 
@@ -30,7 +31,8 @@ constexpr int kBasesSmemLimit = 96 * 1024;  // per-chunk bases kept in shared me
 template <int kPL>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E,
                                                               int k, int block_rows, RouteOut out,
-                                                              WsHeader* hdr, int32_t* __restrict__ chunk_hist,
+                                                              WsHeader* hdr, uint32_t* status,
+                                                              int32_t* __restrict__ chunk_hist,
                                                               int32_t* __restrict__ local_rank, int bases_in_smem) {
   extern __shared__ int32_t s_bases[];  // [nchunks][E] exclusive per-chunk bases (last CTA, when they fit)
   __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
@@ -58,58 +60,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   for (int tl = warp; tl < ntok; tl += kRouteWarps) {
     const int t = t0 + tl;
     const float* row = logits + static_cast<size_t>(t) * E;
-    // Monotone 32-bit keys: a larger float gives a larger unsigned key.  -0.0
-    // becomes +0.0 first, so equal floats always get equal keys and the tie
-    // goes to the lower expert index, as with a float comparison.
-    uint32_t key[kPL];
-    uint32_t taken = 0;
-    bool finite = true;
-#pragma unroll
-    for (int c = 0; c < kPL; ++c) {
-      const int e = lane + 32 * c;
-      const bool in = e < E;
-      float v = in ? __ldg(row + e) : 0.0f;
-      finite &= !in || isfinite(v);
-      if (v == 0.0f) v = 0.0f;
-      const uint32_t u = __float_as_uint(v);
-      key[c] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-      if (!in) taken |= 1u << c;
-    }
-    if (!__all_sync(0xffffffffu, finite)) record_status(&hdr->status, MOE_ERR_NONFINITE);
-
-    uint32_t sel_key = 0;  // lane j keeps the j-th selected key
-    int sel_i = 0;
-    for (int j = 0; j < k; ++j) {
-      // lane-local best: largest key, lowest index among equal keys
-      uint32_t bk = 0;
-      int bi = 0x7FFFFFFF;
-#pragma unroll
-      for (int c = 0; c < kPL; ++c) {
-        if (!((taken >> c) & 1u) && (key[c] > bk || bi == 0x7FFFFFFF)) {
-          bk = key[c];
-          bi = lane + 32 * c;
-        }
-      }
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi == 0x7FFFFFFF ? 0u : bk);
-      const int win = static_cast<int>(
-          __reduce_min_sync(0xffffffffu, (bi != 0x7FFFFFFF && bk == kmax) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu));
-      if ((win & 31) == lane) taken |= 1u << (win >> 5);
-      if (lane == j) {
-        sel_key = kmax;
-        sel_i = win;
-      }
-    }
-    // back from key to float
-    const uint32_t su = (sel_key & 0x80000000u) ? (sel_key & 0x7FFFFFFFu) : ~sel_key;
-    const float sel_v = __uint_as_float(su);
-    // weights: exp(l_j - l_max) in fp64, summed in selection order, one rounding to fp32
-    const float top = __shfl_sync(0xffffffffu, sel_v, 0);
-    const double ex = (lane < k) ? exp(static_cast<double>(sel_v) - static_cast<double>(top)) : 0.0;
-    double sum = 0.0;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    int sel_i;
+    float sel_v;
+    bool finite;
+    warp_topk_select<kPL>(row, E, k, lane, sel_i, sel_v, finite);
+    const float sel_w = warp_topk_weights(sel_v, k, lane);
+    if (!finite && lane == 0) record_status(status, MOE_ERR_NONFINITE);
     if (lane < k) {
       out.ids[static_cast<size_t>(t) * k + lane] = sel_i;
-      out.w[static_cast<size_t>(t) * k + lane] = static_cast<float>(ex / sum);
+      out.w[static_cast<size_t>(t) * k + lane] = sel_w;
       s_ids[tl * k + lane] = sel_i;
     }
   }
@@ -286,8 +245,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out,
-                         void* ws, cudaStream_t stream, bool pdl) {
+                         void* ws, cudaStream_t stream, bool pdl, uint32_t* status) {
   WsHeader* hdr = static_cast<WsHeader*>(ws);
+  if (!status) status = &hdr->status;
   const int nchunks = T > 0 ? (T + kRouteTokensPerCta - 1) / kRouteTokensPerCta : 1;
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(WsHeader));
   int32_t* local_rank = chunk_hist + route_hist_elems(T, E);
@@ -314,10 +274,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   cfg.numAttrs = 1;
   timer_begin(kKRoute, stream);
   const cudaError_t err =
-      E <= 256 ? cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, T, E, k, block_rows, out, hdr, chunk_hist,
-                                    local_rank, bases_in_smem)
-               : cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, T, E, k, block_rows, out, hdr, chunk_hist,
-                                    local_rank, bases_in_smem);
+      E <= 256 ? cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, T, E, k, block_rows, out, hdr, status,
+                                    chunk_hist, local_rank, bases_in_smem)
+               : cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, T, E, k, block_rows, out, hdr, status,
+                                    chunk_hist, local_rank, bases_in_smem);
   timer_end(kKRoute, stream);
   return err;
 }

@@ -12,8 +12,8 @@ namespace bm {
 struct WsHeader {
   uint32_t status;     // first device-side error (moe_status), 0 = none
   uint32_t ticket;     // arrival counter of the routing kernel; reset by its last CTA
-  uint32_t dec_arrive;  // decode kernel: CTAs that have written their partial output
-  uint32_t dec_done;    // decode kernel: reducers that have finished; the last resets both
+  uint32_t dec_arrive;  // decode kernel: CTAs that have written their partial output (grid barrier)
+  uint32_t dec_done;    // decode kernel: CTAs that have finished; the last resets both
   uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");

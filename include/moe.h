@@ -214,8 +214,27 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
                        const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y,
                        void* ws, size_t ws_bytes, moe_stream stream);
 
+/* ------------------------------------------------------------------ whole layer
+ * Workspace bytes moe_layer needs (the forward workspace followed by a routing
+ * workspace); same rules: zero-filled once, 256-byte aligned, one in-flight
+ * call per workspace. */
+size_t moe_layer_workspace_bytes(int T, int d, int I, int E, int k, int I_shared);
+
+/* moe_route followed by moe_forward on the same stream, with the same
+ * arguments and results: r receives every routing output and Y the layer
+ * output.  E = routed->n_experts.  When the decode kernel takes the call
+ * (1 <= T <= 4, E <= 256, its shared-memory plan fits, MOE_PATH not "gemm")
+ * this is ONE launch: every CTA of the decode kernel selects the tokens'
+ * experts itself with the routing kernel's arithmetic, and one extra CTA pair
+ * writes the routing outputs.  Otherwise it launches the routing kernel and
+ * then the moe_forward kernels.  Device-side errors of both parts go to the
+ * status word at the start of ws (read it with moe_check_status(ws, ...)). */
+moe_status moe_layer(const float* logits, const uint16_t* X, int T, int d, int I, int k, int block_rows,
+                     const moe_experts* routed, const moe_experts* shared, int I_shared, moe_routing* r,
+                     uint16_t* Y, void* ws, size_t ws_bytes, moe_stream stream);
+
 /* Synchronises `stream`, returns the status recorded in the workspace of a
- * previous moe_route or moe_forward call (MOE_OK if none) and clears it.  For
+ * previous moe_route, moe_forward or moe_layer call (MOE_OK if none) and clears it.  For
  * tests and debugging; never needed on the hot path. */
 moe_status moe_check_status(void* ws, moe_stream stream);
 

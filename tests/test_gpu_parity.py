@@ -270,3 +270,78 @@ def test_full_size_gemv_and_gemm_agree(name):
     Y64, _ = oracle.forward(dl.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"])
     G.assert_y_close(Yv, Y64, "gemv")
     G.assert_y_close(Ym, Y64, "gemm")
+
+
+# ------------------------------------------------------------------ whole layer (moe_layer)
+
+def _layer_gpu(layer, cfg, block_rows):
+    dl = G.DeviceLayer.from_host(layer)
+    T, E = cfg.T, cfg.E
+    lg = torch.from_numpy(np.ascontiguousarray(layer.logits, dtype=np.float32)).cuda()
+    r = bm.Routing.empty(T, E, cfg.k, block_rows)
+    ws = bm.workspace(bm.moe_layer_workspace_bytes(T, cfg.d, cfg.I, E, cfg.k, cfg.I_shared))
+    Y = torch.empty((T, cfg.d), dtype=torch.int16, device="cuda")
+    bm.moe_layer(lg, dl.X, dl.routed, dl.shared, cfg.k, block_rows, r, Y, ws)
+    torch.cuda.synchronize()
+    return r, ws, Y.cpu().numpy().view(np.uint16)
+
+
+LAYER_CASES = [
+    ("T1_fused", dict(T=1, d=1024, E=64, k=8, I=256, I_shared=192), 32),
+    ("T2_fused_no_shared", dict(T=2, d=512, E=32, k=4, I=128, I_shared=0), 8),
+    ("T3_fused_shared_experts", dict(T=3, d=512, E=12, k=8, I=128, I_shared=128), 16),
+    ("T4_fused", dict(T=4, d=768, E=40, k=6, I=192, I_shared=64), 1),
+    ("T2_two_launches_E300", dict(T=2, d=256, E=300, k=4, I=64, I_shared=64), 16),
+    ("T20_two_launches", dict(T=20, d=256, E=16, k=2, I=128, I_shared=128), 32),
+]
+
+
+@pytest.mark.parametrize("name,kw,br", LAYER_CASES, ids=[c[0] for c in LAYER_CASES])
+def test_layer_matches_oracle(name, kw, br):
+    """moe_layer: every routing output bit-exact, Y within tolerance, whether it
+    runs as one launch (decode kernel routing its own tokens) or as two."""
+    cfg = synth.small_config(**kw)
+    layer = synth.draw_layer(cfg)
+    r, ws, Y = _layer_gpu(layer, cfg, br)
+    assert bm.moe_check_status(ws) == 0
+    ref = oracle.route(layer.logits, cfg.k, br)
+    G.assert_routing_equal(G.routing_to_host(r), ref)
+    Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, ref["ids"], ref["w"])
+    G.assert_y_close(Y, Y64, name)
+
+
+def test_layer_fused_forced_ties_and_nonfinite():
+    cfg = synth.small_config(T=2, d=256, E=16, k=4, I=64, I_shared=64)
+    layer = synth.draw_layer(cfg)
+    layer.logits[0, :] = 0.5  # all equal: experts 0..3, weights 1/4
+    layer.logits[1, 3] = -0.0
+    layer.logits[1, 9] = 0.0
+    r, ws, Y = _layer_gpu(layer, cfg, 4)
+    assert bm.moe_check_status(ws) == 0
+    ref = oracle.route(layer.logits, cfg.k, 4)
+    G.assert_routing_equal(G.routing_to_host(r), ref)
+    assert list(ref["ids"][0]) == [0, 1, 2, 3]
+    layer.logits[1, 5] = np.nan
+    r, ws, Y = _layer_gpu(layer, cfg, 4)
+    assert bm.moe_check_status(ws) == 6
+
+
+def test_layer_decode_full_size_and_deterministic():
+    cfg = synth.CONFIGS["decode"]
+    dl = G.DeviceLayer.from_device_draw(cfg, 2, 1)
+    lg = torch.from_numpy(dl.logits).cuda()
+    r = bm.Routing.empty(1, cfg.E, cfg.k, 96)
+    ws = bm.workspace(bm.moe_layer_workspace_bytes(1, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared))
+    outs = []
+    for _ in range(3):
+        Y = torch.empty((1, cfg.d), dtype=torch.int16, device="cuda")
+        bm.moe_layer(lg, dl.X, dl.routed, dl.shared, cfg.k, 96, r, Y, ws)
+        torch.cuda.synchronize()
+        assert bm.moe_check_status(ws) == 0
+        outs.append(Y.cpu().numpy().view(np.uint16))
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
+    ref = oracle.route(dl.logits, cfg.k, 96)
+    G.assert_routing_equal(G.routing_to_host(r), ref)
+    Y64, _ = oracle.forward(dl.X_host, dl.routed_host, dl.shared_host, ref["ids"], ref["w"])
+    G.assert_y_close(outs[0], Y64, "decode layer")
