@@ -203,11 +203,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
 template <int kT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -272,28 +267,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   // gate and up codes of groups [8c, 8c+8) (32 rows each), lane nchunk the
   // gate/up group parameters, the next nboxd lanes the down rows of this CTA's
   // half for the unit's group (codes and parameters).
+  // Warp 0 issues a unit's loads without divergence: first every barrier's
+  // byte count (one lane per barrier), then one TMA copy per lane:
+  //   copies 0, 1:               gate and up group parameters
+  //   copies 2c+2, 2c+3:         gate and up codes of groups [8c, 8c+8), 32 rows (c < nchunk)
+  //   then per down box b:       down codes and parameters of this CTA's half, the unit's group
   auto issue = [&](const Unit& m, int e) {
     const uint64_t pol = l2_policy_evict_first();  // every weight byte is read once
     const int n0 = m.g * 64 + static_cast<int>(rank) * kRows;
     const int Ge = m.shared ? Gs : G;
-    if (lane < L.nchunk) {
-      const uint32_t bytes = kChunkGroups * kRows * 32;
-      mbar_arrive_expect_tx(&bar_gu[lane], 2 * bytes);
-      const int gz = e * L.KB1 + lane * kChunkGroups;
-      tma_load_3d_hint(qg + static_cast<size_t>(lane) * bytes, m.shared ? &qg_s : &qg_r, &bar_gu[lane], 0, n0, gz, pol);
-      tma_load_3d_hint(qu + static_cast<size_t>(lane) * bytes, m.shared ? &qu_s : &qu_r, &bar_gu[lane], 0, n0, gz, pol);
-    } else if (lane == L.nchunk) {
-      mbar_arrive_expect_tx(bar_sb, static_cast<uint32_t>(2 * L.KB1 * kRows * 4));
-      tma_load_3d_hint(smem + L.sbgu, m.shared ? &sbg_s : &sbg_r, bar_sb, n0, 0, e, pol);
-      tma_load_3d_hint(smem + L.sbgu + L.sb1_slot, m.shared ? &sbu_s : &sbu_r, bar_sb, n0, 0, e, pol);
-    } else if (lane < L.nchunk + 1 + L.nboxd) {
-      const int b = lane - L.nchunk - 1;
-      const int sr0 = static_cast<int>(rank) * (L.half / 4) + b * L.box_sr;
-      mbar_arrive_expect_tx(&bar_d[b], static_cast<uint32_t>(L.box_sr * (128 + 16)));
-      tma_load_3d_hint(smem + L.qd + static_cast<size_t>(b) * L.box_sr * 128, m.shared ? &qd_s : &qd_r, &bar_d[b], 0,
-                  sr0, e * Ge + m.g, pol);
-      tma_load_3d_hint(smem + L.sbd + static_cast<size_t>(b) * L.box_sr * 16, m.shared ? &sbd_s : &sbd_r, &bar_d[b], 0,
-                  sr0, e * Ge + m.g, pol);
+    const uint32_t cbytes = kChunkGroups * kRows * 32;
+    if (lane < L.nchunk + 1 + L.nboxd) {
+      uint64_t* bar;
+      uint32_t bytes;
+      if (lane < L.nchunk) {
+        bar = &bar_gu[lane];
+        bytes = 2 * cbytes;
+      } else if (lane == L.nchunk) {
+        bar = bar_sb;
+        bytes = static_cast<uint32_t>(2 * L.KB1 * kRows * 4);
+      } else {
+        bar = &bar_d[lane - L.nchunk - 1];
+        bytes = static_cast<uint32_t>(L.box_sr * (128 + 16));
+      }
+      mbar_arrive_expect_tx(bar, bytes);
+    }
+    __syncwarp();
+    const int ncopy = 2 * (L.nchunk + 1 + L.nboxd);
+    if (lane < ncopy) {
+      // the group parameters first: every gate/up product needs them
+      const int slot = lane >> 1, second = lane & 1;
+      const int which = slot == 0 ? L.nchunk : slot - 1 < L.nchunk ? slot - 1 : slot;
+      const CUtensorMap* map;
+      void* dst;
+      uint64_t* bar;
+      int c1, c2;
+      if (which < L.nchunk) {
+        map = second ? (m.shared ? &qu_s : &qu_r) : (m.shared ? &qg_s : &qg_r);
+        dst = (second ? qu : qg) + static_cast<size_t>(which) * cbytes;
+        bar = &bar_gu[which];
+        c1 = n0;
+        c2 = e * L.KB1 + which * kChunkGroups;
+      } else if (which == L.nchunk) {
+        map = second ? (m.shared ? &sbu_s : &sbu_r) : (m.shared ? &sbg_s : &sbg_r);
+        dst = smem + L.sbgu + (second ? L.sb1_slot : 0);
+        bar = bar_sb;
+        c1 = 0;
+        c2 = e;
+      } else {
+        const int b = which - L.nchunk - 1;
+        map = second ? (m.shared ? &sbd_s : &sbd_r) : (m.shared ? &qd_s : &qd_r);
+        dst = second ? smem + L.sbd + static_cast<size_t>(b) * L.box_sr * 16
+                     : smem + L.qd + static_cast<size_t>(b) * L.box_sr * 128;
+        bar = &bar_d[b];
+        c1 = static_cast<int>(rank) * (L.half / 4) + b * L.box_sr;
+        c2 = e * Ge + m.g;
+      }
+      // the gate/up parameter boxes start at row n0 (their first coordinate)
+      tma_load_3d_hint(dst, map, bar, which == L.nchunk ? n0 : 0, c1, c2, pol);
     }
   };
 
@@ -366,7 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Distinct experts of the call in order of first appearance, and the
     // routing weight of each for each token.
     int nsl = rs0;
-    if (na <= 32) {
+    if (kT == 1 && fused) {
+      // one token: its k experts are distinct, slot j holds selection j
+      if (lane < na) {
+        slot_e[rs0 + lane] = s_ids[lane];
+        s_slot[lane] = rs0 + lane;
+      }
+      nsl = rs0 + na;
+    } else if (na <= 32) {
       // one assignment per lane: a lane whose expert no lower lane holds opens a slot
       const bool valid = lane < na;
       int e = valid ? s_ids[lane] : -1 - lane;
@@ -664,7 +702,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it < items) {
         t = it / (r1 - r0);
         row = r0 + it % (r1 - r0);
-        for (int c = j; c < nclu; c += S) v += __ldcg(a.part + (static_cast<size_t>(c) * kT + t) * d + row);
+        // four loads in flight per round, added in cluster order
+        for (int c0 = j; c0 < nclu; c0 += 4 * S) {
+          float pv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = c0 + q * S;
+            pv[q] = c < nclu ? __ldcg(a.part + (static_cast<size_t>(c) * kT + t) * d + row) : 0.0f;
+          }
+          v += pv[0];
+          v += pv[1];
+          v += pv[2];
+          v += pv[3];
+        }
       }
       for (int off = 1; off < S; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
       if (it < items && j == 0) a.Y[static_cast<size_t>(t) * d + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v));

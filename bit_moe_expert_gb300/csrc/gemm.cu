@@ -501,27 +501,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The gate/up GEMM's token operand: fp16 rows of X in the routing's permuted
 // order (row p = X[perm[p] / k]), followed by the T rows of X in token order
 // when there is a shared expert.  Values outside the fp16 range are recorded
-// as MOE_ERR_UNSUPPORTED.  One warp per row, 16-byte loads and stores.
+// as MOE_ERR_UNSUPPORTED.  16-byte pieces, four in flight per thread.
 __global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, int T, int d,
                                 int k, int rows, uint16_t* __restrict__ Xg, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
+  constexpr int kU = 4;
   const int A = T * k;
   const int d8 = d / 8;
+  const size_t n = static_cast<size_t>(rows) * d8;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   bool range_ok = true, idx_ok = true;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
-    int t = r - A;
-    if (r < A) t = __ldg(perm + r) / k;
-    if (t < 0 || t >= T) {
-      idx_ok = false;
-      continue;
+  for (size_t base = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n; base += stride * kU) {
+    uint4 v[kU];
+    bool ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const size_t i = base + u * stride;
+      ok[u] = false;
+      if (i < n) {
+        const int r = static_cast<int>(i / d8);
+        const int c = static_cast<int>(i - static_cast<size_t>(r) * d8);
+        const int t = r < A ? __ldg(perm + r) / k : r - A;
+        ok[u] = t >= 0 && t < T;
+        idx_ok &= ok[u];
+        if (ok[u]) v[u] = __ldg(reinterpret_cast<const uint4*>(X) + static_cast<size_t>(t) * d8 + c);
+      }
     }
-    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<size_t>(t) * d);
-    uint4* dst = reinterpret_cast<uint4*>(Xg + static_cast<size_t>(r) * d);
-    for (int c = lane; c < d8; c += 32) {
-      const uint4 v = src[c];
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (!ok[u]) continue;
+      const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       uint32_t out[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -530,7 +540,7 @@ __global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* _
         range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
         out[j] = f32x2_to_f16x2(lo, hi);
       }
-      dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<uint4*>(Xg)[base + u * stride] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
   if (!range_ok) record_status(status, MOE_ERR_UNSUPPORTED);
@@ -538,46 +548,71 @@ __global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* _
 }
 
 // Y[t] = bf16( sum_j w[t][j] * yexp[inv_perm[t*k + j]] + yexp[A + t] ): the
-// weighted top-k combine plus the shared expert, summed in slot order.
+// weighted top-k combine plus the shared expert, summed in slot order.  Four
+// warps per token, each a quarter of the columns; the lanes read the token's
+// k rows and weights once; the rows' 16-byte pieces are loaded eight at a time.
 __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ inv_perm,
                                const float* __restrict__ w, int T, int d, int k, int has_shared,
                                uint16_t* __restrict__ Y, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int kJ = 8;
+  const int lane = threadIdx.x & 31;
   const size_t A = static_cast<size_t>(T) * k;
   const int d4 = d / 4;
-  const size_t total4 = static_cast<size_t>(T) * d4;
+  const int q4 = (d4 + 3) / 4;  // columns (float4) per quarter
   bool ok = true;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t t = i / d4;
-    const int n = static_cast<int>(i - t * d4) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int p = __ldg(inv_perm + t * k + j);
-      const float wj = __ldg(w + t * k + j);
-      if (p < 0 || static_cast<size_t>(p) >= A) {
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < 4 * T; wi += nw) {
+    const int t = wi >> 2;
+    const int cq0 = (wi & 3) * q4, cq1 = min(d4, cq0 + q4);
+    int pj = 0;
+    float wj = 0.0f;
+    if (lane < k) {
+      pj = __ldg(inv_perm + static_cast<size_t>(t) * k + lane);
+      wj = __ldg(w + static_cast<size_t>(t) * k + lane);
+      if (pj < 0 || static_cast<size_t>(pj) >= A) {
         ok = false;
-        continue;
+        pj = 0;
+        wj = 0.0f;
       }
-      const float4 v = *reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d + n);
-      acc.x = fmaf(wj, v.x, acc.x);
-      acc.y = fmaf(wj, v.y, acc.y);
-      acc.z = fmaf(wj, v.z, acc.z);
-      acc.w = fmaf(wj, v.w, acc.w);
     }
-    if (has_shared) {
-      const float4 v = *reinterpret_cast<const float4*>(ypart + (A + t) * d + n);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    const float4* sh = reinterpret_cast<const float4*>(ypart + (A + t) * d);
+    uint2* yt = reinterpret_cast<uint2*>(Y + static_cast<size_t>(t) * d);
+    for (int c = cq0 + lane; c < cq1; c += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < k; j0 += kJ) {
+        float4 v[kJ];
+        float wv[kJ];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+          const int jj = j0 + j < k ? j0 + j : 0;
+          const int p = __shfl_sync(0xffffffffu, pj, jj);
+          wv[j] = j0 + j < k ? __shfl_sync(0xffffffffu, wj, jj) : 0.0f;
+          v[j] = reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d)[c];
+        }
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+          if (j0 + j < k) {
+            acc.x = fmaf(wv[j], v[j].x, acc.x);
+            acc.y = fmaf(wv[j], v[j].y, acc.y);
+            acc.z = fmaf(wv[j], v[j].z, acc.z);
+            acc.w = fmaf(wv[j], v[j].w, acc.w);
+          }
+        }
+      }
+      if (has_shared) {
+        const float4 s0 = sh[c];
+        acc.x += s0.x;
+        acc.y += s0.y;
+        acc.z += s0.z;
+        acc.w += s0.w;
+      }
+      yt[c] = make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16),
+                         static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16));
     }
-    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(Y + t * d + n) = make_uint2(lo, hi);
   }
   if (!ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
@@ -611,7 +646,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
 
   {
     cudaLaunchConfig_t c2 = cfg;
-    c2.gridDim = dim3(a.num_sms * 2);
+    c2.gridDim = dim3(a.num_sms * 8);
     c2.blockDim = dim3(256);
     c2.dynamicSmemBytes = 0;
     const int rows = a.T * a.k + (a.I_shared > 0 ? a.T : 0);
@@ -637,7 +672,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 
-  cfg.gridDim = dim3(a.num_sms * 4);
+  cfg.gridDim = dim3((a.T + 1) / 2 < a.num_sms * 8 ? (a.T + 1) / 2 : a.num_sms * 8);  // 2 tokens per block of 8 warps
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   timer_begin(kKCombine, stream);

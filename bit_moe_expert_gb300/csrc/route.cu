@@ -33,14 +33,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
                                                               int k, int block_rows, RouteOut out,
                                                               WsHeader* hdr, uint32_t* status,
                                                               int32_t* __restrict__ chunk_hist,
-                                                              int32_t* __restrict__ local_rank, int bases_in_smem) {
+                                                              int32_t* __restrict__ local_rank, int bases_in_smem,
+                                                              int gridsync) {
   extern __shared__ int32_t s_bases[];  // [nchunks][E] exclusive per-chunk bases (last CTA, when they fit)
   __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
+  __shared__ float s_v[kRouteTokensPerCta * kMaxK];    // selected logits
+  __shared__ double s_ex[kRouteTokensPerCta * kMaxK];  // exp(l_j - l_max)
   __shared__ int32_t s_rank[kRouteTokensPerCta * kMaxK];
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ int32_t s_off[kMaxE + 1];
   __shared__ int32_t s_boff[kMaxE + 1];
   __shared__ int32_t s_part[2][kRouteThreads];
+  __shared__ int32_t s_base[kMaxE];  // grid-synchronised mode: this chunk's base within each expert
   __shared__ int s_is_last;
 
   pdl_wait();  // the previous kernel on the stream may still own our outputs
@@ -64,15 +68,32 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     float sel_v;
     bool finite;
     warp_topk_select<kPL>(row, E, k, lane, sel_i, sel_v, finite);
-    const float sel_w = warp_topk_weights(sel_v, k, lane);
     if (!finite && lane == 0) record_status(status, MOE_ERR_NONFINITE);
     if (lane < k) {
       out.ids[static_cast<size_t>(t) * k + lane] = sel_i;
-      out.w[static_cast<size_t>(t) * k + lane] = sel_w;
       s_ids[tl * k + lane] = sel_i;
+      s_v[tl * k + lane] = sel_v;
     }
   }
   __syncthreads();
+  // ---- weights: softmax over each token's selected logits in fp64 (summed in
+  // selection order, rounded once).  One assignment per thread, so every lane
+  // of a warp works (fp64 is slow on this GPU; a warp per token would leave
+  // most lanes idle).
+  {
+    const int na_ = ntok * k;
+    for (int a = threadIdx.x; a < na_; a += kRouteThreads) {
+      const int tl = a / k;
+      s_ex[a] = exp(static_cast<double>(s_v[a]) - static_cast<double>(s_v[tl * k]));
+    }
+    __syncthreads();
+    for (int a = threadIdx.x; a < na_; a += kRouteThreads) {
+      const int tl = a / k;
+      double sum = 0.0;
+      for (int j = 0; j < k; ++j) sum += s_ex[tl * k + j];
+      out.w[static_cast<size_t>(t0) * k + a] = static_cast<float>(s_ex[a] / sum);
+    }
+  }
 
   // ---- stable per-chunk ranks: one warp walks the chunk's assignments in order
   const int na = ntok * k;
@@ -96,7 +117,41 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   }
   __syncthreads();
 
-  if (nchunks > 1) {
+  if (nchunks > 1 && gridsync) {
+    // Every CTA is resident (the launch is sized for it): publish this chunk's
+    // counts, wait for every chunk (bounded spin), then each CTA derives the
+    // totals and its own chunk's bases and places its own assignments.
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) chunk_hist[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      atom_add_acq_rel_gpu(&hdr->ticket, 1u);
+      const long long tw = clock64();
+      while (ld_acquire_gpu(&hdr->ticket) < static_cast<uint32_t>(nchunks)) {
+        if (clock64() - tw > kWaitLimitCycles) {
+          record_status(status, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+      int run = 0, mine = 0;
+      for (int c0 = 0; c0 < nchunks; c0 += 8) {
+        int h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          h[i] = (c0 + i < nchunks) ? __ldcg(chunk_hist + static_cast<size_t>(c0 + i) * E + e) : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i == chunk) mine = run;
+          run += h[i];
+        }
+      }
+      s_cnt[e] = run;
+      s_base[e] = mine;
+    }
+    __syncthreads();
+  } else if (nchunks > 1) {
     // publish this chunk's counts and ranks, then the last CTA finishes
     for (int e = threadIdx.x; e < E; e += kRouteThreads) chunk_hist[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
     for (int a = threadIdx.x; a < na; a += kRouteThreads) local_rank[static_cast<size_t>(t0) * k + a] = s_rank[a];
@@ -132,7 +187,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     }
     __syncthreads();
   }
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) out.counts[e] = s_cnt[e];
+  const bool writer = !gridsync || chunk == 0;  // in grid-synchronised mode CTA 0 writes the per-expert outputs
+  if (writer)
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) out.counts[e] = s_cnt[e];
 
   // ---- exclusive scans over experts: row offsets and tile offsets
   {
@@ -194,22 +251,39 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += kRouteThreads) out.offsets[e] = s_off[e];
-  if (threadIdx.x == 0) *out.num_blocks = s_boff[E];
+  if (writer) {
+    for (int e = threadIdx.x; e <= E; e += kRouteThreads) out.offsets[e] = s_off[e];
+    if (threadIdx.x == 0) *out.num_blocks = s_boff[E];
 
-  // ---- block map
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
-    const int cnt = s_cnt[e];
-    int b = s_boff[e];
-    for (int r = 0; r < cnt; r += block_rows, ++b) {
-      out.block_map[3 * b + 0] = e;
-      out.block_map[3 * b + 1] = s_off[e] + r;
-      out.block_map[3 * b + 2] = min(block_rows, cnt - r);
+    // ---- block map
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+      const int cnt = s_cnt[e];
+      int b = s_boff[e];
+      for (int r = 0; r < cnt; r += block_rows, ++b) {
+        out.block_map[3 * b + 0] = e;
+        out.block_map[3 * b + 1] = s_off[e] + r;
+        out.block_map[3 * b + 2] = min(block_rows, cnt - r);
+      }
     }
   }
 
   // ---- scatter: position = offsets[e] + base of the chunk for e + rank within the chunk
-  if (nchunks == 1) {
+  if (nchunks > 1 && gridsync) {
+    for (int a = threadIdx.x; a < na; a += kRouteThreads) {
+      const int e = s_ids[a];
+      const int pos = s_off[e] + s_base[e] + s_rank[a];
+      const int ga = t0 * k + a;
+      out.perm[pos] = ga;
+      out.inv_perm[ga] = pos;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && atom_add_acq_rel_gpu(&hdr->route_done, 1u) == static_cast<uint32_t>(nchunks - 1)) {
+      // every CTA has passed the barrier: ready for the next call
+      hdr->ticket = 0;
+      hdr->route_done = 0;
+      __threadfence();
+    }
+  } else if (nchunks == 1) {
     for (int a = threadIdx.x; a < na; a += kRouteThreads) {
       const int pos = s_off[s_ids[a]] + s_rank[a];
       out.perm[pos] = a;
@@ -255,17 +329,29 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   const int bases_in_smem = (nchunks > 1 && bases_bytes <= static_cast<size_t>(kBasesSmemLimit)) ? 1 : 0;
 
   static bool attr_set = false;
+  static int resident[2] = {0, 0};  // CTAs of route_kernel<8>, <32> resident at once (no dynamic shared memory)
   if (!attr_set) {
     cudaError_t e1 = cudaFuncSetAttribute(route_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
     cudaError_t e2 = cudaFuncSetAttribute(route_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
     if (e1 != cudaSuccess) return e1;
     if (e2 != cudaSuccess) return e2;
+    int dev = 0, sms = 0, per8 = 0, per32 = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per8, route_kernel<8>, kRouteThreads, 0) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per32, route_kernel<32>, kRouteThreads, 0) == cudaSuccess) {
+      resident[0] = sms * per8;
+      resident[1] = sms * per32;
+    }
     attr_set = true;
   }
+  // Grid-synchronised mode when every chunk's CTA can be resident at once
+  // (leaving room for other work); otherwise the last CTA finishes alone.
+  const int gridsync = (nchunks > 1 && nchunks <= resident[E <= 256 ? 0 : 1] / 2) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunks);
   cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = bases_in_smem ? bases_bytes : 0;
+  cfg.dynamicSmemBytes = (bases_in_smem && !gridsync) ? bases_bytes : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -275,9 +361,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   timer_begin(kKRoute, stream);
   const cudaError_t err =
       E <= 256 ? cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, T, E, k, block_rows, out, hdr, status,
-                                    chunk_hist, local_rank, bases_in_smem)
+                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync)
                : cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, T, E, k, block_rows, out, hdr, status,
-                                    chunk_hist, local_rank, bases_in_smem);
+                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync);
   timer_end(kKRoute, stream);
   return err;
 }

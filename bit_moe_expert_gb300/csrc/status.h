@@ -14,7 +14,8 @@ struct WsHeader {
   uint32_t ticket;     // arrival counter of the routing kernel; reset by its last CTA
   uint32_t dec_arrive;  // decode kernel: CTAs that have written their partial output (grid barrier)
   uint32_t dec_done;    // decode kernel: CTAs that have finished; the last resets both
-  uint32_t pad[60];
+  uint32_t route_done;  // routing kernel (grid-synchronised mode): CTAs that have finished
+  uint32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 
