@@ -548,71 +548,46 @@ __global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* _
 }
 
 // Y[t] = bf16( sum_j w[t][j] * yexp[inv_perm[t*k + j]] + yexp[A + t] ): the
-// weighted top-k combine plus the shared expert, summed in slot order.  Four
-// warps per token, each a quarter of the columns; the lanes read the token's
-// k rows and weights once; the rows' 16-byte pieces are loaded eight at a time.
+// weighted top-k combine plus the shared expert, summed in slot order.
 __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ inv_perm,
                                const float* __restrict__ w, int T, int d, int k, int has_shared,
                                uint16_t* __restrict__ Y, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
-  constexpr int kJ = 8;
-  const int lane = threadIdx.x & 31;
   const size_t A = static_cast<size_t>(T) * k;
   const int d4 = d / 4;
-  const int q4 = (d4 + 3) / 4;  // columns (float4) per quarter
+  const size_t total4 = static_cast<size_t>(T) * d4;
   bool ok = true;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < 4 * T; wi += nw) {
-    const int t = wi >> 2;
-    const int cq0 = (wi & 3) * q4, cq1 = min(d4, cq0 + q4);
-    int pj = 0;
-    float wj = 0.0f;
-    if (lane < k) {
-      pj = __ldg(inv_perm + static_cast<size_t>(t) * k + lane);
-      wj = __ldg(w + static_cast<size_t>(t) * k + lane);
-      if (pj < 0 || static_cast<size_t>(pj) >= A) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t t = i / d4;
+    const int n = static_cast<int>(i - t * d4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int p = __ldg(inv_perm + t * k + j);
+      const float wj = __ldg(w + t * k + j);
+      if (p < 0 || static_cast<size_t>(p) >= A) {
         ok = false;
-        pj = 0;
-        wj = 0.0f;
+        continue;
       }
+      const float4 v = *reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d + n);
+      acc.x = fmaf(wj, v.x, acc.x);
+      acc.y = fmaf(wj, v.y, acc.y);
+      acc.z = fmaf(wj, v.z, acc.z);
+      acc.w = fmaf(wj, v.w, acc.w);
     }
-    const float4* sh = reinterpret_cast<const float4*>(ypart + (A + t) * d);
-    uint2* yt = reinterpret_cast<uint2*>(Y + static_cast<size_t>(t) * d);
-    for (int c = cq0 + lane; c < cq1; c += 32) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j0 = 0; j0 < k; j0 += kJ) {
-        float4 v[kJ];
-        float wv[kJ];
-#pragma unroll
-        for (int j = 0; j < kJ; ++j) {
-          const int jj = j0 + j < k ? j0 + j : 0;
-          const int p = __shfl_sync(0xffffffffu, pj, jj);
-          wv[j] = j0 + j < k ? __shfl_sync(0xffffffffu, wj, jj) : 0.0f;
-          v[j] = reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d)[c];
-        }
-#pragma unroll
-        for (int j = 0; j < kJ; ++j) {
-          if (j0 + j < k) {
-            acc.x = fmaf(wv[j], v[j].x, acc.x);
-            acc.y = fmaf(wv[j], v[j].y, acc.y);
-            acc.z = fmaf(wv[j], v[j].z, acc.z);
-            acc.w = fmaf(wv[j], v[j].w, acc.w);
-          }
-        }
-      }
-      if (has_shared) {
-        const float4 s0 = sh[c];
-        acc.x += s0.x;
-        acc.y += s0.y;
-        acc.z += s0.z;
-        acc.w += s0.w;
-      }
-      yt[c] = make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16),
-                         static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-                             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16));
+    if (has_shared) {
+      const float4 v = *reinterpret_cast<const float4*>(ypart + (A + t) * d + n);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
     }
+    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+    *reinterpret_cast<uint2*>(Y + t * d + n) = make_uint2(lo, hi);
   }
   if (!ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
@@ -672,7 +647,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 
-  cfg.gridDim = dim3((a.T + 1) / 2 < a.num_sms * 8 ? (a.T + 1) / 2 : a.num_sms * 8);  // 2 tokens per block of 8 warps
+  cfg.gridDim = dim3(a.num_sms * 4);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   timer_begin(kKCombine, stream);
