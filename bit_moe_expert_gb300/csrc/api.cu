@@ -51,25 +51,17 @@ bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuui
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, sw);
 }
 
-// The same codes seen as [E*K/64][N/4][32]: 128-byte super-rows of four
-// consecutive rows of one group (N a multiple of 4); a box covers box_sr
-// super-rows of one group
-bool encode_codes_sr(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_sr) {
+// The same codes seen as [E][K/64][N*8]: the pieces of consecutive rows of
+// one group are contiguous, so a box of box_rows rows (box_rows*32 bytes, at
+// most 1 KiB) is one line; box_groups consecutive groups of one expert
+// (groups past the last read as zeros)
+bool encode_codes_rows(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_rows,
+                       cuuint32_t box_groups) {
   const int G = K / 64;
-  const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(N / 4), static_cast<cuuint64_t>(E) * G};
-  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(N) * 32};
-  const cuuint32_t box[3] = {32, box_sr, 1};
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N) * 8, static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 32, static_cast<cuuint64_t>(N) * 32 * G};
+  const cuuint32_t box[3] = {box_rows * 8, box_groups, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// group parameters sb [E][K/64][N] seen as [E*K/64][N/4][4]: a box covers
-// 4 * box_sr consecutive rows of one group
-bool encode_groups_sr(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_sr) {
-  const int G = K / 64;
-  const cuuint64_t dims[3] = {4, static_cast<cuuint64_t>(N / 4), static_cast<cuuint64_t>(E) * G};
-  const cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(N) * 4};
-  const cuuint32_t box[3] = {4, box_sr, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // fp16 activations [rows][cols]: boxes of 64 columns (128 bytes) x kGemmBN
@@ -118,7 +110,7 @@ enum class Path { kGemv, kGemm };
 
 // Forward workspace: header, then one region used by either path.
 struct FwdLayout {
-  size_t dec_part;                                           // fp32 partial outputs of the decode kernel
+  size_t dec_h;                                              // h records of the decode kernel
   size_t gemm_h_routed, gemm_h_shared, gemm_ypart, gemm_xh;  // fp16, fp16, fp32, fp16
   size_t total;
 };
@@ -128,8 +120,8 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
   const size_t A = static_cast<size_t>(T) * k;
   size_t o = sizeof(WsHeader);
   const size_t base = o;
-  L.dec_part = o;
-  o = round256(o + (T <= kGemvMaxT ? decode_partial_bytes(T, d) : 0));
+  L.dec_h = o;
+  o = round256(o + (T <= kGemvMaxT ? decode_scratch_bytes(T, I, I_shared) : 0));
   const size_t dec_end = o;
   o = base;
   L.gemm_h_routed = o;
@@ -274,23 +266,22 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
 
   if (path == Path::kGemv) {
     DecodeMaps mr, ms;
-    const int KB1 = d / 64;
-    const cuuint32_t bsr = static_cast<cuuint32_t>(decode_box_superrows(d));
-    bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              encode_codes(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              encode_codes_sr(&mr.q_down, routed->down.q, E, d, I, bsr) &&
-              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, KB1) &&
-              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, KB1) &&
-              encode_groups_sr(&mr.sb_down, routed->down.sb, E, d, I, bsr);
-    if (ok && shared)
-      ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode_codes_sr(&ms.q_down, shared->down.q, 1, d, I_shared, bsr) &&
-           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
-           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, KB1) &&
-           encode_groups_sr(&ms.sb_down, shared->down.sb, 1, d, I_shared, bsr);
+    const cuuint32_t G2 = static_cast<cuuint32_t>(I / 64);
+    bool ok = encode_codes_rows(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+              encode_codes_rows(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+              encode_codes_rows(&mr.q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2) &&
+              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+              encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kDecodeRowsDown, G2);
+    if (ok && shared) {
+      const cuuint32_t G2s = static_cast<cuuint32_t>(I_shared / 64);
+      ok = encode_codes_rows(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+           encode_codes_rows(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+           encode_codes_rows(&ms.q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s) &&
+           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+           encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kDecodeRowsDown, G2s);
+    }
     if (!ok) return MOE_ERR_CUDA;
     DecodeArgs a{};
     a.X = X;
@@ -300,7 +291,7 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
     a.out = RouteOut{r->ids, r->w, r->counts, r->offsets, r->perm, r->inv_perm, r->block_map, r->num_blocks};
     a.block_rows = r->block_rows;
     a.Y = Y;
-    a.part = reinterpret_cast<float*>(wsb + L.dec_part);
+    a.hbuf = reinterpret_cast<uint8_t*>(wsb + L.dec_h);
     a.status = status;
     a.T = T;
     a.d = d;

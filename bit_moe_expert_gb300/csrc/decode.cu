@@ -1,36 +1,43 @@
-// Decode path (T <= 4 tokens): the expert projections as matrix-vector
-// products on the CUDA cores.  "Perplexity's Lily Beats MLX-LM on MacBook M5",
-// section "Prefill and decode are different problems": batch-1 decode is a
-// GEMV bound by memory bandwidth that belongs on the vector ALUs; section
-// "Decode: minimize bytes per token": the expert input projections are fused
-// with the gate activation and the output projection with the routing scores
-// and the shared expert.
+// Decode path (T <= 4 tokens).  "Perplexity's Lily Beats MLX-LM on MacBook
+// M5", section "Prefill and decode are different problems": batch-1 decode is
+// a matrix-vector product bound by memory bandwidth; section "Decode: minimize
+// bytes per token": the expert input projections are fused with the gate
+// activation and the output projection with the routing scores and the
+// shared expert, and every weight byte is read once.
 //
-// Design (sm_103a): one launch per layer, clusters of two CTAs, no grid-wide
-// barrier.  A unit of work is one group of 64 intermediate features of one
-// active expert (the shared expert's groups first, then the distinct routed
-// experts of the call).  The two CTAs of a cluster split a unit:
-//   gate/up  CTA r computes h = silu(x Wg^T) * (x Wu^T) for features
-//            [64g + 32r, 64g + 32r + 32) of every token and writes them into
-//            both CTAs' shared memory (distributed shared memory), then a
-//            cluster barrier;
-//   down     CTA r multiplies rows [r d/2, (r+1) d/2) of the down projection,
-//            restricted to the group's 64 columns (one quantisation group, 32
-//            bytes of codes per row), by the 64 h values and accumulates the
-//            routing-weighted result in registers.
-// Every byte of an active expert's three matrices is loaded once, by TMA,
-// issued up front in few large boxes (the codes are stored group-major, so a
-// group of many rows is one contiguous block); the next unit's loads start as
-// soon as a buffer is free.
-// Each cluster writes its partial output rows; after one barrier over the
-// grid every CTA sums a few output rows over the clusters in a fixed order, so
-// the result does not depend on timing.
+// Design (sm_103a): one launch per layer, one CTA per SM, two phases around
+// one barrier over the grid.
+//   phase 1  an item is 32 rows of the gate and up projections of one active
+//            expert (the shared expert's items first).  CTA c takes items c,
+//            c + grid, ...; it computes h = silu(x Wg^T) * (x Wu^T) for those
+//            32 features of every token and writes it, in fp16, to the slot's
+//            h record in global memory, with the sums of each 32 values.
+//   barrier  every h record is complete.
+//   phase 2  CTA c takes output rows [16c, 16c + 16) (and c + grid, ...): the
+//            down projection of every active expert restricted to those rows,
+//            times that expert's h and the token's routing weight, summed over
+//            the experts, gives Y directly; nothing is reduced across CTAs.
+// Every weight byte is loaded once by TMA into a ring of shared-memory stages
+// (phase 1: chunks of 8 groups of 64 columns; phase 2: 16 rows of one expert),
+// issued as soon as the routing is known (the shared expert's before the wait
+// for the previous kernel); the phase-2 down rows load while phase 1 runs.
 //
-// Arithmetic: a 4-bit code becomes the fp32 value 128 + q with one byte
-// permute (exponent of 128, code in the low mantissa bits); products with x
-// use packed fp32x2 FMAs; the affine map is applied once per 64-column group:
-//   sum_k (q_k s + b) x_k = s * sum_k (128 + q_k) x_k + (b - 128 s) * sum_k x_k.
+// Arithmetic on the tensor cores (mma.sync m16n8k16, fp32 accumulators):
+// weight rows are the 16 rows of the MMA, tokens its 8 columns (T <= 4 used).
+// A code becomes 128 + q (bf16) or 1024 + q (fp16) with one mask (the codes of
+// a word are interleaved: columns 2p and 2p+1 in bits 4p and 4p+16), and the
+// affine map of each 64-column group is applied to the group's MMA result:
+//   sum_k (q_k s + b) v_k = s * sum_k (M + q_k) v_k + (b - M s) * sum_k v_k.
+// Phase 1 multiplies bf16 codes with the bf16 activations (exact products);
+// phase 2 multiplies fp16 codes with fp16 h.
+//
+// The K order inside the MMA: lane (g, q) of a row holds the row's words 2q
+// and 2q+1 of a group (an 8-byte load); step m of the group's four MMA steps
+// takes code pairs 2(m&1) and 2(m&1)+1 of word 2q + (m>>1), which are columns
+// 16q + 4m + {0,1} and + {2,3} of the group, so its activation operand is four
+// consecutive values of the token (columns 16q .. 16q+15 over the four steps).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -43,321 +50,266 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRows = kDecodeRowsGU;              // gate/up rows per CTA and unit (lane = row)
-constexpr int kPairs = kThreads / 2;              // down rows are taken by thread pairs
-constexpr int kChunkGroups = kDecodeChunkGroups;  // gate/up codes arrive in chunks of groups, one barrier each
+constexpr int kRows1 = kDecodeRowsGU;           // gate/up rows per phase-1 item
+constexpr int kChunk = kDecodeChunkGroups;      // groups per phase-1 stage
+constexpr int kRows2 = kDecodeRowsDown;         // output rows per phase-2 block
+constexpr int kS1 = 5;                          // phase-1 stages
+constexpr int kS2Max = 12;                      // phase-2 stages at most
 constexpr int kMaxSlots = kMaxK * kGemvMaxT + 1;  // distinct experts of a call, plus the shared one
-constexpr uint32_t kMagic128 = 0x43000000u;  // fp32 128.0: a code in bits 16..19 reads as 128 + q
+constexpr uint32_t kCodeQ = kChunk * kRows1 * 32;   // bytes of one matrix's codes in a phase-1 stage
+constexpr uint32_t kCodeSB = kChunk * kRows1 * 4;   // bytes of one matrix's group parameters in a stage
+constexpr uint32_t kSt1 = 2 * kCodeQ + 2 * kCodeSB;  // phase-1 stage: gate codes, up codes, gate sb, up sb
+constexpr size_t kSmemMax = 227 * 1024;
+
+static_assert(kWarps == 2 * kChunk, "phase 1 gives one warp to each (matrix, group) of a stage");
+static_assert(kRows1 == 32 && kRows2 == 16, "fragment layout");
 
 __host__ __device__ constexpr int div_up(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  int KB1, nchunk, half, nboxd, box_sr;
-  size_t sb1_slot, qgu, qd, sbgu, sbd, accd, xs, sx, red, hb, hsb, wt, slot_e, rid, misc, bars, total;
+  int G1, nchunk, Imax, hs_stride, S2;
+  size_t hrec;                // bytes of one slot's h record: h fp16 [T][Imax], then half-group sums fp32 [T][hs_stride]
+  size_t st2, st2_sb, st2_h;  // phase-2 stage bytes; offsets of its parameters and its h record
+  size_t ring1, xs, sx, red1, red2, wt, slot_e, rid, bk, misc, cnt, bars, ring2, total;
 };
 
-// TMA destinations start on 128 bytes.
-__host__ __device__ inline Layout layout(int T, int d) {
+// TMA and bulk-copy destinations start on 128 bytes.
+__host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
   Layout L;
-  L.KB1 = d / 64;
-  L.nchunk = div_up(L.KB1, kChunkGroups);
-  L.half = d / 2;
-  const int sr = d / 8;  // 128-byte super-rows (4 rows of 32 bytes) in a half of the down rows
-  L.nboxd = div_up(sr, 256);
-  L.box_sr = static_cast<int>(round_up(div_up(sr, L.nboxd), 8));
-  L.sb1_slot = round_up(static_cast<size_t>(L.KB1) * kRows * 4, 128);
+  L.G1 = d / 64;
+  L.nchunk = div_up(L.G1, kChunk);
+  L.Imax = I > I_shared ? I : I_shared;
+  const int G2max = L.Imax / 64;
+  L.hs_stride = static_cast<int>(round_up(L.Imax / 32, 4));
+  L.hrec = static_cast<size_t>(T) * L.Imax * 2 + static_cast<size_t>(T) * L.hs_stride * 4;
+  L.st2_sb = static_cast<size_t>(G2max) * kRows2 * 32;  // codes [G2][16 rows][8 words]
+  L.st2_h = round_up(L.st2_sb + static_cast<size_t>(G2max) * kRows2 * 4, 128);
+  L.st2 = round_up(L.st2_h + L.hrec, 128);
   size_t o = 0;
-  L.qgu = o;  // gate codes [KB1][32 rows][32 B], then up codes
-  o += 2ull * L.nchunk * kChunkGroups * kRows * 32;
-  L.qd = o;  // down codes of the unit's group: [rows of this half][32 B]
-  o += static_cast<size_t>(L.nboxd) * L.box_sr * 128;
-  L.sbgu = o;
-  o += 2 * L.sb1_slot;
-  L.sbd = o;
-  o += static_cast<size_t>(L.nboxd) * L.box_sr * 16;
-  L.accd = o;  // down accumulators [rows of this half][T]
-  o += static_cast<size_t>(L.half) * T * 4;
-  o = round_up(o, 16);
-  L.xs = o;  // x of every token, fp32 [T][d]
-  o += static_cast<size_t>(T) * d * 4;
-  L.sx = o;  // sums of x over each half group of 32 columns [T][d/32]
-  o += static_cast<size_t>(T) * 2 * L.KB1 * 4;
-  o = round_up(o, 16);
-  L.red = o;  // gate and up partial dots [2][warp][row][T]
-  o += 2ull * kWarps * kRows * T * 4;
-  L.hb = o;  // h of the unit's 64 features, two buffers [2][T][64]
-  o += 2ull * T * 64 * 4;
-  L.hsb = o;  // the two halves' sums of h, [2][T][2]
-  o += 2ull * T * 2 * 4;
+  L.ring1 = o;
+  o += static_cast<size_t>(kS1) * kSt1;
+  L.xs = o;  // x of every token, bf16 [T][d]
+  o += round_up(static_cast<size_t>(T) * d * 2, 128);
+  L.sx = o;  // sums of x over each group [T][G1]
+  o += round_up(static_cast<size_t>(T) * L.G1 * 4, 16);
+  L.red1 = o;  // phase-1 partial dots [warp][32 rows][T]
+  o += static_cast<size_t>(kWarps) * kRows1 * T * 4;
+  L.red2 = o;  // phase-2 partial rows [warp][16 rows][T]
+  o += static_cast<size_t>(kWarps) * kRows2 * T * 4;
   L.wt = o;  // routing weight of each slot for each token [slot][T]
   o += static_cast<size_t>(kMaxSlots) * T * 4;
   L.slot_e = o;  // expert of each slot
-  o += kMaxSlots * 4;
+  o += round_up(kMaxSlots * 4, 16);
   L.rid = o;  // the call's assignments: expert [T*k], weight [T*k], slot [T*k]
   o += 3ull * T * kMaxK * 4;
-  L.misc = o;  // slot count, arrival ticket
+  L.bk = o;  // routing outputs' scratch: counts [E], offsets [E+1], tile offsets [E+1] (E <= 256)
+  o += 3 * 260 * 4;
+  L.misc = o;  // distinct routed experts
   o += 16;
+  L.cnt = o;  // per-stage consumption counters; the job each phase-2 stage was last issued
+  o += (kS1 + 2 * kS2Max) * 4;
   o = round_up(o, 8);
-  L.bars = o;  // gate/up code chunks, gate/up group parameters, down boxes, two h exchanges
-  o += static_cast<size_t>(L.nchunk + 1 + L.nboxd + 2) * 8;
-  L.total = o + 128;  // room to align the dynamic shared memory base
+  L.bars = o;  // phase-1 stages, phase-2 codes, phase-2 h records, x
+  o += static_cast<size_t>(kS1 + 2 * kS2Max + 1) * 8;
+  o = round_up(o, 128);
+  L.ring2 = o;
+  const size_t room = kSmemMax > o + 128 ? kSmemMax - o - 128 : 0;
+  size_t s2 = room / L.st2;
+  if (s2 > kS2Max) s2 = kS2Max;
+  L.S2 = static_cast<int>(s2);
+  L.total = o + s2 * L.st2 + 128;  // room to align the dynamic shared memory base
   return L;
 }
 
-struct Unit {
-  int g, slot;
-  bool shared;
-};
-
-// The shared expert's groups come first (they need no routing), then each
-// routed slot's groups.
-__device__ __forceinline__ Unit unit_of(int u, int Gs, int G, bool has_shared) {
-  Unit m;
-  if (u < Gs) {
-    m.shared = true;
-    m.g = u;
-    m.slot = 0;
-  } else {
-    const int v = u - Gs;
-    m.shared = false;
-    m.slot = (has_shared ? 1 : 0) + v / G;
-    m.g = v % G;
-  }
-  return m;
-}
-
-// Four fp32 pairs (128 + q) for the eight codes of one word, in k order.
-__device__ __forceinline__ void codes8(uint32_t w, float2 (&q)[4]) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;         // codes 0, 2, 4, 6 in bytes 0..3
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // codes 1, 3, 5, 7
-  q[0] = make_float2(__uint_as_float(prmt(lo, kMagic128, 0x7054)), __uint_as_float(prmt(hi, kMagic128, 0x7054)));
-  q[1] = make_float2(__uint_as_float(prmt(lo, kMagic128, 0x7154)), __uint_as_float(prmt(hi, kMagic128, 0x7154)));
-  q[2] = make_float2(__uint_as_float(prmt(lo, kMagic128, 0x7254)), __uint_as_float(prmt(hi, kMagic128, 0x7254)));
-  q[3] = make_float2(__uint_as_float(prmt(lo, kMagic128, 0x7354)), __uint_as_float(prmt(hi, kMagic128, 0x7354)));
-}
-
-// sum over eight codes of (128 + q) * x for every token; x at xp[t * stride].
-template <int kT>
-__device__ __forceinline__ void word_dot(uint32_t w, const float* xp, int stride, float2 (&acc)[kT]) {
-  float2 q[4];
-  codes8(w, q);
+// Four MMA steps over one 64-column group (see the K order above).
+//   wa, wb: words 2q, 2q+1 of rows g and g+8; b: the activation operand of
+//   the four steps (columns 16q .. 16q+15 of the group, token g).
+template <bool kBF16>
+__device__ __forceinline__ void mma_group(uint2 wa, uint2 wb, const uint32_t (&b)[8], float (&dd)[4]) {
+  constexpr uint32_t magic = kBF16 ? 0x43004300u : 0x64006400u;  // pairs (128, 128) / (1024, 1024)
 #pragma unroll
-  for (int t = 0; t < kT; ++t) {
-    const float4 xa = *reinterpret_cast<const float4*>(xp + t * stride);
-    const float4 xb = *reinterpret_cast<const float4*>(xp + t * stride + 4);
-    acc[t] = f32x2_fma(q[0], make_float2(xa.x, xa.y), acc[t]);
-    acc[t] = f32x2_fma(q[1], make_float2(xa.z, xa.w), acc[t]);
-    acc[t] = f32x2_fma(q[2], make_float2(xb.x, xb.y), acc[t]);
-    acc[t] = f32x2_fma(q[3], make_float2(xb.z, xb.w), acc[t]);
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t xa = m < 2 ? wa.x : wa.y;
+    const uint32_t xb = m < 2 ? wb.x : wb.y;
+    const int sh = (m & 1) * 8;
+    const uint32_t a0 = lop3_and_or(xa >> sh, 0x000F000Fu, magic);
+    const uint32_t a1 = lop3_and_or(xb >> sh, 0x000F000Fu, magic);
+    const uint32_t a2 = lop3_and_or(xa >> (sh + 4), 0x000F000Fu, magic);
+    const uint32_t a3 = lop3_and_or(xb >> (sh + 4), 0x000F000Fu, magic);
+    mma_16816<kBF16>(dd, a0, a1, a2, a3, b[2 * m], b[2 * m + 1]);
   }
 }
 
-// One gate/up row's contribution from half (32 columns) of one group, for
-// every token, for gate and up together (they share the x loads).
-//   qg, qu: codes [groups][32 rows][32 bytes]; xs: x [T][d]; sx: sums of x
-//   over each half group [T][nh]
-template <int kT>
-__device__ __forceinline__ void half_group_dot2(const uint8_t* qg, const uint8_t* qu, int row, int kb, int hh,
-                                                const float* xs, int d, const float* sx, int nh, uint32_t sbg,
-                                                uint32_t sbu, float (&og)[kT], float (&ou)[kT]) {
-  const int off = (kb * kRows + row) * 32 + hh * 16;
-  const uint4 wg = *reinterpret_cast<const uint4*>(qg + off);
-  const uint4 wu = *reinterpret_cast<const uint4*>(qu + off);
-  const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
-  const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
-  float2 ag[kT], au[kT];
-#pragma unroll
-  for (int t = 0; t < kT; ++t) ag[t] = au[t] = make_float2(0.0f, 0.0f);
-  const float* xg = xs + kb * 64 + hh * 32;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float2 qa[4], qb[4];
-    codes8(gw[j], qa);
-    codes8(uw[j], qb);
-#pragma unroll
-    for (int t = 0; t < kT; ++t) {
-      const float4 xa = *reinterpret_cast<const float4*>(xg + t * d + 8 * j);
-      const float4 xb = *reinterpret_cast<const float4*>(xg + t * d + 8 * j + 4);
-      ag[t] = f32x2_fma(qa[0], make_float2(xa.x, xa.y), ag[t]);
-      au[t] = f32x2_fma(qb[0], make_float2(xa.x, xa.y), au[t]);
-      ag[t] = f32x2_fma(qa[1], make_float2(xa.z, xa.w), ag[t]);
-      au[t] = f32x2_fma(qb[1], make_float2(xa.z, xa.w), au[t]);
-      ag[t] = f32x2_fma(qa[2], make_float2(xb.x, xb.y), ag[t]);
-      au[t] = f32x2_fma(qb[2], make_float2(xb.x, xb.y), au[t]);
-      ag[t] = f32x2_fma(qa[3], make_float2(xb.z, xb.w), ag[t]);
-      au[t] = f32x2_fma(qb[3], make_float2(xb.z, xb.w), au[t]);
-    }
+// The activation operand: 16 consecutive 16-bit values at p (zero when the
+// lane's token does not exist).
+__device__ __forceinline__ void load_b(const uint16_t* p, bool valid, uint32_t (&b)[8]) {
+  uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+  if (valid) {
+    v0 = *reinterpret_cast<const uint4*>(p);
+    v1 = *reinterpret_cast<const uint4*>(p + 8);
   }
-  const float s1 = __uint_as_float(sbg << 16), c1 = __uint_as_float(sbg & 0xFFFF0000u) - 128.0f * s1;
-  const float s2 = __uint_as_float(sbu << 16), c2 = __uint_as_float(sbu & 0xFFFF0000u) - 128.0f * s2;
-#pragma unroll
-  for (int t = 0; t < kT; ++t) {
-    const float sxv = sx[t * nh + 2 * kb + hh];
-    og[t] += fmaf(s1, ag[t].x + ag[t].y, c1 * sxv);
-    ou[t] += fmaf(s2, au[t].x + au[t].y, c2 * sxv);
-  }
+  b[0] = v0.x;
+  b[1] = v0.y;
+  b[2] = v0.z;
+  b[3] = v0.w;
+  b[4] = v1.x;
+  b[5] = v1.y;
+  b[6] = v1.z;
+  b[7] = v1.w;
 }
 
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+// Waits (bounded) until *slot, written by another warp of the CTA, reaches
+// `job`; returns true when it gave up.
+__device__ __forceinline__ bool issued2_wait(const int* slot, int job) {
+  if (*reinterpret_cast<const volatile int*>(slot) >= job) return false;
+  const long long t0 = clock64();
+  while (*reinterpret_cast<const volatile int*>(slot) < job)
+    if (clock64() - t0 > kWaitLimitCycles) return true;
+  return false;
 }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 template <int kT>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap qg_r, const __grid_constant__ CUtensorMap qu_r,
-                  const __grid_constant__ CUtensorMap sbg_r, const __grid_constant__ CUtensorMap sbu_r,
-                  const __grid_constant__ CUtensorMap qd_r, const __grid_constant__ CUtensorMap sbd_r,
-                  const __grid_constant__ CUtensorMap qg_s, const __grid_constant__ CUtensorMap qu_s,
-                  const __grid_constant__ CUtensorMap sbg_s, const __grid_constant__ CUtensorMap sbu_s,
-                  const __grid_constant__ CUtensorMap qd_s, const __grid_constant__ CUtensorMap sbd_s,
-                  DecodeArgs a, WsHeader* hdr) {
+    decode_kernel(const __grid_constant__ DecodeMaps mr, const __grid_constant__ DecodeMaps ms, const DecodeArgs a,
+                  WsHeader* hdr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int d = a.d;
-  const Layout L = layout(kT, d);
-  const bool has_shared = a.I_shared > 0;
-  const int G = a.I / 64, Gs = a.I_shared / 64;
+  const Layout L = layout(kT, d, a.I, a.I_shared);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cl = static_cast<int>(blockIdx.x >> 1);
+  const int g8 = lane >> 2, q4 = lane & 3;  // MMA fragment row group and column pair
+  const int nC = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const bool fused = a.logits != nullptr;
-  // with fused routing the last cluster takes no unit: its first CTA writes the routing outputs
-  const int ncl = static_cast<int>(gridDim.x >> 1) - (fused ? 1 : 0);
-  const bool bookkeeper = fused && cl == ncl && rank == 0;
+  const bool has_shared = a.I_shared > 0;
+  const int rs0 = has_shared ? 1 : 0;
+  const int it_r = a.I / kRows1, it_s = a.I_shared / kRows1;  // phase-1 items per routed / shared expert
+  const int G2 = a.I / 64, G2s = a.I_shared / 64;               // phase-2 groups per routed / shared slot
+  const int nrb = d / kRows2;
+  const int my_rbs = cta < nrb ? div_up(nrb - cta, nC) : 0;
+  const bool bookkeeper = fused && cta == nC - 1;
 
-  uint8_t* qg = smem + L.qgu;
-  uint8_t* qu = qg + static_cast<size_t>(L.nchunk) * kChunkGroups * kRows * 32;
-  const uint8_t* qd = smem + L.qd;
-  const uint32_t* sbg = reinterpret_cast<const uint32_t*>(smem + L.sbgu);
-  const uint32_t* sbu = reinterpret_cast<const uint32_t*>(smem + L.sbgu + L.sb1_slot);
-  const uint32_t* sbd = reinterpret_cast<const uint32_t*>(smem + L.sbd);
-  float* accd = reinterpret_cast<float*>(smem + L.accd);
-  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  uint8_t* ring1 = smem + L.ring1;
+  uint8_t* ring2 = smem + L.ring2;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
   float* sx = reinterpret_cast<float*>(smem + L.sx);
-  float* red = reinterpret_cast<float*>(smem + L.red);
-  float* hb = reinterpret_cast<float*>(smem + L.hb);
-  float* hsb = reinterpret_cast<float*>(smem + L.hsb);
+  float* red1 = reinterpret_cast<float*>(smem + L.red1);
+  float* red2 = reinterpret_cast<float*>(smem + L.red2);
   float* wt = reinterpret_cast<float*>(smem + L.wt);
   int* slot_e = reinterpret_cast<int*>(smem + L.slot_e);
   int* s_ids = reinterpret_cast<int*>(smem + L.rid);
   float* s_w = reinterpret_cast<float*>(smem + L.rid + static_cast<size_t>(kT) * kMaxK * 4);
   int* s_slot = reinterpret_cast<int*>(smem + L.rid + 2ull * kT * kMaxK * 4);
   int* misc = reinterpret_cast<int*>(smem + L.misc);
-  uint64_t* bar_gu = reinterpret_cast<uint64_t*>(smem + L.bars);  // one per code chunk
-  uint64_t* bar_sb = bar_gu + L.nchunk;
-  uint64_t* bar_d = bar_sb + 1;
-  uint64_t* bar_h = bar_d + L.nboxd;  // [2]: the other CTA's h values of a unit have arrived
+  int* cnt1 = reinterpret_cast<int*>(smem + L.cnt);
+  int* cnt2 = cnt1 + kS1;
+  int* issued2 = cnt2 + kS2Max;
+  uint64_t* full1 = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* full2c = full1 + kS1;
+  uint64_t* full2h = full2c + kS2Max;
+  uint64_t* bar_x = full2h + kS2Max;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < L.nchunk + 1 + L.nboxd; ++b) mbar_init(&bar_gu[b], 1);
-    // an h exchange completes with the expected bytes from the other CTA, one
-    // arrival with the byte count and one per exchanging warp of this CTA
-    mbar_init(&bar_h[0], 1 + kT);
-    mbar_init(&bar_h[1], 1 + kT);
+    for (int i = 0; i < kS1 + 2 * kS2Max + 1; ++i) mbar_init(&full1[i], 1);
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < L.half * kT; i += kThreads) accd[i] = 0.0f;
+  for (int i = threadIdx.x; i < kS1 + kS2Max; i += kThreads) cnt1[i] = 0;
+  for (int i = threadIdx.x; i < kS2Max; i += kThreads) issued2[i] = i;  // stage s first holds job s
   for (int i = threadIdx.x; i < kMaxSlots * kT; i += kThreads) wt[i] = 0.0f;
   __syncthreads();
-  cluster_arrive_relaxed();  // matched by a wait before the first write into the other CTA
 
-  // The lanes of warp 0 issue a unit's loads in parallel: lane c < nchunk the
-  // gate and up codes of groups [8c, 8c+8) (32 rows each), lane nchunk the
-  // gate/up group parameters, the next nboxd lanes the down rows of this CTA's
-  // half for the unit's group (codes and parameters).
-  // Warp 0 issues a unit's loads without divergence: first every barrier's
-  // byte count (one lane per barrier), then one TMA copy per lane:
-  //   copies 0, 1:               gate and up group parameters
-  //   copies 2c+2, 2c+3:         gate and up codes of groups [8c, 8c+8), 32 rows (c < nchunk)
-  //   then per down box b:       down codes and parameters of this CTA's half, the unit's group
-  auto issue = [&](const Unit& m, int e) {
-    const uint64_t pol = l2_policy_evict_first();  // every weight byte is read once
-    const int n0 = m.g * 64 + static_cast<int>(rank) * kRows;
-    const int Ge = m.shared ? Gs : G;
-    const uint32_t cbytes = kChunkGroups * kRows * 32;
-    if (lane < L.nchunk + 1 + L.nboxd) {
-      uint64_t* bar;
-      uint32_t bytes;
-      if (lane < L.nchunk) {
-        bar = &bar_gu[lane];
-        bytes = 2 * cbytes;
-      } else if (lane == L.nchunk) {
-        bar = bar_sb;
-        bytes = static_cast<uint32_t>(2 * L.KB1 * kRows * 4);
-      } else {
-        bar = &bar_d[lane - L.nchunk - 1];
-        bytes = static_cast<uint32_t>(L.box_sr * (128 + 16));
-      }
-      mbar_arrive_expect_tx(bar, bytes);
-    }
-    __syncwarp();
-    const int ncopy = 2 * (L.nchunk + 1 + L.nboxd);
-    if (lane < ncopy) {
-      // the group parameters first: every gate/up product needs them
-      const int slot = lane >> 1, second = lane & 1;
-      const int which = slot == 0 ? L.nchunk : slot - 1 < L.nchunk ? slot - 1 : slot;
-      const CUtensorMap* map;
-      void* dst;
-      uint64_t* bar;
-      int c1, c2;
-      if (which < L.nchunk) {
-        map = second ? (m.shared ? &qu_s : &qu_r) : (m.shared ? &qg_s : &qg_r);
-        dst = (second ? qu : qg) + static_cast<size_t>(which) * cbytes;
-        bar = &bar_gu[which];
-        c1 = n0;
-        c2 = e * L.KB1 + which * kChunkGroups;
-      } else if (which == L.nchunk) {
-        map = second ? (m.shared ? &sbu_s : &sbu_r) : (m.shared ? &sbg_s : &sbg_r);
-        dst = smem + L.sbgu + (second ? L.sb1_slot : 0);
-        bar = bar_sb;
-        c1 = 0;
-        c2 = e;
-      } else {
-        const int b = which - L.nchunk - 1;
-        map = second ? (m.shared ? &sbd_s : &sbd_r) : (m.shared ? &qd_s : &qd_r);
-        dst = second ? smem + L.sbd + static_cast<size_t>(b) * L.box_sr * 16
-                     : smem + L.qd + static_cast<size_t>(b) * L.box_sr * 128;
-        bar = &bar_d[b];
-        c1 = static_cast<int>(rank) * (L.half / 4) + b * L.box_sr;
-        c2 = e * Ge + m.g;
-      }
-      // the gate/up parameter boxes start at row n0 (their first coordinate)
-      tma_load_3d_hint(dst, map, bar, which == L.nchunk ? n0 : 0, c1, c2, pol);
+  // ------------------------------------------------------------ loads
+  // Phase-1 job j of this CTA: chunk j % nchunk of its item j / nchunk.
+  auto item_slot = [&](int it, int& slot, int& rb) {
+    if (it < it_s) {
+      slot = 0;
+      rb = it;
+    } else {
+      const int v = it - it_s;
+      slot = rs0 + v / it_r;
+      rb = v % it_r;
     }
   };
+  auto issue1 = [&](int j, uint64_t pol) {
+    const int stage = j % kS1, ch = j % L.nchunk;
+    int slot, rb;
+    item_slot(cta + (j / L.nchunk) * nC, slot, rb);
+    const bool sh = has_shared && slot == 0;
+    const int e = sh ? 0 : slot_e[slot];
+    const DecodeMaps& m = sh ? ms : mr;
+    uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1;
+    uint64_t* bar = &full1[stage];
+    mbar_arrive_expect_tx(bar, kSt1);
+    tma_load_3d_hint(st, &m.q_gate, bar, rb * kRows1 * 8, ch * kChunk, e, pol);
+    tma_load_3d_hint(st + kCodeQ, &m.q_up, bar, rb * kRows1 * 8, ch * kChunk, e, pol);
+    tma_load_3d_hint(st + 2 * kCodeQ, &m.sb_gate, bar, rb * kRows1, ch * kChunk, e, pol);
+    tma_load_3d_hint(st + 2 * kCodeQ + kCodeSB, &m.sb_up, bar, rb * kRows1, ch * kChunk, e, pol);
+  };
+  // Phase-2 job j2: slot j2 % nsl of the CTA's row block j2 / nsl.
+  auto issue2c = [&](int j2, int nsl, uint64_t pol) {
+    const int stage = j2 % L.S2, slot = j2 % nsl;
+    const int rb = cta + (j2 / nsl) * nC;
+    const bool sh = has_shared && slot == 0;
+    const int e = sh ? 0 : slot_e[slot];
+    const uint32_t gx = static_cast<uint32_t>(sh ? G2s : G2);
+    const DecodeMaps& m = sh ? ms : mr;
+    uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
+    uint64_t* bar = &full2c[stage];
+    mbar_arrive_expect_tx(bar, gx * kRows2 * (32 + 4));
+    tma_load_3d_hint(st, &m.q_down, bar, rb * kRows2 * 8, 0, e, pol);
+    tma_load_3d_hint(st + L.st2_sb, &m.sb_down, bar, rb * kRows2, 0, e, pol);
+  };
+  auto issue2h = [&](int j2, int nsl) {
+    const int stage = j2 % L.S2, slot = j2 % nsl;
+    uint64_t* bar = &full2h[stage];
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(L.hrec));
+    bulk_g2s(ring2 + static_cast<size_t>(stage) * L.st2 + L.st2_h, a.hbuf + static_cast<size_t>(slot) * L.hrec,
+             static_cast<uint32_t>(L.hrec), bar);
+  };
 
-  const int u0 = cl < ncl ? cl : 0x3FFFFFFF;  // the routing cluster has no unit
-  const int rs0 = has_shared ? 1 : 0;
-  // Shared-expert weights do not depend on the previous kernels: start them
-  // first.  Tensor maps, router logits and X are only pulled towards the SM
-  // (the logits and X are read after the wait; an L2 prefetch of a line the
-  // previous kernel still writes is harmless: L2 is where writes land).
-  if (warp == 0 && u0 < Gs) issue(unit_of(u0, Gs, G, has_shared), 0);
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&qg_r);
-    tma_prefetch_desc(&qu_r);
-    tma_prefetch_desc(&sbg_r);
-    tma_prefetch_desc(&sbu_r);
-    tma_prefetch_desc(&qd_r);
-    tma_prefetch_desc(&sbd_r);
-  }
-  if (warp == 1) {
+  // The shared expert's loads need no routing and do not depend on the
+  // previous kernels: issue them first (the CTA's items come in index order,
+  // the shared expert's first).  Tensor maps, router logits and X are only
+  // pulled towards the SM (an L2 prefetch of a line the previous kernel still
+  // writes is harmless: L2 is where writes land).
+  const int my_sh_items = cta < it_s ? div_up(it_s - cta, nC) : 0;
+  const int pre1 = min(kS1, my_sh_items * L.nchunk);
+  const int pre2 = has_shared && my_rbs > 0 ? 1 : 0;
+  if (warp == 0) {
+    const uint64_t pol = l2_policy_evict_first();  // every weight byte is read once
+    if (lane < pre1) issue1(lane, pol);
+    if (lane == 31 && pre2) issue2c(0, 1, pol);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mr.q_gate);
+      tma_prefetch_desc(&mr.q_up);
+      tma_prefetch_desc(&mr.sb_gate);
+      tma_prefetch_desc(&mr.sb_up);
+      tma_prefetch_desc(&mr.q_down);
+      tma_prefetch_desc(&mr.sb_down);
+    }
     const char* lg = reinterpret_cast<const char*>(a.logits);
     const char* xp = reinterpret_cast<const char*>(a.X);
     if (lg)
       for (int off = lane * 128; off < kT * a.E * 4; off += 32 * 128) prefetch_l2(lg + off);
     for (int off = lane * 128; off < kT * d * 2; off += 32 * 128) prefetch_l2(xp + off);
   }
-  pdl_wait();  // routing, X and the previous layer's use of the workspace
+  pdl_wait();  // X, the routing and the previous layer's use of the workspace
 
+  if (threadIdx.x == 32 * kGemvMaxT) {  // X into shared memory
+    mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(kT * d * 2));
+    bulk_g2s(xs, a.X, static_cast<uint32_t>(kT * d * 2), bar_x);
+  }
+
+  // ------------------------------------------------------------ routing
   const int na = kT * a.k;
-  float sel_v = 0.0f;  // fused routing: this lane's selected logit (warps < kT)
+  bool ok = true;  // every wait completed
+  float sel_v = 0.0f;  // fused routing: this lane's selected logit (warps < T)
   if (warp < kT) {
-    // the call's assignments: routed here (one warp per token) or read from memory
     if (fused) {
-      // the selection now; its weights after the expert loads have been issued
       int sel_i;
       bool finite;
       warp_topk_select<8>(a.logits + static_cast<size_t>(warp) * a.E, a.E, a.k, lane, sel_i, sel_v, finite);
@@ -365,131 +317,131 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < a.k) s_ids[warp * a.k + lane] = sel_i;
     } else {
       for (int i = lane; i < a.k; i += 32) {
-        s_ids[warp * a.k + i] = __ldg(a.ids + warp * a.k + i);
-        s_w[warp * a.k + i] = __ldg(a.w + warp * a.k + i);
+        s_ids[warp * a.k + i] = __ldcg(a.ids + warp * a.k + i);
+        s_w[warp * a.k + i] = __ldcg(a.w + warp * a.k + i);
       }
     }
-  } else {
-    // the other warps stage x (bf16 -> fp32) and its per-group sums
-    constexpr int kStagers = kThreads - 32 * kGemvMaxT;
-    const int n8 = kT * d / 8;
-    for (int f = threadIdx.x - 32 * kGemvMaxT; f >= 0 && f < n8; f += kStagers) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X) + f);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      float4* d4 = reinterpret_cast<float4*>(xs + f * 8);
-      d4[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
-                          __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
-      d4[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
-                          __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
-    }
-    if (warp >= kGemvMaxT) {
-      asm volatile("bar.sync 1, %0;" ::"r"(kStagers) : "memory");  // the staging warps only
-      for (int idx = warp - kGemvMaxT; idx < kT * 2 * L.KB1; idx += kWarps - kGemvMaxT) {
-        float v = xs[(idx / (2 * L.KB1)) * d + (idx % (2 * L.KB1)) * 32 + lane];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) sx[idx] = v;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // Distinct experts of the call in order of first appearance, and the
-    // routing weight of each for each token.
-    int nsl = rs0;
-    if (kT == 1 && fused) {
-      // one token: its k experts are distinct, slot j holds selection j
-      if (lane < na) {
-        slot_e[rs0 + lane] = s_ids[lane];
-        s_slot[lane] = rs0 + lane;
-      }
-      nsl = rs0 + na;
-    } else if (na <= 32) {
-      // one assignment per lane: a lane whose expert no lower lane holds opens a slot
-      const bool valid = lane < na;
-      int e = valid ? s_ids[lane] : -1 - lane;
-      if (valid && (e < 0 || e >= a.E)) {
-        record_status(a.status, MOE_ERR_INVALID_ARG);
-        e = 0;
-      }
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int leader = __ffs(peers) - 1;
-      const unsigned opens = __ballot_sync(0xffffffffu, valid && leader == lane);
-      const int my_slot = rs0 + __popc(opens & ((1u << lane) - 1u));
-      const int slot = __shfl_sync(0xffffffffu, my_slot, leader);
-      if (valid) {
-        if (leader == lane) slot_e[slot] = e;
-        s_slot[lane] = slot;
-      }
-      nsl = rs0 + __popc(opens);
-    } else {
-      // more assignments than lanes: walk them in order
-      for (int i = 0; i < na; ++i) {
-        int e = s_ids[i];
-        if (e < 0 || e >= a.E) {
-          if (lane == 0) record_status(a.status, MOE_ERR_INVALID_ARG);
+    if (kT > 1) asm volatile("bar.sync 3, %0;" ::"r"(32 * kT) : "memory");
+    if (warp == 0) {
+      // Distinct experts of the call in order of first appearance.
+      __syncwarp();
+      int nsl = rs0;
+      if (kT == 1 && fused) {
+        // one token: its k experts are distinct, slot j holds selection j
+        if (lane < na) {
+          slot_e[rs0 + lane] = s_ids[lane];
+          s_slot[lane] = rs0 + lane;
+        }
+        nsl = rs0 + na;
+      } else if (na <= 32) {
+        // one assignment per lane: a lane whose expert no lower lane holds opens a slot
+        const bool valid = lane < na;
+        int e = valid ? s_ids[lane] : -1 - lane;
+        if (valid && (e < 0 || e >= a.E)) {
+          record_status(a.status, MOE_ERR_INVALID_ARG);
           e = 0;
         }
-        int slot = -1;
-        for (int c0 = rs0; c0 < nsl && slot < 0; c0 += 32) {
-          const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < nsl && slot_e[c0 + lane] == e);
-          if (hit) slot = c0 + __ffs(hit) - 1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(peers) - 1;
+        const unsigned opens = __ballot_sync(0xffffffffu, valid && leader == lane);
+        const int my_slot = rs0 + __popc(opens & ((1u << lane) - 1u));
+        const int slot = __shfl_sync(0xffffffffu, my_slot, leader);
+        if (valid) {
+          if (leader == lane) slot_e[slot] = e;
+          s_slot[lane] = slot;
         }
-        if (slot < 0) slot = nsl++;
-        __syncwarp();
-        if (lane == 0) {
-          slot_e[slot] = e;
-          s_slot[i] = slot;
+        nsl = rs0 + __popc(opens);
+      } else {
+        // more assignments than lanes: walk them in order
+        for (int i = 0; i < na; ++i) {
+          int e = s_ids[i];
+          if (e < 0 || e >= a.E) {
+            if (lane == 0) record_status(a.status, MOE_ERR_INVALID_ARG);
+            e = 0;
+          }
+          int slot = -1;
+          for (int c0 = rs0; c0 < nsl && slot < 0; c0 += 32) {
+            const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < nsl && slot_e[c0 + lane] == e);
+            if (hit) slot = c0 + __ffs(hit) - 1;
+          }
+          if (slot < 0) slot = nsl++;
+          __syncwarp();
+          if (lane == 0) {
+            slot_e[slot] = e;
+            s_slot[i] = slot;
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
+      if (has_shared && lane == 0) slot_e[0] = 0;
+      if (lane == 0) misc[0] = nsl - rs0;
+      __syncwarp();
+      asm volatile("bar.arrive 4, 64;" ::: "memory");  // the slots are known: warp 4 issues the phase-2 loads
+      // the routed experts' gate/up loads start as soon as they are known
+      const int NI = it_s + (nsl - rs0) * it_r;
+      const int my_items = cta < NI ? div_up(NI - cta, nC) : 0;
+      const int n1 = min(kS1, my_items * L.nchunk) - pre1;
+      if (lane < n1) issue1(pre1 + lane, l2_policy_evict_first());
     }
-    __syncwarp();
-    if (lane == 0) {
-      misc[0] = nsl - rs0;
-      if (has_shared) slot_e[0] = 0;
+  } else {
+    if (warp == kGemvMaxT) {
+      asm volatile("bar.sync 4, 64;" ::: "memory");
+      const int nsl = rs0 + misc[0];
+      const int n2 = min(L.S2, my_rbs * nsl) - pre2;
+      if (lane < n2) issue2c(pre2 + lane, nsl, l2_policy_evict_first());
     }
-    __syncwarp();
-    // the routed unit's loads start as soon as its expert is known
-    const int U = Gs + (nsl - rs0) * G;
-    if (u0 >= Gs && u0 < U) {
-      const Unit m = unit_of(u0, Gs, G, has_shared);
-      issue(m, slot_e[m.slot]);
+    // the other warps: sums of x over each group of 64 columns, 8 threads per (token, group)
+    const int t0 = threadIdx.x - 32 * kGemvMaxT;
+    if (t0 >= 0) {
+      ok &= mbar_wait(bar_x, 0, nullptr);
+      constexpr int kSum = kThreads - 32 * kGemvMaxT;
+      for (int i = t0; i < div_up(kT * L.G1 * 8, kSum) * kSum; i += kSum) {
+        const int pair = i >> 3, part = i & 7;
+        float v = 0.0f;
+        if (pair < kT * L.G1) {
+          const int t = pair / L.G1, gi = pair % L.G1;
+          const uint4 u = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(t) * d + gi * 64 + part * 8);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) v += bf16_lo(w[c]) + bf16_hi(w[c]);
+        }
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        if (pair < kT * L.G1 && part == 0) sx[pair] = v;
+      }
     }
   }
   __syncthreads();
-  const int U = Gs + misc[0] * G;
+  const int nsl_r = misc[0];
+  const int nsl = rs0 + nsl_r;
   pdl_launch_dependents();
 
-  // The routing weights (fp64, slow on this GPU) are needed only from the down
-  // projection on: warps < T compute them (and the weight of every slot)
-  // while the other warps start on the gate/up products; warps < T take no
-  // gate/up work.
-  if (warp < kT) {
-    if (fused) {
+  // Routing weights are needed only in phase 2.  Read from memory, they are
+  // placed now; computed here (fp64, slow on this GPU), only the CTA that
+  // writes the routing outputs computes them, and every CTA reads them back
+  // after the barrier.
+  if (!fused && warp == 0) {
+    for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = s_w[i];
+    if (has_shared && lane < kT) wt[lane] = 1.0f;
+  }
+  if (bookkeeper) {
+    if (warp < kT) {
       const float w = warp_topk_weights(sel_v, a.k, lane);
       if (lane < a.k) s_w[warp * a.k + lane] = w;
     }
-    asm volatile("bar.sync 3, %0;" ::"r"(32 * kT) : "memory");
-    if (warp == 0) {
-      for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = s_w[i];
-      if (has_shared && lane < kT) wt[lane] = 1.0f;
-    }
-  }
-  if (bookkeeper) {
     asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");  // the weights are in s_w
     // every routing output, as the routing kernel writes it for one chunk:
     // ids and weights, counts, exclusive offsets, the stable permutation and
     // the tile block map (experts ascending)
-    int* cnt = reinterpret_cast<int*>(smem + L.qgu);  // [E]
-    int* off = cnt + a.E;                              // [E + 1]
-    int* boff = off + a.E + 1;                         // [E + 1]
+    int* cnt = reinterpret_cast<int*>(smem + L.bk);  // [E]
+    int* off = cnt + a.E;                             // [E + 1]
+    int* boff = off + a.E + 1;                        // [E + 1]
     for (int i = threadIdx.x; i < na; i += kThreads) {
       a.out.ids[i] = s_ids[i];
       a.out.w[i] = s_w[i];
     }
     for (int e = threadIdx.x; e < a.E; e += kThreads) cnt[e] = 0;
-    __syncwarp();
     asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
     for (int i = threadIdx.x; i < na; i += kThreads) atomicAdd(&cnt[s_ids[i]], 1);
     asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
@@ -544,288 +496,304 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  const int p = threadIdx.x >> 1;  // down rows p, p + 256, ... of this CTA's half
-  const int hf = threadIdx.x & 1;  // which 32 of the group's 64 columns
-  uint32_t par = 0;
-  int buf = 0;
-  bool waited = false;
-  bool ok = true;
-  for (int u = u0; u < U; u += ncl) {
-    const Unit m = unit_of(u, Gs, G, has_shared);
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar_h[buf], static_cast<uint32_t>(kT * (kRows + 1) * 4));
-    // ---------------------------------------------------- gate/up: lane = row, warp = K slice
-    float ag[kT], au[kT];
+  // ------------------------------------------------------------ phase 1: h of this CTA's items
+  const int NI = it_s + nsl_r * it_r;
+  const int my_items = cta < NI ? div_up(NI - cta, nC) : 0;
+  const int total1 = my_items * L.nchunk;
+  const int mat = warp >> 3;  // 0: gate, 1: up
+  const int gl = warp & 7;    // group inside a stage
+  for (int il = 0; il < my_items; ++il) {
+    int slot, rb;
+    item_slot(cta + il * nC, slot, rb);
+    float acc[2][4];
 #pragma unroll
-    for (int t = 0; t < kT; ++t) ag[t] = au[t] = 0.0f;
-    // work item i = (group i/2, half i%2); warp w >= T takes items w-T,
-    // w-T + (16-T), ...: the warps work on each chunk of codes as it lands
-    ok &= mbar_wait_poll(bar_sb, par);
-    for (int i = warp - kT; warp >= kT && i < 2 * L.KB1; i += kWarps - kT) {
-      const int kb = i >> 1, hh = i & 1;
-      ok &= mbar_wait_poll(&bar_gu[kb / kChunkGroups], par);
-      half_group_dot2<kT>(qg, qu, lane, kb, hh, xs, d, sx, 2 * L.KB1, sbg[kb * kRows + lane], sbu[kb * kRows + lane],
-                          ag, au);
-    }
+    for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.0f;
+    for (int ch = 0; ch < L.nchunk; ++ch) {
+      const int j = il * L.nchunk + ch, stage = j % kS1;
+      ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
+      const int gi = ch * kChunk + gl;
+      if (gi < L.G1) {
+        const uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1;
+        const uint32_t* qm = reinterpret_cast<const uint32_t*>(st + mat * kCodeQ) + gl * kRows1 * 8;
+        const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + 2 * kCodeQ + mat * kCodeSB) + gl * kRows1;
+        uint32_t b[8];
+        load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
+        const float sxa = 2 * q4 < kT ? sx[(2 * q4) * L.G1 + gi] : 0.0f;
+        const float sxb = 2 * q4 + 1 < kT ? sx[(2 * q4 + 1) * L.G1 + gi] : 0.0f;
 #pragma unroll
-    for (int t = 0; t < kT; ++t) {
-      red[(warp * kRows + lane) * kT + t] = ag[t];
-      red[((kWarps + warp) * kRows + lane) * kT + t] = au[t];
-    }
-    if (!waited) {
-      cluster_wait();  // the other CTA of the cluster is running
-      waited = true;
-    }
-    __syncthreads();
-    float* hbb = hb + buf * kT * 64;
-    if (warp < kT) {
-      // token t = warp: h of this CTA's 32 features, into both CTAs; the copy
-      // to the other CTA completes its exchange barrier
-      const int t = warp;
-      float g = 0.0f, uu = 0.0f;
-#pragma unroll
-      for (int s = 0; s < kWarps; ++s) {
-        g += red[(s * kRows + lane) * kT + t];
-        uu += red[((kWarps + s) * kRows + lane) * kT + t];
+        for (int tile = 0; tile < 2; ++tile) {
+          const int r0 = tile * 16 + g8;
+          const uint2 wa = *reinterpret_cast<const uint2*>(qm + r0 * 8 + 2 * q4);
+          const uint2 wb = *reinterpret_cast<const uint2*>(qm + (r0 + 8) * 8 + 2 * q4);
+          float dd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mma_group<true>(wa, wb, b, dd);
+          const uint32_t p0 = sbm[r0], p1 = sbm[r0 + 8];
+          const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 128.0f * s0;
+          const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 128.0f * s1;
+          acc[tile][0] += fmaf(s0, dd[0], c0 * sxa);
+          acc[tile][1] += fmaf(s0, dd[1], c0 * sxb);
+          acc[tile][2] += fmaf(s1, dd[2], c1 * sxa);
+          acc[tile][3] += fmaf(s1, dd[3], c1 * sxb);
+        }
       }
-      const float h = g / (1.0f + expf(-g)) * uu;
-      const uint32_t peer = rank ^ 1u;
-      const uint32_t peer_bar = mapa_shared(smem_u32(&bar_h[buf]), peer);
-      float* dst = hbb + t * 64 + static_cast<int>(rank) * kRows + lane;
-      *dst = h;
-      st_async_f32(mapa_shared(smem_u32(dst), peer), h, peer_bar);
-      // and the sum of these 32 values (the group sum of h needs both halves)
-      float hsum_part = h;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) hsum_part += __shfl_xor_sync(0xffffffffu, hsum_part, off);
-      if (lane == 0) {
-        float* sdst = hsb + (buf * kT + t) * 2 + static_cast<int>(rank);
-        *sdst = hsum_part;
-        st_async_f32(mapa_shared(smem_u32(sdst), peer), hsum_part, peer_bar);
-      }
+      // the last warp done with a stage refills it
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_h[buf]);  // this CTA's own half is written
-    }
-    ok &= mbar_wait_poll(&bar_h[buf], (static_cast<uint32_t>(u - u0) / static_cast<uint32_t>(ncl) >> 1) & 1u);
-    // ---------------------------------------------------- down: thread pair = row, 32 columns each
-    float wts[kT], hs[kT];
-#pragma unroll
-    for (int t = 0; t < kT; ++t) {
-      wts[t] = wt[m.slot * kT + t];
-      hs[t] = hsb[(buf * kT + t) * 2] + hsb[(buf * kT + t) * 2 + 1];  // same order in both CTAs
-    }
-    for (int b = 0; b < L.nboxd; ++b) ok &= mbar_wait_poll(&bar_d[b], par);
-    const float* hp = hbb + hf * 32;
-    // two rows at a time: independent dependency chains
-    for (int row0 = p; row0 < L.half; row0 += 2 * kPairs) {
-      const int row1 = row0 + kPairs;
-      const bool has1 = row1 < L.half;
-      float2 pp0[kT], pp1[kT];
-#pragma unroll
-      for (int t = 0; t < kT; ++t) pp0[t] = pp1[t] = make_float2(0.0f, 0.0f);
-      const uint4 w0 = *reinterpret_cast<const uint4*>(qd + row0 * 32 + hf * 16);
-      const uint4 w1 = has1 ? *reinterpret_cast<const uint4*>(qd + row1 * 32 + hf * 16) : make_uint4(0, 0, 0, 0);
-      word_dot<kT>(w0.x, hp + 0, 64, pp0);
-      word_dot<kT>(w1.x, hp + 0, 64, pp1);
-      word_dot<kT>(w0.y, hp + 8, 64, pp0);
-      word_dot<kT>(w1.y, hp + 8, 64, pp1);
-      word_dot<kT>(w0.z, hp + 16, 64, pp0);
-      word_dot<kT>(w1.z, hp + 16, 64, pp1);
-      word_dot<kT>(w0.w, hp + 24, 64, pp0);
-      word_dot<kT>(w1.w, hp + 24, 64, pp1);
-      const uint32_t sb0 = sbd[row0];
-      const uint32_t sb1 = has1 ? sbd[row1] : 0u;
-      const float s0 = __uint_as_float(sb0 << 16), s1 = __uint_as_float(sb1 << 16);
-      const float c0 = __uint_as_float(sb0 & 0xFFFF0000u) - 128.0f * s0;
-      const float c1 = __uint_as_float(sb1 & 0xFFFF0000u) - 128.0f * s1;
-#pragma unroll
-      for (int t = 0; t < kT; ++t) {
-        float pv0 = pp0[t].x + pp0[t].y;
-        float pv1 = pp1[t].x + pp1[t].y;
-        pv0 += __shfl_xor_sync(0xffffffffu, pv0, 1);
-        pv1 += __shfl_xor_sync(0xffffffffu, pv1, 1);
-        if (hf == 0 && wts[t] != 0.0f) {
-          accd[row0 * kT + t] = fmaf(wts[t], fmaf(s0, pv0, c0 * hs[t]), accd[row0 * kT + t]);
-          if (has1) accd[row1 * kT + t] = fmaf(wts[t], fmaf(s1, pv1, c1 * hs[t]), accd[row1 * kT + t]);
+      if (lane == 0) {
+        const int old = atomicAdd(&cnt1[stage], 1);
+        if ((old + 1) % kWarps == 0 && j + kS1 < total1) {
+          fence_proxy_async_smem();
+          issue1(j + kS1, l2_policy_evict_first());
         }
       }
     }
-    __syncthreads();  // every box of this unit has been read
-    if (u + ncl < U && warp == 0) {
-      const Unit nx = unit_of(u + ncl, Gs, G, has_shared);
-      issue(nx, nx.shared ? 0 : slot_e[nx.slot]);
+    // h of the item's 32 features for every token
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile) {
+      const int r0 = tile * 16 + g8;
+      if (2 * q4 < kT) {
+        red1[(warp * kRows1 + r0) * kT + 2 * q4] = acc[tile][0];
+        red1[(warp * kRows1 + r0 + 8) * kT + 2 * q4] = acc[tile][2];
+      }
+      if (2 * q4 + 1 < kT) {
+        red1[(warp * kRows1 + r0) * kT + 2 * q4 + 1] = acc[tile][1];
+        red1[(warp * kRows1 + r0 + 8) * kT + 2 * q4 + 1] = acc[tile][3];
+      }
     }
-    par ^= 1;
-    buf ^= 1;
+    __syncthreads();
+    if (warp < kT) {
+      const int t = warp, r = lane;
+      float gs = 0.0f, us = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kChunk; ++w) {
+        gs += red1[(w * kRows1 + r) * kT + t];
+        us += red1[((kChunk + w) * kRows1 + r) * kT + t];
+      }
+      const __half hh = __float2half_rn(gs / (1.0f + expf(-gs)) * us);
+      uint8_t* rec = a.hbuf + static_cast<size_t>(slot) * L.hrec;
+      reinterpret_cast<__half*>(rec)[t * L.Imax + rb * kRows1 + r] = hh;
+      float hsum = __half2float(hh);  // the sum of the values the MMA sees
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
+      if (lane == 0) reinterpret_cast<float*>(rec + static_cast<size_t>(kT) * L.Imax * 2)[t * L.hs_stride + rb] = hsum;
+    }
+    __syncthreads();
   }
-  if (!waited) cluster_wait();
-  if (!ok) record_status(a.status, MOE_ERR_TIMEOUT);
 
-  // ---------------------------------------------------- Y: partial rows, one grid barrier, every CTA sums a few rows
-  // This cluster's share of the output (rows of this CTA's half; zeros for a
-  // CTA with no unit) goes to global memory.  After a barrier over the grid
-  // (bounded spin on an arrival counter; every CTA of the launch is resident,
-  // one per SM), CTA b sums the partials of rows [b*per, (b+1)*per) over the
-  // clusters in a fixed order, so the result does not depend on timing.
-  {
-    float* part = a.part + static_cast<size_t>(cl) * kT * d + static_cast<int>(rank) * L.half;
-    for (int i = threadIdx.x; i < L.half * kT; i += kThreads) {
-      const int t = i / L.half, row = i % L.half;
-      part[static_cast<size_t>(t) * d + row] = accd[row * kT + t];
-    }
-  }
+  // ------------------------------------------------------------ barrier over the grid
+  // Every CTA of the launch is resident (one per SM, the grid is capped at
+  // what fits); the h records written with ordinary stores are read by bulk
+  // copies after it.
+  fence_proxy_async_global();
   __syncthreads();
+  // Call g of this workspace counts arrivals in dec_count[g % 2]; after the
+  // barrier CTA 0 clears the other counter (last used by call g - 1, which
+  // has finished) and advances the call number for call g + 1 (which reads it
+  // only after this call has finished).
   if (threadIdx.x == 0) {
-    atom_add_acq_rel_gpu(&hdr->dec_arrive, 1u);
+    const uint32_t gen = *reinterpret_cast<volatile uint32_t*>(&hdr->dec_gen);
+    uint32_t* count = &hdr->dec_count[gen & 1u];
+    red_release_gpu_add(count, 1u);
     const long long t0 = clock64();
-    while (ld_acquire_gpu(&hdr->dec_arrive) < gridDim.x) {
+    while (ld_acquire_gpu(count) < static_cast<uint32_t>(nC)) {
       if (clock64() - t0 > kWaitLimitCycles) {
         record_status(a.status, MOE_ERR_TIMEOUT);
         break;
       }
-      __nanosleep(20);
+    }
+    if (cta == 0) {
+      hdr->dec_count[(gen + 1) & 1u] = 0;
+      hdr->dec_gen = gen + 1;
     }
   }
   __syncthreads();
-  {
-    const int nclu = static_cast<int>(gridDim.x >> 1);
-    const int per = (d + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    const int r0 = static_cast<int>(blockIdx.x) * per;
-    const int r1 = min(d, r0 + per);
-    const int items = max(0, r1 - r0) * kT;
-    // S threads per output value, S a power of two <= 32 (lanes of one warp)
-    int S = 1;
-    while (S < 32 && items * S * 2 <= kThreads) S *= 2;
-    const int j = threadIdx.x % S;
-    for (int it = threadIdx.x / S; it < (items + (kThreads / S) - 1) / (kThreads / S) * (kThreads / S); it += kThreads / S) {
-      float v = 0.0f;
-      int t = 0, row = 0;
-      if (it < items) {
-        t = it / (r1 - r0);
-        row = r0 + it % (r1 - r0);
-        // four loads in flight per round, added in cluster order
-        for (int c0 = j; c0 < nclu; c0 += 4 * S) {
-          float pv[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = c0 + q * S;
-            pv[q] = c < nclu ? __ldcg(a.part + (static_cast<size_t>(c) * kT + t) * d + row) : 0.0f;
-          }
-          v += pv[0];
-          v += pv[1];
-          v += pv[2];
-          v += pv[3];
+  if (warp == 0) {
+    fence_proxy_async_global();
+    if (lane < min(L.S2, my_rbs * nsl)) issue2h(lane, nsl);
+  } else if (warp == 1 && fused) {
+    for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = __ldcg(a.out.w + i);
+    if (has_shared && lane < kT) wt[lane] = 1.0f;
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ phase 2: Y rows of this CTA
+  // Warp w takes a contiguous run of the (slot, group) pairs of each row
+  // block: it waits for and releases each slot's stage once.
+  const int total2 = my_rbs * nsl;
+  const int G2first = has_shared ? G2s : G2;  // groups of slot 0
+  const int pairs = (has_shared ? G2s : 0) + nsl_r * G2;
+  const int p_begin = warp * pairs / kWarps, p_end = (warp + 1) * pairs / kWarps;
+  int s_begin = 0, g_begin = p_begin;
+  if (p_begin >= G2first) {
+    s_begin = 1 + (p_begin - G2first) / G2;
+    g_begin = (p_begin - G2first) % G2;
+  }
+  for (int rl = 0; rl < my_rbs; ++rl) {
+    const int rb = cta + rl * nC;
+    float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int slot = s_begin, gr = g_begin;
+    for (int p = p_begin; p < p_end; ++slot, gr = 0) {
+      const int gx = slot == 0 ? G2first : G2;
+      const int g_stop = min(gx, gr + (p_end - p));
+      const int j2 = rl * nsl + slot, stage = j2 % L.S2;
+      const uint32_t par = static_cast<uint32_t>(j2 / L.S2) & 1u;
+      // A warp may reach a job two uses of its stage ahead of the job the
+      // stage holds, where the parity wait would pass on the older phase:
+      // first wait until the job has been issued.
+      if (issued2_wait(issued2 + stage, j2)) ok = false;
+      ok &= mbar_wait(&full2c[stage], par, nullptr);
+      ok &= mbar_wait(&full2h[stage], par, nullptr);
+      const uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
+      const uint32_t* qm = reinterpret_cast<const uint32_t*>(st) + g8 * 8 + 2 * q4;
+      const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + L.st2_sb) + g8;
+      const uint16_t* hp = reinterpret_cast<const uint16_t*>(st + L.st2_h) + static_cast<size_t>(g8) * L.Imax + 16 * q4;
+      const float* hsp = reinterpret_cast<const float*>(st + L.st2_h + static_cast<size_t>(kT) * L.Imax * 2);
+      const float* hsa = hsp + (2 * q4) * L.hs_stride;
+      const float* hsb = hsa + L.hs_stride;
+      float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the slot's rows before its routing weight
+      for (int g = gr; g < g_stop; ++g) {
+        uint32_t b[8];
+        load_b(hp + g * 64, g8 < kT, b);
+        const uint2 wa = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8);
+        const uint2 wb = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8 + 64);
+        float dd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_group<false>(wa, wb, b, dd);
+        const uint32_t p0 = sbm[g * kRows2], p1 = sbm[g * kRows2 + 8];
+        const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 1024.0f * s0;
+        const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 1024.0f * s1;
+        const float ha = 2 * q4 < kT ? hsa[2 * g] + hsa[2 * g + 1] : 0.0f;
+        const float hb = 2 * q4 + 1 < kT ? hsb[2 * g] + hsb[2 * g + 1] : 0.0f;
+        sa[0] += fmaf(s0, dd[0], c0 * ha);
+        sa[1] += fmaf(s0, dd[1], c0 * hb);
+        sa[2] += fmaf(s1, dd[2], c1 * ha);
+        sa[3] += fmaf(s1, dd[3], c1 * hb);
+      }
+      // tokens not routed to the slot contribute nothing (their h is never used)
+      const float ra = 2 * q4 < kT ? wt[slot * kT + 2 * q4] : 0.0f;
+      const float rb2 = 2 * q4 + 1 < kT ? wt[slot * kT + 2 * q4 + 1] : 0.0f;
+      if (ra != 0.0f) {
+        acc2[0] = fmaf(ra, sa[0], acc2[0]);
+        acc2[2] = fmaf(ra, sa[2], acc2[2]);
+      }
+      if (rb2 != 0.0f) {
+        acc2[1] = fmaf(rb2, sa[1], acc2[1]);
+        acc2[3] = fmaf(rb2, sa[3], acc2[3]);
+      }
+      // the last warp done with a stage refills it
+      const int done = g_stop - gr;
+      p += done;
+      __syncwarp();
+      if (lane == 0) {
+        const int old = atomicAdd(&cnt2[stage], done);
+        int need = 0;  // pairs of every job this stage has held, up to this one
+        for (int jj = stage; jj <= j2; jj += L.S2) need += jj % nsl == 0 ? G2first : G2;
+        if (old + done == need && j2 + L.S2 < total2) {
+          *reinterpret_cast<volatile int*>(issued2 + stage) = j2 + L.S2;
+          fence_proxy_async_smem();
+          fence_proxy_async_global();
+          const uint64_t pol = l2_policy_evict_first();
+          issue2c(j2 + L.S2, nsl, pol);
+          issue2h(j2 + L.S2, nsl);
         }
       }
-      for (int off = 1; off < S; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (it < items && j == 0) a.Y[static_cast<size_t>(t) * d + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // the last CTA out resets the counters for the next call (all have passed the barrier)
-    if (atom_add_acq_rel_gpu(&hdr->dec_done, 1u) == gridDim.x - 1) {
-      hdr->dec_arrive = 0;
-      hdr->dec_done = 0;
-      __threadfence();
+    if (2 * q4 < kT) {
+      red2[(warp * kRows2 + g8) * kT + 2 * q4] = acc2[0];
+      red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4] = acc2[2];
     }
+    if (2 * q4 + 1 < kT) {
+      red2[(warp * kRows2 + g8) * kT + 2 * q4 + 1] = acc2[1];
+      red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4 + 1] = acc2[3];
+    }
+    __syncthreads();
+    if (threadIdx.x < kRows2 * kT) {
+      const int r = threadIdx.x % kRows2, t = threadIdx.x / kRows2;
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += red2[(w * kRows2 + r) * kT + t];  // fixed order: deterministic
+      a.Y[static_cast<size_t>(t) * d + rb * kRows2 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+    __syncthreads();
   }
+  if (!ok) record_status(a.status, MOE_ERR_TIMEOUT);
 }
 
-// Clusters of this kernel that can be resident at once on the current device
-// (0 on error).  The kernel's grid barrier needs every CTA resident together.
+// CTAs of this kernel that can be resident at once on the current device (0
+// on error).  The barrier over the grid needs every CTA resident together.
 template <int kT>
-int max_clusters(size_t smem) {
+int max_ctas(size_t smem, int num_sms) {
   static int cached_dev = -1, cached = 0;
   static size_t cached_smem = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev == cached_dev && smem == cached_smem) return cached;
-  if (cudaFuncSetAttribute(decode_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(decode_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemMax)) != cudaSuccess)
     return 0;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kT>, &cfg) != cudaSuccess) return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kT>, kThreads, smem) != cudaSuccess)
+    return 0;
   cached_dev = dev;
   cached_smem = smem;
-  cached = n;
-  return n;
+  cached = per_sm * num_sms;
+  return cached;
 }
 
 template <int kT>
-cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int ncl,
+cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
                      size_t smem, cudaStream_t stream, bool pdl) {
-  const int resident = max_clusters<kT>(smem);
-  if (resident < 1 + (a.logits ? 1 : 0)) return cudaErrorInvalidConfiguration;
-  if (ncl > resident) ncl = resident;
-  const int grid = 2 * ncl;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  const int resident = max_ctas<kT>(smem, a.num_sms);
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const int grid = want < resident ? want : resident;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kT>, routed->q_gate, routed->q_up, routed->sb_gate, routed->sb_up,
-                            routed->q_down, routed->sb_down, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up,
-                            sh->q_down, sh->sb_down, a, hdr);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kT>, *routed, *sh, a, hdr);
 }
 
 }  // namespace
 
 bool decode_supported(int T, int d, int I, int I_shared, int k) {
-  if (T < 1 || T > kGemvMaxT || k > kMaxK) return false;
-  const Layout L = layout(T, d);
-  // the routing outputs' scratch (counts and two scans over E <= 256) reuses the gate/up code buffer
-  if (2ull * L.nchunk * kChunkGroups * kRows * 32 < 3ull * 257 * 4) return false;
-  return L.total <= 227 * 1024 && L.nchunk + 1 + L.nboxd <= 32 && d % 64 == 0 && I % 64 == 0 &&
-         I_shared % 64 == 0;
+  if (T < 1 || T > kGemvMaxT || k > kMaxK || k < 1) return false;
+  if (d % 64 || I % 64 || I_shared % 64 || I < 64) return false;
+  const int Imax = I > I_shared ? I : I_shared;
+  if (Imax / 64 > 256) return false;  // a down-projection box covers every group of a row block
+  const Layout L = layout(T, d, I, I_shared);
+  return L.S2 >= 2 && L.total <= kSmemMax;
 }
 
-size_t decode_partial_bytes(int T, int d) { return static_cast<size_t>(kDecodeMaxClusters) * T * d * 4; }
-
-int decode_box_superrows(int d) { return layout(1, d).box_sr; }
+size_t decode_scratch_bytes(int T, int I, int I_shared) {
+  const int Imax = I > I_shared ? I : I_shared;
+  const size_t hs = round_up(Imax / 32, 4);
+  return static_cast<size_t>(kMaxSlots) * (static_cast<size_t>(T) * Imax * 2 + static_cast<size_t>(T) * hs * 4);
+}
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
                           cudaStream_t stream, bool pdl) {
-  const Layout L = layout(a.T, a.d);
-  const bool aligned = L.qgu % 128 == 0 && L.qd % 128 == 0 && L.sbgu % 128 == 0 && L.sb1_slot % 128 == 0 &&
-                       L.sbd % 128 == 0 && (L.box_sr * 16) % 128 == 0 && L.bars % 8 == 0;
-  if (!aligned || !decode_supported(a.T, a.d, a.I, a.I_shared, a.k)) return cudaErrorInvalidValue;
+  if (!decode_supported(a.T, a.d, a.I, a.I_shared, a.k)) return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(a.hbuf) & 15u) return cudaErrorInvalidValue;
+  const Layout L = layout(a.T, a.d, a.I, a.I_shared);
   const DecodeMaps* sh = shared ? shared : routed;  // never read without a shared expert
   const int distinct = a.T * a.k < a.E ? a.T * a.k : a.E;
-  const int units = a.I_shared / 64 + distinct * (a.I / 64);
-  const int extra = a.logits ? 1 : 0;  // the cluster that writes the routing outputs
-  int ncl = a.num_sms / 2 - extra;
-  if (ncl > units) ncl = units;
-  if (ncl > kDecodeMaxClusters - extra) ncl = kDecodeMaxClusters - extra;
-  if (ncl < 1) ncl = 1;
-  ncl += extra;  // capped below by the clusters that fit on the device at once
+  const int items = a.I_shared / kRows1 + distinct * (a.I / kRows1);
+  const int rbs = a.d / kRows2;
+  int want = items > rbs ? items : rbs;
+  if (a.logits) want += 1;  // a CTA with no item writes the routing outputs when the grid has room
+  if (want > a.num_sms) want = a.num_sms;
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   timer_begin(kKDecode, stream);
   cudaError_t err;
   switch (a.T) {
-    case 1: err = launch_t<1>(a, routed, sh, hdr, ncl, L.total, stream, pdl); break;
-    case 2: err = launch_t<2>(a, routed, sh, hdr, ncl, L.total, stream, pdl); break;
-    case 3: err = launch_t<3>(a, routed, sh, hdr, ncl, L.total, stream, pdl); break;
-    default: err = launch_t<4>(a, routed, sh, hdr, ncl, L.total, stream, pdl); break;
+    case 1: err = launch_t<1>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+    case 2: err = launch_t<2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+    case 3: err = launch_t<3>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+    default: err = launch_t<4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
   }
   timer_end(kKDecode, stream);
   return err;

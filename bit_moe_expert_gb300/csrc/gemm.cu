@@ -112,24 +112,27 @@ __device__ __forceinline__ Item get_item(const GemmArgs& a, const Sched& s, int 
 
 __device__ __forceinline__ int tile_n(int rows) { return max(16, (rows + 15) & ~15); }
 
-// Eight 4-bit codes (one word, k ascending from the low nibble) -> four f16x2
-// values of q*scale + bias, adjacent columns paired (low half = lower k).
-// fp16 carries 11 significant bits, so q*scale + bias is exact whenever it fits
-// them (always when bias = -8*scale: |q-8| <= 8 adds at most 3 bits to the
-// 8-bit bf16 scale); otherwise it is rounded once.
+// Eight 4-bit codes of one word in the interleaved order of the prepacked
+// layout (code 2p in bits 4p, code 2p+1 in bits 4p+16) -> four f16x2 values of
+// q*scale + bias, adjacent columns paired (low half = lower k).  A mask puts
+// 1024 + q (codes in bits 0..3 and 16..19) or 1024 + 16 q (bits 4..7, 20..23)
+// into an f16 pair; one fp16 FMA recovers q exactly, one more applies scale
+// and bias.  fp16 carries 11 significant bits, so q*scale + bias is exact
+// whenever it fits them (always when bias = -8*scale: |q-8| <= 8 adds at most
+// 3 bits to the 8-bit bf16 scale); otherwise it is rounded once.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* out) {
-  const uint32_t w4 = w >> 4;
-  const uint32_t magic = 0x64006400u;        // f16 pair (1024, 1024): a code in the low mantissa bits reads 1024 + q
-  const uint32_t one = 0x3C003C00u;          // f16 pair (1, 1)
-  const uint32_t minus_magic = 0xE400E400u;  // f16 pair (-1024, -1024)
-  const uint32_t sel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t t = prmt(w, w4, sel[m]);                 // low nibbles: byte 0 = q_2m, byte 2 = q_2m+1
-    const uint32_t v = lop3_and_or(t, 0x000F000Fu, magic);  // (1024 + q_2m, 1024 + q_2m+1)
-    const uint32_t q = f16x2_fma(v, one, minus_magic);      // (q_2m, q_2m+1), exact
-    out[m] = f16x2_fma(q, s2, b2);                          // q*scale + bias, one rounding
-  }
+  const uint32_t magic = 0x64006400u;  // f16 pair (1024, 1024)
+  const uint32_t w8 = w >> 8;
+  const uint32_t v0 = lop3_and_or(w, 0x000F000Fu, magic);    // 1024 + q: codes 0, 1
+  const uint32_t v1 = lop3_and_or(w, 0x00F000F0u, magic);    // 1024 + 16 q: codes 2, 3
+  const uint32_t v2 = lop3_and_or(w8, 0x000F000Fu, magic);   // codes 4, 5
+  const uint32_t v3 = lop3_and_or(w8, 0x00F000F0u, magic);   // codes 6, 7
+  const uint32_t one = 0x3C003C00u, minus_1024 = 0xE400E400u;      // f16 pairs (1, 1), (-1024, -1024)
+  const uint32_t sixteenth = 0x2C002C00u, minus_64 = 0xD400D400u;  // (1/16, 1/16), (-64, -64)
+  out[0] = f16x2_fma(f16x2_fma(v0, one, minus_1024), s2, b2);
+  out[1] = f16x2_fma(f16x2_fma(v1, sixteenth, minus_64), s2, b2);
+  out[2] = f16x2_fma(f16x2_fma(v2, one, minus_1024), s2, b2);
+  out[3] = f16x2_fma(f16x2_fma(v3, sixteenth, minus_64), s2, b2);
 }
 
 template <bool kGateUp>

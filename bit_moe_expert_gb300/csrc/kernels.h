@@ -46,35 +46,34 @@ cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, i
                            cudaStream_t stream);
 
 // ---------------------------------------------------------------- decode GEMV
-constexpr int kDecodeRowsGU = 32;        // gate/up rows per CTA and unit
-constexpr int kDecodeChunkGroups = 8;    // 64-column groups per gate/up code box
-constexpr int kDecodeMaxClusters = 128;  // clusters per launch at most
+constexpr int kDecodeRowsGU = 32;      // gate/up rows per item (phase 1)
+constexpr int kDecodeChunkGroups = 8;  // 64-column groups per gate/up stage
+constexpr int kDecodeRowsDown = 16;    // output rows per block (phase 2)
 
 // Tensor maps of one expert set for the decode kernel.
 struct DecodeMaps {
-  CUtensorMap q_gate, q_up;    // codes, box (8 words, 32 rows, kDecodeChunkGroups groups)
-  CUtensorMap sb_gate, sb_up;  // group parameters, box (32 rows, d/64, 1)
-  CUtensorMap q_down;          // codes as 128-byte super-rows, box (32 words, decode_box_superrows, 1 group)
-  CUtensorMap sb_down;         // group parameters as 4-row super-rows, same box rows
+  CUtensorMap q_gate, q_up;    // codes [E][d/64][I*8], box (32 rows * 8 words, kDecodeChunkGroups groups, 1)
+  CUtensorMap sb_gate, sb_up;  // group parameters [E][d/64][I], box (32 rows, kDecodeChunkGroups groups, 1)
+  CUtensorMap q_down;          // codes [E][I/64][d*8], box (16 rows * 8 words, I/64 groups, 1)
+  CUtensorMap sb_down;         // group parameters [E][I/64][d], box (16 rows, I/64 groups, 1)
 };
 
 struct DecodeArgs {
   const uint16_t* X;      // [T][d] bf16
   const int32_t* ids;     // [T][k] (routing read from memory)
   const float* w;         // [T][k]
-  const float* logits;    // [T][E]: when not null the kernel routes its own tokens (E <= 256) and one extra
-                          // cluster writes every routing output to `out`
+  const float* logits;    // [T][E]: when not null the kernel routes its own tokens (E <= 256) and its last
+                          // CTA writes every routing output to `out`
   RouteOut out;           // routing outputs written by the kernel (logits != null)
   int block_rows;         // tile height of the block map it writes
   uint16_t* Y;            // [T][d] bf16
-  float* part;            // [kDecodeMaxClusters][T][d] fp32 partial outputs
+  uint8_t* hbuf;          // h records of the call's slots, decode_scratch_bytes, 16-byte aligned
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms;
 };
 
 bool decode_supported(int T, int d, int I, int I_shared, int k);
-size_t decode_partial_bytes(int T, int d);  // bytes of the partial outputs
-int decode_box_superrows(int d);  // 128-byte super-rows per down-projection box
+size_t decode_scratch_bytes(int T, int I, int I_shared);  // global scratch: the h records
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
                           cudaStream_t stream, bool pdl);
 

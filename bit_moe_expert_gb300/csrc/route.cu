@@ -391,8 +391,26 @@ __global__ void prepack_kernel(const uint16_t* __restrict__ scale, const uint16_
   }
 }
 
+// Inside a word, codes k = 0..7 (k at bits 4k) are reordered so that code 2p
+// sits at bits 4p and code 2p+1 at bits 4p+16: one mask then takes a pair of
+// adjacent codes into the two halves of a 32-bit register.
+__device__ __forceinline__ uint32_t interleave_nibbles(uint32_t w) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int k = 2 * (i & 3) + (i >> 2);
+    r |= ((w >> (4 * k)) & 0xFu) << (4 * i);
+  }
+  return r;
+}
+__device__ __forceinline__ uint4 interleave_nibbles(uint4 v) {
+  return make_uint4(interleave_nibbles(v.x), interleave_nibbles(v.y), interleave_nibbles(v.z),
+                    interleave_nibbles(v.w));
+}
+
 // codes [E][N][K/8] -> [E][K/64][N][8]: each row's 32-byte piece of one group
-// moves next to the same group's piece of the next row
+// moves next to the same group's piece of the next row; the codes of every
+// word are interleaved (interleave_nibbles)
 __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, int G, uint4* __restrict__ qp) {
   const size_t total = static_cast<size_t>(E) * G * N;  // 32-byte pieces
   for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
@@ -402,9 +420,8 @@ __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, 
     const int g = static_cast<int>(eg % G);
     const int e = static_cast<int>(eg / G);
     const size_t i = (static_cast<size_t>(e) * N + n) * G + g;
-    const uint4 a = q[2 * i], b = q[2 * i + 1];
-    qp[2 * o] = a;
-    qp[2 * o + 1] = b;
+    qp[2 * o] = interleave_nibbles(q[2 * i]);
+    qp[2 * o + 1] = interleave_nibbles(q[2 * i + 1]);
   }
 }
 }  // namespace

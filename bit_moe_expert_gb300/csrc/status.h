@@ -12,10 +12,10 @@ namespace bm {
 struct WsHeader {
   uint32_t status;     // first device-side error (moe_status), 0 = none
   uint32_t ticket;     // arrival counter of the routing kernel; reset by its last CTA
-  uint32_t dec_arrive;  // decode kernel: CTAs that have written their partial output (grid barrier)
-  uint32_t dec_done;    // decode kernel: CTAs that have finished; the last resets both
   uint32_t route_done;  // routing kernel (grid-synchronised mode): CTAs that have finished
-  uint32_t pad[59];
+  uint32_t dec_gen;     // decode kernel: calls so far; call g counts its barrier arrivals in dec_count[g % 2]
+  uint32_t dec_count[2];
+  uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header must be 256 bytes");
 

@@ -64,8 +64,11 @@ const char* moe_status_string(moe_status s);
  * multiple of 64):
  *   q   uint32 [E][K/64][N][8]  the codes, group-major: the 8 words of row n,
  *                            columns 64g .. 64g+63 sit at [e][g][n][0..7];
- *                            inside a word the code of column k sits in bits
- *                            4*(k%8) (low nibble = lowest k).  Build it once
+ *                            inside a word the 8 codes are interleaved: the
+ *                            code of column 8j+2p sits in bits 4p and that of
+ *                            column 8j+2p+1 in bits 4p+16 (p = 0..3), so one
+ *                            mask takes two adjacent columns into the halves
+ *                            of a register.  Build it once
  *                            per weight set with moe_prepack_codes from the
  *                            row-major [E][N][K/8] checkpoint layout;
  *   sb  uint32 [E][K/64][N]  the group parameters, transposed so one group of
@@ -95,7 +98,8 @@ size_t moe_prepack_bytes(int E, int N, int K);
  * its K/8 words) into the group-major layout qp [E][K/64][N][8] that
  * moe_forward reads: the 32-byte piece of every row for one group of 64
  * columns becomes contiguous, so one group of many rows is one contiguous
- * block.  A pure data movement (same size, E*N*K/2 bytes); bit-exact.  Both
+ * block, and the codes inside each word are interleaved (see above).  A pure
+ * data movement (same size, E*N*K/2 bytes); bit-exact.  Both
  * pointers 16-byte aligned device memory, not overlapping.  Sizes: E >= 1,
  * N >= 1, K a positive multiple of 64.  Returns MOE_ERR_INVALID_ARG on a bad
  * size or pointer. */

@@ -52,8 +52,26 @@ def test_prepack_codes_is_exact_reordering():
         qp = torch.empty((E, K // 64, N, 8), dtype=torch.int32, device="cuda")
         bm.moe_prepack_codes(qd, qp)
         got = qp.cpu().numpy().view(np.uint32)
-        ref = q.reshape(E, N, K // 64, 8).transpose(0, 2, 1, 3)
+        ref = _interleave_nibbles(q.reshape(E, N, K // 64, 8).transpose(0, 2, 1, 3))
         np.testing.assert_array_equal(got, ref)
+
+
+def _interleave_nibbles(w):
+    """The prepacked word order: column 2p of a word's eight in bits 4p,
+    column 2p+1 in bits 4p+16."""
+    out = np.zeros_like(w)
+    for p in range(4):
+        for h in range(2):
+            k = 2 * p + h
+            out |= ((w >> np.uint32(4 * k)) & np.uint32(0xF)) << np.uint32(4 * p + 16 * h)
+    return out
+
+
+def test_interleave_nibbles_helper():
+    # column k of the word holds value k: the interleaved word reads, from the
+    # low nibble up, columns 0 2 4 6 1 3 5 7
+    w = np.array([0x76543210], dtype=np.uint32)
+    assert int(_interleave_nibbles(w)[0]) == 0x75316420
 
 
 # ------------------------------------------------------------------ routing
