@@ -266,20 +266,20 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
 
   if (path == Path::kGemv) {
     DecodeMaps mr, ms;
-    const cuuint32_t G2 = static_cast<cuuint32_t>(I / 64);
+    const cuuint32_t G1 = static_cast<cuuint32_t>(d / 64), G2 = static_cast<cuuint32_t>(I / 64);
     bool ok = encode_codes_rows(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
               encode_codes_rows(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
               encode_codes_rows(&mr.q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2) &&
-              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, G1) &&
+              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, G1) &&
               encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kDecodeRowsDown, G2);
     if (ok && shared) {
       const cuuint32_t G2s = static_cast<cuuint32_t>(I_shared / 64);
       ok = encode_codes_rows(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
            encode_codes_rows(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
            encode_codes_rows(&ms.q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s) &&
-           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
+           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
+           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
            encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kDecodeRowsDown, G2s);
     }
     if (!ok) return MOE_ERR_CUDA;

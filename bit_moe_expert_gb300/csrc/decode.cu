@@ -48,30 +48,41 @@ namespace bm {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = 16;                   // compute warps
+constexpr int kCons = kWarps * 32;           // compute threads
+constexpr int kProducer = kWarps;            // the warp that issues every copy
+constexpr int kThreads = kCons + 32;
 constexpr int kRows1 = kDecodeRowsGU;           // gate/up rows per phase-1 item
 constexpr int kChunk = kDecodeChunkGroups;      // groups per phase-1 stage
 constexpr int kRows2 = kDecodeRowsDown;         // output rows per phase-2 block
 constexpr int kS1 = 5;                          // phase-1 stages
+constexpr int kSB1 = kS1;                       // phase-1 group-parameter buffers: one per stage
 constexpr int kS2Max = 12;                      // phase-2 stages at most
 constexpr int kMaxSlots = kMaxK * kGemvMaxT + 1;  // distinct experts of a call, plus the shared one
-constexpr uint32_t kCodeQ = kChunk * kRows1 * 32;   // bytes of one matrix's codes in a phase-1 stage
-constexpr uint32_t kCodeSB = kChunk * kRows1 * 4;   // bytes of one matrix's group parameters in a stage
-constexpr uint32_t kSt1 = 2 * kCodeQ + 2 * kCodeSB;  // phase-1 stage: gate codes, up codes, gate sb, up sb
+constexpr uint32_t kCodeQ = kChunk * kRows1 * 32;  // bytes of one matrix's codes in a phase-1 stage
+constexpr uint32_t kSt1 = 2 * kCodeQ;               // phase-1 stage: gate codes, up codes
 constexpr size_t kSmemMax = 227 * 1024;
 
 static_assert(kWarps == 2 * kChunk, "phase 1 gives one warp to each (matrix, group) of a stage");
 static_assert(kRows1 == 32 && kRows2 == 16, "fragment layout");
+constexpr int kBars = 2 * kS1 + 3 * kS2Max + 3;  // mbarriers: full/empty per phase-1 stage, full (codes, h)/empty per
+                                                 // phase-2 stage, x, routing weights, first h records
+
+// Named barriers over the compute warps only (the producer may be waiting
+// for room in the copy queue).
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kCons) : "memory"); }
+__device__ __forceinline__ void book_sync() { asm volatile("bar.sync 2, %0;" ::"r"(kCons) : "memory"); }
 
 __host__ __device__ constexpr int div_up(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
   int G1, nchunk, Imax, hs_stride, S2;
+  size_t sb1;                 // bytes of one item's group parameters: gate [G1][32 rows], then up
   size_t hrec;                // bytes of one slot's h record: h fp16 [T][Imax], then half-group sums fp32 [T][hs_stride]
-  size_t st2, st2_sb, st2_h;  // phase-2 stage bytes; offsets of its parameters and its h record
-  size_t ring1, xs, sx, red1, red2, wt, slot_e, rid, bk, misc, cnt, bars, ring2, total;
+  size_t st2, st2_sb;         // phase-2 stage bytes (codes, then parameters); offset of the parameters
+  size_t hring;               // h records of the phase-2 stages, [S2][hrec], consecutive like the global ones
+  size_t ring1, sbuf1, xs, sx, red1, red2, wt, slot_e, rid, bk, misc, cnt, bars, ring2, total;
 };
 
 // TMA and bulk-copy destinations start on 128 bytes.
@@ -84,11 +95,13 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
   L.hs_stride = static_cast<int>(round_up(L.Imax / 32, 4));
   L.hrec = static_cast<size_t>(T) * L.Imax * 2 + static_cast<size_t>(T) * L.hs_stride * 4;
   L.st2_sb = static_cast<size_t>(G2max) * kRows2 * 32;  // codes [G2][16 rows][8 words]
-  L.st2_h = round_up(L.st2_sb + static_cast<size_t>(G2max) * kRows2 * 4, 128);
-  L.st2 = round_up(L.st2_h + L.hrec, 128);
+  L.st2 = round_up(L.st2_sb + static_cast<size_t>(G2max) * kRows2 * 4, 128);
   size_t o = 0;
   L.ring1 = o;
   o += static_cast<size_t>(kS1) * kSt1;
+  L.sb1 = round_up(2ull * L.G1 * kRows1 * 4, 128);
+  L.sbuf1 = o;
+  o += kSB1 * L.sb1;
   L.xs = o;  // x of every token, bf16 [T][d]
   o += round_up(static_cast<size_t>(T) * d * 2, 128);
   L.sx = o;  // sums of x over each group [T][G1]
@@ -101,8 +114,10 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
   o += static_cast<size_t>(kMaxSlots) * T * 4;
   L.slot_e = o;  // expert of each slot
   o += round_up(kMaxSlots * 4, 16);
-  L.rid = o;  // the call's assignments: expert [T*k], weight [T*k], slot [T*k]
-  o += 3ull * T * kMaxK * 4;
+  L.rid = o;  // the call's assignments: expert, weight, slot, selected logit [T*k] each; exp terms fp64 [T*k]
+  o += 4ull * T * kMaxK * 4;
+  o = round_up(o, 8);
+  o += 8ull * T * kMaxK;
   L.bk = o;  // routing outputs' scratch: counts [E], offsets [E+1], tile offsets [E+1] (E <= 256)
   o += 3 * 260 * 4;
   L.misc = o;  // distinct routed experts
@@ -110,15 +125,16 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
   L.cnt = o;  // per-stage consumption counters; the job each phase-2 stage was last issued
   o += (kS1 + 2 * kS2Max) * 4;
   o = round_up(o, 8);
-  L.bars = o;  // phase-1 stages, phase-2 codes, phase-2 h records, x
-  o += static_cast<size_t>(kS1 + 2 * kS2Max + 1) * 8;
+  L.bars = o;  // mbarriers
+  o += static_cast<size_t>(kBars) * 8;
   o = round_up(o, 128);
   L.ring2 = o;
   const size_t room = kSmemMax > o + 128 ? kSmemMax - o - 128 : 0;
-  size_t s2 = room / L.st2;
+  size_t s2 = room / (L.st2 + L.hrec);
   if (s2 > kS2Max) s2 = kS2Max;
   L.S2 = static_cast<int>(s2);
-  L.total = o + s2 * L.st2 + 128;  // room to align the dynamic shared memory base
+  L.hring = o + s2 * L.st2;
+  L.total = L.hring + s2 * L.hrec + 128;  // room to align the dynamic shared memory base
   return L;
 }
 
@@ -207,13 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* cnt1 = reinterpret_cast<int*>(smem + L.cnt);
   int* cnt2 = cnt1 + kS1;
   int* issued2 = cnt2 + kS2Max;
-  uint64_t* full1 = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* full2c = full1 + kS1;
-  uint64_t* full2h = full2c + kS2Max;
-  uint64_t* bar_x = full2h + kS2Max;
+  uint64_t* full1 = reinterpret_cast<uint64_t*>(smem + L.bars);  // phase-1 stage loaded
+  uint64_t* empty1 = full1 + kS1;                                 // phase-1 stage consumed
+  uint64_t* full2c = empty1 + kS1;                                // phase-2 stage: down rows loaded
+  uint64_t* full2h = full2c + kS2Max;                             // phase-2 stage: h record loaded
+  uint64_t* empty2 = full2h + kS2Max;                             // phase-2 stage consumed
+  uint64_t* bar_x = empty2 + kS2Max;
+  uint64_t* bar_w = bar_x + 1;   // the routing weights are in wt
+  uint64_t* bar_h0 = bar_w + 1;  // the h records of the first min(S2, jobs) phase-2 jobs have landed
+  uint8_t* hring = smem + L.hring;
+  float* s_v = reinterpret_cast<float*>(smem + L.rid + 3ull * kT * kMaxK * 4);
+  double* s_ex = reinterpret_cast<double*>(smem + round_up(L.rid + 4ull * kT * kMaxK * 4, 8));
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kS1 + 2 * kS2Max + 1; ++i) mbar_init(&full1[i], 1);
+    for (int i = 0; i < kBars; ++i) mbar_init(&full1[i], 1);
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < kS1 + kS2Max; i += kThreads) cnt1[i] = 0;
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i < kMaxSlots * kT; i += kThreads) wt[i] = 0.0f;
   __syncthreads();
 
-  // ------------------------------------------------------------ loads
+  // ------------------------------------------------------------ loads (the producer warp)
   // Phase-1 job j of this CTA: chunk j % nchunk of its item j / nchunk.
   auto item_slot = [&](int it, int& slot, int& rb) {
     if (it < it_s) {
@@ -233,23 +256,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       rb = v % it_r;
     }
   };
-  auto issue1 = [&](int j, uint64_t pol) {
-    const int stage = j % kS1, ch = j % L.nchunk;
+  // The item's group parameters (every group of its 32 rows, both matrices)
+  // come with its first chunk, into the parameter buffer of that chunk's
+  // stage; the stage's next first chunk is issued only once this item has
+  // been consumed, so the buffer lives as long as the item.
+  auto issue1 = [&](int j) {
+    const int stage = j % kS1, ch = j % L.nchunk, il = j / L.nchunk;
     int slot, rb;
-    item_slot(cta + (j / L.nchunk) * nC, slot, rb);
+    item_slot(cta + il * nC, slot, rb);
     const bool sh = has_shared && slot == 0;
     const int e = sh ? 0 : slot_e[slot];
     const DecodeMaps& m = sh ? ms : mr;
     uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1;
     uint64_t* bar = &full1[stage];
-    mbar_arrive_expect_tx(bar, kSt1);
-    tma_load_3d_hint(st, &m.q_gate, bar, rb * kRows1 * 8, ch * kChunk, e, pol);
-    tma_load_3d_hint(st + kCodeQ, &m.q_up, bar, rb * kRows1 * 8, ch * kChunk, e, pol);
-    tma_load_3d_hint(st + 2 * kCodeQ, &m.sb_gate, bar, rb * kRows1, ch * kChunk, e, pol);
-    tma_load_3d_hint(st + 2 * kCodeQ + kCodeSB, &m.sb_up, bar, rb * kRows1, ch * kChunk, e, pol);
+    const uint32_t sbb = static_cast<uint32_t>(L.G1) * kRows1 * 4;
+    mbar_arrive_expect_tx(bar, kSt1 + (ch == 0 ? 2 * sbb : 0u));
+    tma_load_3d(st, &m.q_gate, bar, rb * kRows1 * 8, ch * kChunk, e);
+    tma_load_3d(st + kCodeQ, &m.q_up, bar, rb * kRows1 * 8, ch * kChunk, e);
+    if (ch == 0) {
+      uint8_t* sbd = smem + L.sbuf1 + static_cast<size_t>(stage) * L.sb1;
+      tma_load_3d(sbd, &m.sb_gate, bar, rb * kRows1, 0, e);
+      tma_load_3d(sbd + sbb, &m.sb_up, bar, rb * kRows1, 0, e);
+    }
   };
   // Phase-2 job j2: slot j2 % nsl of the CTA's row block j2 / nsl.
-  auto issue2c = [&](int j2, int nsl, uint64_t pol) {
+  auto issue2c = [&](int j2, int nsl) {
     const int stage = j2 % L.S2, slot = j2 % nsl;
     const int rb = cta + (j2 / nsl) * nC;
     const bool sh = has_shared && slot == 0;
@@ -259,15 +290,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
     uint64_t* bar = &full2c[stage];
     mbar_arrive_expect_tx(bar, gx * kRows2 * (32 + 4));
-    tma_load_3d_hint(st, &m.q_down, bar, rb * kRows2 * 8, 0, e, pol);
-    tma_load_3d_hint(st + L.st2_sb, &m.sb_down, bar, rb * kRows2, 0, e, pol);
+    tma_load_3d(st, &m.q_down, bar, rb * kRows2 * 8, 0, e);
+    tma_load_3d(st + L.st2_sb, &m.sb_down, bar, rb * kRows2, 0, e);
   };
   auto issue2h = [&](int j2, int nsl) {
     const int stage = j2 % L.S2, slot = j2 % nsl;
     uint64_t* bar = &full2h[stage];
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(L.hrec));
-    bulk_g2s(ring2 + static_cast<size_t>(stage) * L.st2 + L.st2_h, a.hbuf + static_cast<size_t>(slot) * L.hrec,
+    bulk_g2s(hring + static_cast<size_t>(stage) * L.hrec, a.hbuf + static_cast<size_t>(slot) * L.hrec,
              static_cast<uint32_t>(L.hrec), bar);
+  };
+  // The same copies issued by the whole producer warp at once, one copy per
+  // lane (a warp issues copies about three times faster than one lane issuing
+  // them in turn): first every barrier's byte count, then the copies.
+  //   phase-1 jobs [j0, j0 + n), n <= 8: lane 4i + c issues copy c of job j0 + i
+  //   (gate codes, up codes, gate parameters, up parameters; the last two with
+  //   an item's first chunk only)
+  auto issue1_warp = [&](int j0, int n) {
+    const uint32_t sbb = static_cast<uint32_t>(L.G1) * kRows1 * 4;
+    if (lane < n) {
+      const int j = j0 + lane;
+      mbar_arrive_expect_tx(&full1[j % kS1], kSt1 + (j % L.nchunk == 0 ? 2 * sbb : 0u));
+    }
+    __syncwarp();
+    const int i = lane >> 2, c = lane & 3;
+    const int j = j0 + i, ch = j % L.nchunk, il = j / L.nchunk;
+    if (i < n && (c < 2 || ch == 0)) {
+      int slot, rb;
+      item_slot(cta + il * nC, slot, rb);
+      const bool sh = has_shared && slot == 0;
+      const int e = sh ? 0 : slot_e[slot];
+      const DecodeMaps& m = sh ? ms : mr;
+      const int stage = j % kS1;
+      uint64_t* bar = &full1[stage];
+      if (c < 2) {
+        tma_load_3d(ring1 + static_cast<size_t>(stage) * kSt1 + c * kCodeQ, c == 0 ? &m.q_gate : &m.q_up, bar,
+                    rb * kRows1 * 8, ch * kChunk, e);
+      } else {
+        tma_load_3d(smem + L.sbuf1 + static_cast<size_t>(stage) * L.sb1 + (c - 2) * sbb, c == 2 ? &m.sb_gate : &m.sb_up,
+                    bar, rb * kRows1, 0, e);
+      }
+    }
+  };
+  //   phase-2 jobs [j0, j0 + n), n <= 16: lane 2i + c issues the codes (c = 0) or
+  //   the parameters (c = 1) of job j0 + i
+  auto issue2c_warp = [&](int j0, int n, int nsl) {
+    if (lane < n) {
+      const int j2 = j0 + lane, slot = j2 % nsl;
+      const uint32_t gx = static_cast<uint32_t>(has_shared && slot == 0 ? G2s : G2);
+      mbar_arrive_expect_tx(&full2c[j2 % L.S2], gx * kRows2 * (32 + 4));
+    }
+    __syncwarp();
+    const int i = lane >> 1, c = lane & 1;
+    if (i < n) {
+      const int j2 = j0 + i, stage = j2 % L.S2, slot = j2 % nsl;
+      const int rb = cta + (j2 / nsl) * nC;
+      const bool sh = has_shared && slot == 0;
+      const int e = sh ? 0 : slot_e[slot];
+      const DecodeMaps& m = sh ? ms : mr;
+      uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
+      if (c == 0) tma_load_3d(st, &m.q_down, &full2c[stage], rb * kRows2 * 8, 0, e);
+      else tma_load_3d(st + L.st2_sb, &m.sb_down, &full2c[stage], rb * kRows2, 0, e);
+    }
   };
 
   // The shared expert's loads need no routing and do not depend on the
@@ -278,26 +362,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_sh_items = cta < it_s ? div_up(it_s - cta, nC) : 0;
   const int pre1 = min(kS1, my_sh_items * L.nchunk);
   const int pre2 = has_shared && my_rbs > 0 ? 1 : 0;
-  if (warp == 0) {
-    const uint64_t pol = l2_policy_evict_first();  // every weight byte is read once
-    if (lane < pre1) issue1(lane, pol);
-    if (lane == 31 && pre2) issue2c(0, 1, pol);
-  } else if (warp == 1) {
-    if (lane == 0) {
+  if (warp == kProducer) {
+    issue1_warp(0, pre1);
+    if (pre2) issue2c_warp(0, 1, 1);
+    if (lane == 1) {
       tma_prefetch_desc(&mr.q_gate);
       tma_prefetch_desc(&mr.q_up);
       tma_prefetch_desc(&mr.sb_gate);
       tma_prefetch_desc(&mr.sb_up);
       tma_prefetch_desc(&mr.q_down);
       tma_prefetch_desc(&mr.sb_down);
+    } else if (lane == 2 && has_shared) {
+      tma_prefetch_desc(&ms.q_gate);
+      tma_prefetch_desc(&ms.q_up);
+      tma_prefetch_desc(&ms.sb_gate);
+      tma_prefetch_desc(&ms.sb_up);
+      tma_prefetch_desc(&ms.q_down);
+      tma_prefetch_desc(&ms.sb_down);
     }
+  } else if (warp == 1) {
+    // Loads (values unused) bring the router logits and X into L2 now; they
+    // are read for use after the wait (L2 is where a write by the previous
+    // kernel lands, so a line fetched early is never stale there).
     const char* lg = reinterpret_cast<const char*>(a.logits);
     const char* xp = reinterpret_cast<const char*>(a.X);
     if (lg)
-      for (int off = lane * 128; off < kT * a.E * 4; off += 32 * 128) prefetch_l2(lg + off);
-    for (int off = lane * 128; off < kT * d * 2; off += 32 * 128) prefetch_l2(xp + off);
+      for (int off = lane * 128; off < kT * a.E * 4; off += 32 * 128) touch_l2(lg + off);
+    for (int off = lane * 128; off < kT * d * 2; off += 32 * 128) touch_l2(xp + off);
   }
   pdl_wait();  // X, the routing and the previous layer's use of the workspace
+  // Call g of this workspace counts barrier arrivals in dec_count[g % 2]; read
+  // before the CTA's first barrier so it precedes every arrival of the call.
+  const uint32_t gen = *reinterpret_cast<volatile uint32_t*>(&hdr->dec_gen);
 
   if (threadIdx.x == 32 * kGemvMaxT) {  // X into shared memory
     mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(kT * d * 2));
@@ -314,7 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool finite;
       warp_topk_select<8>(a.logits + static_cast<size_t>(warp) * a.E, a.E, a.k, lane, sel_i, sel_v, finite);
       if (bookkeeper && !finite && lane == 0) record_status(a.status, MOE_ERR_NONFINITE);
-      if (lane < a.k) s_ids[warp * a.k + lane] = sel_i;
+      if (lane < a.k) {
+        s_ids[warp * a.k + lane] = sel_i;
+        s_v[warp * a.k + lane] = sel_v;
+      }
     } else {
       for (int i = lane; i < a.k; i += 32) {
         s_ids[warp * a.k + i] = __ldcg(a.ids + warp * a.k + i);
@@ -376,343 +475,397 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (has_shared && lane == 0) slot_e[0] = 0;
       if (lane == 0) misc[0] = nsl - rs0;
       __syncwarp();
-      asm volatile("bar.arrive 4, 64;" ::: "memory");  // the slots are known: warp 4 issues the phase-2 loads
-      // the routed experts' gate/up loads start as soon as they are known
-      const int NI = it_s + (nsl - rs0) * it_r;
-      const int my_items = cta < NI ? div_up(NI - cta, nC) : 0;
-      const int n1 = min(kS1, my_items * L.nchunk) - pre1;
-      if (lane < n1) issue1(pre1 + lane, l2_policy_evict_first());
-    }
-  } else {
-    if (warp == kGemvMaxT) {
-      asm volatile("bar.sync 4, 64;" ::: "memory");
-      const int nsl = rs0 + misc[0];
-      const int n2 = min(L.S2, my_rbs * nsl) - pre2;
-      if (lane < n2) issue2c(pre2 + lane, nsl, l2_policy_evict_first());
-    }
-    // the other warps: sums of x over each group of 64 columns, 8 threads per (token, group)
-    const int t0 = threadIdx.x - 32 * kGemvMaxT;
-    if (t0 >= 0) {
-      ok &= mbar_wait(bar_x, 0, nullptr);
-      constexpr int kSum = kThreads - 32 * kGemvMaxT;
-      for (int i = t0; i < div_up(kT * L.G1 * 8, kSum) * kSum; i += kSum) {
-        const int pair = i >> 3, part = i & 7;
-        float v = 0.0f;
-        if (pair < kT * L.G1) {
-          const int t = pair / L.G1, gi = pair % L.G1;
-          const uint4 u = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(t) * d + gi * 64 + part * 8);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) v += bf16_lo(w[c]) + bf16_hi(w[c]);
-        }
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        if (pair < kT * L.G1 && part == 0) sx[pair] = v;
+      if (!fused) {  // weights read from memory are placed now
+        for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = s_w[i];
+        if (has_shared && lane < kT) wt[lane] = 1.0f;
       }
     }
   }
-  __syncthreads();
+  __syncthreads();  // the slots are known
   const int nsl_r = misc[0];
   const int nsl = rs0 + nsl_r;
   pdl_launch_dependents();
-
-  // Routing weights are needed only in phase 2.  Read from memory, they are
-  // placed now; computed here (fp64, slow on this GPU), only the CTA that
-  // writes the routing outputs computes them, and every CTA reads them back
-  // after the barrier.
-  if (!fused && warp == 0) {
-    for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = s_w[i];
-    if (has_shared && lane < kT) wt[lane] = 1.0f;
-  }
-  if (bookkeeper) {
-    if (warp < kT) {
-      const float w = warp_topk_weights(sel_v, a.k, lane);
-      if (lane < a.k) s_w[warp * a.k + lane] = w;
-    }
-    asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");  // the weights are in s_w
-    // every routing output, as the routing kernel writes it for one chunk:
-    // ids and weights, counts, exclusive offsets, the stable permutation and
-    // the tile block map (experts ascending)
-    int* cnt = reinterpret_cast<int*>(smem + L.bk);  // [E]
-    int* off = cnt + a.E;                             // [E + 1]
-    int* boff = off + a.E + 1;                        // [E + 1]
-    for (int i = threadIdx.x; i < na; i += kThreads) {
-      a.out.ids[i] = s_ids[i];
-      a.out.w[i] = s_w[i];
-    }
-    for (int e = threadIdx.x; e < a.E; e += kThreads) cnt[e] = 0;
-    asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
-    for (int i = threadIdx.x; i < na; i += kThreads) atomicAdd(&cnt[s_ids[i]], 1);
-    asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
-    if (warp == 0) {
-      int run = 0, brun = 0;
-      for (int e0 = 0; e0 < a.E; e0 += 32) {
-        const int e = e0 + lane;
-        const int c = e < a.E ? cnt[e] : 0;
-        const int b = (c + a.block_rows - 1) / a.block_rows;
-        int ic = c, ib = b;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int c2 = __shfl_up_sync(0xffffffffu, ic, o);
-          const int b2 = __shfl_up_sync(0xffffffffu, ib, o);
-          if (lane >= o) {
-            ic += c2;
-            ib += b2;
-          }
-        }
-        if (e < a.E) {
-          off[e] = run + ic - c;
-          boff[e] = brun + ib - b;
-        }
-        run += __shfl_sync(0xffffffffu, ic, 31);
-        brun += __shfl_sync(0xffffffffu, ib, 31);
-      }
-      if (lane == 0) {
-        off[a.E] = run;
-        boff[a.E] = brun;
-        *a.out.num_blocks = brun;
-      }
-    }
-    asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");
-    for (int e = threadIdx.x; e < a.E; e += kThreads) a.out.counts[e] = cnt[e];
-    for (int e = threadIdx.x; e <= a.E; e += kThreads) a.out.offsets[e] = off[e];
-    for (int i = threadIdx.x; i < na; i += kThreads) {
-      const int e = s_ids[i];
-      int r = 0;
-      for (int j = 0; j < i; ++j) r += s_ids[j] == e;
-      const int pos = off[e] + r;
-      a.out.perm[pos] = i;
-      a.out.inv_perm[i] = pos;
-    }
-    for (int e = threadIdx.x; e < a.E; e += kThreads) {
-      const int c = cnt[e];
-      int b = boff[e];
-      for (int r = 0; r < c; r += a.block_rows, ++b) {
-        a.out.block_map[3 * b + 0] = e;
-        a.out.block_map[3 * b + 1] = off[e] + r;
-        a.out.block_map[3 * b + 2] = min(a.block_rows, c - r);
-      }
-    }
-  }
-
-  // ------------------------------------------------------------ phase 1: h of this CTA's items
   const int NI = it_s + nsl_r * it_r;
   const int my_items = cta < NI ? div_up(NI - cta, nC) : 0;
   const int total1 = my_items * L.nchunk;
-  const int mat = warp >> 3;  // 0: gate, 1: up
-  const int gl = warp & 7;    // group inside a stage
-  for (int il = 0; il < my_items; ++il) {
-    int slot, rb;
-    item_slot(cta + il * nC, slot, rb);
-    float acc[2][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.0f;
-    for (int ch = 0; ch < L.nchunk; ++ch) {
-      const int j = il * L.nchunk + ch, stage = j % kS1;
-      ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
-      const int gi = ch * kChunk + gl;
-      if (gi < L.G1) {
-        const uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1;
-        const uint32_t* qm = reinterpret_cast<const uint32_t*>(st + mat * kCodeQ) + gl * kRows1 * 8;
-        const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + 2 * kCodeQ + mat * kCodeSB) + gl * kRows1;
-        uint32_t b[8];
-        load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
-        const float sxa = 2 * q4 < kT ? sx[(2 * q4) * L.G1 + gi] : 0.0f;
-        const float sxb = 2 * q4 + 1 < kT ? sx[(2 * q4 + 1) * L.G1 + gi] : 0.0f;
-#pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-          const int r0 = tile * 16 + g8;
-          const uint2 wa = *reinterpret_cast<const uint2*>(qm + r0 * 8 + 2 * q4);
-          const uint2 wb = *reinterpret_cast<const uint2*>(qm + (r0 + 8) * 8 + 2 * q4);
-          float dd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          mma_group<true>(wa, wb, b, dd);
-          const uint32_t p0 = sbm[r0], p1 = sbm[r0 + 8];
-          const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 128.0f * s0;
-          const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 128.0f * s1;
-          acc[tile][0] += fmaf(s0, dd[0], c0 * sxa);
-          acc[tile][1] += fmaf(s0, dd[1], c0 * sxb);
-          acc[tile][2] += fmaf(s1, dd[2], c1 * sxa);
-          acc[tile][3] += fmaf(s1, dd[3], c1 * sxb);
+  const int total2 = my_rbs * nsl;
+
+  if (warp == kProducer) {
+    // -------------------------------------------------------- producer
+    // Every copy of the CTA, in the order the compute warps use them: the
+    // gate/up chunks (refilling a stage once the compute warps have released
+    // it), the down rows, then, after the barrier over the grid, the h
+    // records.  Issuing a copy waits while the SM's copy queue is full, so no
+    // compute warp issues any.
+    issue1_warp(pre1, min(kS1, total1) - pre1);
+    for (int j0 = pre2, n2 = min(L.S2, total2); j0 < n2; j0 += 16) issue2c_warp(j0, min(16, n2 - j0), nsl);
+    // The routing weights (fp64, slow on this GPU), while the copies stream:
+    // softmax over each token's selected logits, summed in selection order and
+    // rounded once (the routing kernel's arithmetic, so the same bits).
+    if (fused) {
+      for (int i = lane; i < na; i += 32)
+        s_ex[i] = exp(static_cast<double>(s_v[i]) - static_cast<double>(s_v[(i / a.k) * a.k]));
+      __syncwarp();
+      for (int i = lane; i < na; i += 32) {
+        double sum = 0.0;
+        for (int j = 0; j < a.k; ++j) sum += s_ex[(i / a.k) * a.k + j];
+        wt[s_slot[i] * kT + i / a.k] = static_cast<float>(s_ex[i] / sum);
+      }
+      if (has_shared && lane < kT) wt[lane] = 1.0f;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_w);  // releases the weights to the compute warps
+    if (lane == 0) {
+      for (int j = kS1; j < total1; ++j) {
+        ok &= mbar_wait(&empty1[j % kS1], static_cast<uint32_t>(j / kS1 - 1) & 1u, nullptr);
+        issue1(j);
+      }
+      // the barrier: every CTA has written its h records.  CTA 0 then clears
+      // the other counter (last used by call g - 1, which has finished) and
+      // advances the call number for call g + 1 (read only after this call).
+      uint32_t* count = &hdr->dec_count[gen & 1u];
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(count) < static_cast<uint32_t>(nC)) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          record_status(a.status, MOE_ERR_TIMEOUT);
+          break;
         }
       }
-      // the last warp done with a stage refills it
-      __syncwarp();
-      if (lane == 0) {
-        const int old = atomicAdd(&cnt1[stage], 1);
-        if ((old + 1) % kWarps == 0 && j + kS1 < total1) {
-          fence_proxy_async_smem();
-          issue1(j + kS1, l2_policy_evict_first());
+      if (cta == 0) {
+        hdr->dec_count[(gen + 1) & 1u] = 0;
+        hdr->dec_gen = gen + 1;
+      }
+    }
+    if (lane == 0) {
+      // the h records of jobs [0, n0): consecutive jobs of one row block are
+      // consecutive slots, so each run is one copy into consecutive stages
+      fence_proxy_async_global();
+      const int n0 = min(L.S2, total2);
+      if (n0 > 0) {
+        mbar_arrive_expect_tx(bar_h0, static_cast<uint32_t>(n0 * L.hrec));
+        for (int j = 0; j < n0;) {
+          const int run = min(nsl - j % nsl, n0 - j);
+          bulk_g2s(hring + static_cast<size_t>(j) * L.hrec, a.hbuf + static_cast<size_t>(j % nsl) * L.hrec,
+                   static_cast<uint32_t>(run * L.hrec), bar_h0);
+          j += run;
+        }
+      }
+      for (int j2 = L.S2; j2 < total2; ++j2) {
+        const int stage = j2 % L.S2;
+        ok &= mbar_wait(&empty2[stage], static_cast<uint32_t>(j2 / L.S2 - 1) & 1u, nullptr);
+        *reinterpret_cast<volatile int*>(issued2 + stage) = j2;
+        issue2c(j2, nsl);
+        issue2h(j2, nsl);
+      }
+    }
+  } else {
+    // -------------------------------------------------------- compute warps
+    {
+      // sums of x over each group of 64 columns, 8 threads per (token, group)
+      const int t0 = threadIdx.x - 32 * (kGemvMaxT + 1);
+      if (t0 >= 0) {
+        ok &= mbar_wait(bar_x, 0, nullptr);
+        constexpr int kSum = kCons - 32 * (kGemvMaxT + 1);
+        for (int i = t0; i < div_up(kT * L.G1 * 8, kSum) * kSum; i += kSum) {
+          const int pair = i >> 3, part = i & 7;
+          float v = 0.0f;
+          if (pair < kT * L.G1) {
+            const int t = pair / L.G1, gi = pair % L.G1;
+            const uint4 u = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(t) * d + gi * 64 + part * 8);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v += bf16_lo(w[c]) + bf16_hi(w[c]);
+          }
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          if (pair < kT * L.G1 && part == 0) sx[pair] = v;
         }
       }
     }
-    // h of the item's 32 features for every token
+    cons_sync();
+
+    // Routing weights (fp64, slow on this GPU) are computed only by the CTA
+    // that writes the routing outputs; the others read them after the barrier.
+    if (bookkeeper) {
+      if (warp < kT) {
+        const float w = warp_topk_weights(sel_v, a.k, lane);
+        if (lane < a.k) s_w[warp * a.k + lane] = w;
+      }
+      book_sync();  // the weights are in s_w
+      // every routing output, as the routing kernel writes it for one chunk:
+      // ids and weights, counts, exclusive offsets, the stable permutation and
+      // the tile block map (experts ascending)
+      int* cnt = reinterpret_cast<int*>(smem + L.bk);  // [E]
+      int* off = cnt + a.E;                             // [E + 1]
+      int* boff = off + a.E + 1;                        // [E + 1]
+      for (int i = threadIdx.x; i < na; i += kCons) {
+        a.out.ids[i] = s_ids[i];
+        a.out.w[i] = s_w[i];
+      }
+      for (int e = threadIdx.x; e < a.E; e += kCons) cnt[e] = 0;
+      book_sync();
+      for (int i = threadIdx.x; i < na; i += kCons) atomicAdd(&cnt[s_ids[i]], 1);
+      book_sync();
+      if (warp == 0) {
+        int run = 0, brun = 0;
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+          const int e = e0 + lane;
+          const int c = e < a.E ? cnt[e] : 0;
+          const int b = (c + a.block_rows - 1) / a.block_rows;
+          int ic = c, ib = b;
 #pragma unroll
-    for (int tile = 0; tile < 2; ++tile) {
-      const int r0 = tile * 16 + g8;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int c2 = __shfl_up_sync(0xffffffffu, ic, o);
+            const int b2 = __shfl_up_sync(0xffffffffu, ib, o);
+            if (lane >= o) {
+              ic += c2;
+              ib += b2;
+            }
+          }
+          if (e < a.E) {
+            off[e] = run + ic - c;
+            boff[e] = brun + ib - b;
+          }
+          run += __shfl_sync(0xffffffffu, ic, 31);
+          brun += __shfl_sync(0xffffffffu, ib, 31);
+        }
+        if (lane == 0) {
+          off[a.E] = run;
+          boff[a.E] = brun;
+          *a.out.num_blocks = brun;
+        }
+      }
+      book_sync();
+      for (int e = threadIdx.x; e < a.E; e += kCons) a.out.counts[e] = cnt[e];
+      for (int e = threadIdx.x; e <= a.E; e += kCons) a.out.offsets[e] = off[e];
+      for (int i = threadIdx.x; i < na; i += kCons) {
+        const int e = s_ids[i];
+        int r = 0;
+        for (int j = 0; j < i; ++j) r += s_ids[j] == e;
+        const int pos = off[e] + r;
+        a.out.perm[pos] = i;
+        a.out.inv_perm[i] = pos;
+      }
+      for (int e = threadIdx.x; e < a.E; e += kCons) {
+        const int c = cnt[e];
+        int b = boff[e];
+        for (int r = 0; r < c; r += a.block_rows, ++b) {
+          a.out.block_map[3 * b + 0] = e;
+          a.out.block_map[3 * b + 1] = off[e] + r;
+          a.out.block_map[3 * b + 2] = min(a.block_rows, c - r);
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ phase 1: h of this CTA's items
+    const int mat = warp >> 3;  // 0: gate, 1: up
+    const int gl = warp & 7;    // group inside a stage
+    for (int il = 0; il < my_items; ++il) {
+      int slot, rb;
+      item_slot(cta + il * nC, slot, rb);
+      const uint32_t* sbi =
+          reinterpret_cast<const uint32_t*>(smem + L.sbuf1 + static_cast<size_t>((il * L.nchunk) % kS1) * L.sb1) +
+          mat * L.G1 * kRows1;
+      float acc[2][4];  // [tile][fragment]
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.0f;
+      for (int ch = 0; ch < L.nchunk; ++ch) {
+        const int j = il * L.nchunk + ch, stage = j % kS1;
+        ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
+        const int gi = ch * kChunk + gl;  // this warp's group
+        if (gi < L.G1) {
+          const uint32_t* qm = reinterpret_cast<const uint32_t*>(ring1 + static_cast<size_t>(stage) * kSt1 + mat * kCodeQ) +
+                               gl * kRows1 * 8;
+          const uint32_t* sbm = sbi + gi * kRows1;
+          uint32_t b[8];
+          load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
+          const float sxa = 2 * q4 < kT ? sx[(2 * q4) * L.G1 + gi] : 0.0f;
+          const float sxb = 2 * q4 + 1 < kT ? sx[(2 * q4 + 1) * L.G1 + gi] : 0.0f;
+          float dd[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+          for (int tile = 0; tile < 2; ++tile) {
+            const int r0 = tile * 16 + g8;
+            const uint2 wa = *reinterpret_cast<const uint2*>(qm + r0 * 8 + 2 * q4);
+            const uint2 wb = *reinterpret_cast<const uint2*>(qm + (r0 + 8) * 8 + 2 * q4);
+            mma_group<true>(wa, wb, b, dd[tile]);
+          }
+#pragma unroll
+          for (int tile = 0; tile < 2; ++tile) {
+            const int r0 = tile * 16 + g8;
+            const uint32_t p0 = sbm[r0], p1 = sbm[r0 + 8];
+            const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 128.0f * s0;
+            const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 128.0f * s1;
+            acc[tile][0] += fmaf(s0, dd[tile][0], c0 * sxa);
+            acc[tile][1] += fmaf(s0, dd[tile][1], c0 * sxb);
+            acc[tile][2] += fmaf(s1, dd[tile][2], c1 * sxa);
+            acc[tile][3] += fmaf(s1, dd[tile][3], c1 * sxb);
+          }
+        }
+        // the last warp done with a stage releases it to the producer
+        __syncwarp();
+        if (lane == 0 && (atomicAdd(&cnt1[stage], 1) + 1) % kWarps == 0) mbar_arrive(&empty1[stage]);
+      }
+      // h of the item's 32 features for every token
+#pragma unroll
+      for (int tile = 0; tile < 2; ++tile) {
+        float* rp = red1 + (warp * kRows1 + tile * 16 + g8) * kT;
+        if (2 * q4 < kT) {
+          rp[2 * q4] = acc[tile][0];
+          rp[8 * kT + 2 * q4] = acc[tile][2];
+        }
+        if (2 * q4 + 1 < kT) {
+          rp[2 * q4 + 1] = acc[tile][1];
+          rp[8 * kT + 2 * q4 + 1] = acc[tile][3];
+        }
+      }
+      cons_sync();
+      if (warp < kT) {
+        const int t = warp, r = lane;
+        float gs = 0.0f, us = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kChunk; ++w) {
+          gs += red1[(w * kRows1 + r) * kT + t];
+          us += red1[((kChunk + w) * kRows1 + r) * kT + t];
+        }
+        const __half hh = __float2half_rn(gs / (1.0f + expf(-gs)) * us);
+        uint8_t* rec = a.hbuf + static_cast<size_t>(slot) * L.hrec;
+        reinterpret_cast<__half*>(rec)[t * L.Imax + rb * kRows1 + r] = hh;
+        float hsum = __half2float(hh);  // the sum of the values the MMA sees
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
+        if (lane == 0)
+          reinterpret_cast<float*>(rec + static_cast<size_t>(kT) * L.Imax * 2)[t * L.hs_stride + rb] = hsum;
+      }
+      cons_sync();
+    }
+
+    // ------------------------------------------------------------ arrival at the barrier over the grid
+    // Every CTA of the launch is resident (one per SM, the grid is capped at
+    // what fits); the h records written with ordinary stores are read by bulk
+    // copies after it.
+    fence_proxy_async_global();
+    cons_sync();
+    if (threadIdx.x == 0) red_release_gpu_add(&hdr->dec_count[gen & 1u], 1u);
+
+    // ------------------------------------------------------------ phase 2: Y rows of this CTA
+    // Warp w takes a contiguous run of the (slot, group) pairs of each row
+    // block: it waits for and releases each slot's stage once.
+    const int G2first = has_shared ? G2s : G2;  // groups of slot 0
+    const int pairs = (has_shared ? G2s : 0) + nsl_r * G2;
+    const int p_begin = warp * pairs / kWarps, p_end = (warp + 1) * pairs / kWarps;
+    int s_begin = 0, g_begin = p_begin;
+    if (p_begin >= G2first) {
+      s_begin = 1 + (p_begin - G2first) / G2;
+      g_begin = (p_begin - G2first) % G2;
+    }
+    for (int rl = 0; rl < my_rbs; ++rl) {
+      const int rb = cta + rl * nC;
+      float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      int slot = s_begin, gr = g_begin;
+      for (int p = p_begin; p < p_end; ++slot, gr = 0) {
+        const int gx = slot == 0 ? G2first : G2;
+        const int g_stop = min(gx, gr + (p_end - p));
+        const int j2 = rl * nsl + slot, stage = j2 % L.S2;
+        const uint32_t par = static_cast<uint32_t>(j2 / L.S2) & 1u;
+        // A warp may reach a job two uses of its stage ahead of the job the
+        // stage holds, where the parity wait would pass on the older phase:
+        // first wait until the job has been issued.
+        if (issued2_wait(issued2 + stage, j2)) ok = false;
+        ok &= mbar_wait(&full2c[stage], par, nullptr);
+        if (j2 < L.S2) ok &= mbar_wait(bar_h0, 0, nullptr);
+        else ok &= mbar_wait(&full2h[stage], static_cast<uint32_t>(j2 / L.S2 - 1) & 1u, nullptr);
+        const uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
+        const uint8_t* hr = hring + static_cast<size_t>(stage) * L.hrec;
+        const uint32_t* qm = reinterpret_cast<const uint32_t*>(st) + g8 * 8 + 2 * q4;
+        const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + L.st2_sb) + g8;
+        const uint16_t* hp = reinterpret_cast<const uint16_t*>(hr) + static_cast<size_t>(g8) * L.Imax + 16 * q4;
+        const float* hsp = reinterpret_cast<const float*>(hr + static_cast<size_t>(kT) * L.Imax * 2);
+        const float* hsa = hsp + (2 * q4) * L.hs_stride;
+        const float* hsb = hsa + L.hs_stride;
+        float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the slot's rows before its routing weight
+        // one group of 64 columns: four MMA steps, then the group's affine map
+        auto group = [&](int g, float (&dd)[4]) {
+          uint32_t b[8];
+          load_b(hp + g * 64, g8 < kT, b);
+          const uint2 wa = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8);
+          const uint2 wb = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8 + 64);
+          mma_group<false>(wa, wb, b, dd);
+        };
+        auto fold = [&](int g, const float (&dd)[4]) {
+          const uint32_t p0 = sbm[g * kRows2], p1 = sbm[g * kRows2 + 8];
+          const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 1024.0f * s0;
+          const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 1024.0f * s1;
+          const float ha = 2 * q4 < kT ? hsa[2 * g] + hsa[2 * g + 1] : 0.0f;
+          const float hb = 2 * q4 + 1 < kT ? hsb[2 * g] + hsb[2 * g + 1] : 0.0f;
+          sa[0] += fmaf(s0, dd[0], c0 * ha);
+          sa[1] += fmaf(s0, dd[1], c0 * hb);
+          sa[2] += fmaf(s1, dd[2], c1 * ha);
+          sa[3] += fmaf(s1, dd[3], c1 * hb);
+        };
+        int g = gr;
+        for (; g + 1 < g_stop; g += 2) {  // two groups in flight
+          float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          group(g, d0);
+          group(g + 1, d1);
+          fold(g, d0);
+          fold(g + 1, d1);
+        }
+        if (g < g_stop) {
+          float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          group(g, d0);
+          fold(g, d0);
+        }
+        // tokens not routed to the slot contribute nothing (their h is never used)
+        if (slot == s_begin) ok &= mbar_wait(bar_w, 0, nullptr);
+        const float ra = 2 * q4 < kT ? wt[slot * kT + 2 * q4] : 0.0f;
+        const float rb2 = 2 * q4 + 1 < kT ? wt[slot * kT + 2 * q4 + 1] : 0.0f;
+        if (ra != 0.0f) {
+          acc2[0] = fmaf(ra, sa[0], acc2[0]);
+          acc2[2] = fmaf(ra, sa[2], acc2[2]);
+        }
+        if (rb2 != 0.0f) {
+          acc2[1] = fmaf(rb2, sa[1], acc2[1]);
+          acc2[3] = fmaf(rb2, sa[3], acc2[3]);
+        }
+        // the last warp done with a stage releases it to the producer (only
+        // needed when some job waits for a stage)
+        const int done = g_stop - gr;
+        p += done;
+        if (total2 > L.S2) {
+          __syncwarp();
+          if (lane == 0) {
+            const int old = atomicAdd(&cnt2[stage], done);
+            int need = 0;  // pairs of every job this stage has held, up to this one
+            for (int jj = stage; jj <= j2; jj += L.S2) need += jj % nsl == 0 ? G2first : G2;
+            if (old + done == need) mbar_arrive(&empty2[stage]);
+          }
+        }
+      }
       if (2 * q4 < kT) {
-        red1[(warp * kRows1 + r0) * kT + 2 * q4] = acc[tile][0];
-        red1[(warp * kRows1 + r0 + 8) * kT + 2 * q4] = acc[tile][2];
+        red2[(warp * kRows2 + g8) * kT + 2 * q4] = acc2[0];
+        red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4] = acc2[2];
       }
       if (2 * q4 + 1 < kT) {
-        red1[(warp * kRows1 + r0) * kT + 2 * q4 + 1] = acc[tile][1];
-        red1[(warp * kRows1 + r0 + 8) * kT + 2 * q4 + 1] = acc[tile][3];
+        red2[(warp * kRows2 + g8) * kT + 2 * q4 + 1] = acc2[1];
+        red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4 + 1] = acc2[3];
       }
-    }
-    __syncthreads();
-    if (warp < kT) {
-      const int t = warp, r = lane;
-      float gs = 0.0f, us = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kChunk; ++w) {
-        gs += red1[(w * kRows1 + r) * kT + t];
-        us += red1[((kChunk + w) * kRows1 + r) * kT + t];
-      }
-      const __half hh = __float2half_rn(gs / (1.0f + expf(-gs)) * us);
-      uint8_t* rec = a.hbuf + static_cast<size_t>(slot) * L.hrec;
-      reinterpret_cast<__half*>(rec)[t * L.Imax + rb * kRows1 + r] = hh;
-      float hsum = __half2float(hh);  // the sum of the values the MMA sees
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
-      if (lane == 0) reinterpret_cast<float*>(rec + static_cast<size_t>(kT) * L.Imax * 2)[t * L.hs_stride + rb] = hsum;
-    }
-    __syncthreads();
-  }
-
-  // ------------------------------------------------------------ barrier over the grid
-  // Every CTA of the launch is resident (one per SM, the grid is capped at
-  // what fits); the h records written with ordinary stores are read by bulk
-  // copies after it.
-  fence_proxy_async_global();
-  __syncthreads();
-  // Call g of this workspace counts arrivals in dec_count[g % 2]; after the
-  // barrier CTA 0 clears the other counter (last used by call g - 1, which
-  // has finished) and advances the call number for call g + 1 (which reads it
-  // only after this call has finished).
-  if (threadIdx.x == 0) {
-    const uint32_t gen = *reinterpret_cast<volatile uint32_t*>(&hdr->dec_gen);
-    uint32_t* count = &hdr->dec_count[gen & 1u];
-    red_release_gpu_add(count, 1u);
-    const long long t0 = clock64();
-    while (ld_acquire_gpu(count) < static_cast<uint32_t>(nC)) {
-      if (clock64() - t0 > kWaitLimitCycles) {
-        record_status(a.status, MOE_ERR_TIMEOUT);
-        break;
-      }
-    }
-    if (cta == 0) {
-      hdr->dec_count[(gen + 1) & 1u] = 0;
-      hdr->dec_gen = gen + 1;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    fence_proxy_async_global();
-    if (lane < min(L.S2, my_rbs * nsl)) issue2h(lane, nsl);
-  } else if (warp == 1 && fused) {
-    for (int i = lane; i < na; i += 32) wt[s_slot[i] * kT + i / a.k] = __ldcg(a.out.w + i);
-    if (has_shared && lane < kT) wt[lane] = 1.0f;
-  }
-  __syncthreads();
-
-  // ------------------------------------------------------------ phase 2: Y rows of this CTA
-  // Warp w takes a contiguous run of the (slot, group) pairs of each row
-  // block: it waits for and releases each slot's stage once.
-  const int total2 = my_rbs * nsl;
-  const int G2first = has_shared ? G2s : G2;  // groups of slot 0
-  const int pairs = (has_shared ? G2s : 0) + nsl_r * G2;
-  const int p_begin = warp * pairs / kWarps, p_end = (warp + 1) * pairs / kWarps;
-  int s_begin = 0, g_begin = p_begin;
-  if (p_begin >= G2first) {
-    s_begin = 1 + (p_begin - G2first) / G2;
-    g_begin = (p_begin - G2first) % G2;
-  }
-  for (int rl = 0; rl < my_rbs; ++rl) {
-    const int rb = cta + rl * nC;
-    float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int slot = s_begin, gr = g_begin;
-    for (int p = p_begin; p < p_end; ++slot, gr = 0) {
-      const int gx = slot == 0 ? G2first : G2;
-      const int g_stop = min(gx, gr + (p_end - p));
-      const int j2 = rl * nsl + slot, stage = j2 % L.S2;
-      const uint32_t par = static_cast<uint32_t>(j2 / L.S2) & 1u;
-      // A warp may reach a job two uses of its stage ahead of the job the
-      // stage holds, where the parity wait would pass on the older phase:
-      // first wait until the job has been issued.
-      if (issued2_wait(issued2 + stage, j2)) ok = false;
-      ok &= mbar_wait(&full2c[stage], par, nullptr);
-      ok &= mbar_wait(&full2h[stage], par, nullptr);
-      const uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
-      const uint32_t* qm = reinterpret_cast<const uint32_t*>(st) + g8 * 8 + 2 * q4;
-      const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + L.st2_sb) + g8;
-      const uint16_t* hp = reinterpret_cast<const uint16_t*>(st + L.st2_h) + static_cast<size_t>(g8) * L.Imax + 16 * q4;
-      const float* hsp = reinterpret_cast<const float*>(st + L.st2_h + static_cast<size_t>(kT) * L.Imax * 2);
-      const float* hsa = hsp + (2 * q4) * L.hs_stride;
-      const float* hsb = hsa + L.hs_stride;
-      float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the slot's rows before its routing weight
-      for (int g = gr; g < g_stop; ++g) {
-        uint32_t b[8];
-        load_b(hp + g * 64, g8 < kT, b);
-        const uint2 wa = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8);
-        const uint2 wb = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8 + 64);
-        float dd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_group<false>(wa, wb, b, dd);
-        const uint32_t p0 = sbm[g * kRows2], p1 = sbm[g * kRows2 + 8];
-        const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 1024.0f * s0;
-        const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 1024.0f * s1;
-        const float ha = 2 * q4 < kT ? hsa[2 * g] + hsa[2 * g + 1] : 0.0f;
-        const float hb = 2 * q4 + 1 < kT ? hsb[2 * g] + hsb[2 * g + 1] : 0.0f;
-        sa[0] += fmaf(s0, dd[0], c0 * ha);
-        sa[1] += fmaf(s0, dd[1], c0 * hb);
-        sa[2] += fmaf(s1, dd[2], c1 * ha);
-        sa[3] += fmaf(s1, dd[3], c1 * hb);
-      }
-      // tokens not routed to the slot contribute nothing (their h is never used)
-      const float ra = 2 * q4 < kT ? wt[slot * kT + 2 * q4] : 0.0f;
-      const float rb2 = 2 * q4 + 1 < kT ? wt[slot * kT + 2 * q4 + 1] : 0.0f;
-      if (ra != 0.0f) {
-        acc2[0] = fmaf(ra, sa[0], acc2[0]);
-        acc2[2] = fmaf(ra, sa[2], acc2[2]);
-      }
-      if (rb2 != 0.0f) {
-        acc2[1] = fmaf(rb2, sa[1], acc2[1]);
-        acc2[3] = fmaf(rb2, sa[3], acc2[3]);
-      }
-      // the last warp done with a stage refills it
-      const int done = g_stop - gr;
-      p += done;
-      __syncwarp();
-      if (lane == 0) {
-        const int old = atomicAdd(&cnt2[stage], done);
-        int need = 0;  // pairs of every job this stage has held, up to this one
-        for (int jj = stage; jj <= j2; jj += L.S2) need += jj % nsl == 0 ? G2first : G2;
-        if (old + done == need && j2 + L.S2 < total2) {
-          *reinterpret_cast<volatile int*>(issued2 + stage) = j2 + L.S2;
-          fence_proxy_async_smem();
-          fence_proxy_async_global();
-          const uint64_t pol = l2_policy_evict_first();
-          issue2c(j2 + L.S2, nsl, pol);
-          issue2h(j2 + L.S2, nsl);
+      cons_sync();
+      // Y = the sum over the 16 warps' partial rows: 8 lanes per output value
+      // add pairs of partials, then a fixed shuffle tree (deterministic)
+      if (threadIdx.x < kRows2 * kT * 8) {
+        const int w8 = threadIdx.x & 7, o = threadIdx.x >> 3;  // output o = r * kT + t
+        float v = red2[w8 * kRows2 * kT + o] + red2[(w8 + 8) * kRows2 * kT + o];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        if (w8 == 0) {
+          const int r = o / kT, t = o % kT;
+          a.Y[static_cast<size_t>(t) * d + rb * kRows2 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         }
       }
+      cons_sync();
     }
-    if (2 * q4 < kT) {
-      red2[(warp * kRows2 + g8) * kT + 2 * q4] = acc2[0];
-      red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4] = acc2[2];
-    }
-    if (2 * q4 + 1 < kT) {
-      red2[(warp * kRows2 + g8) * kT + 2 * q4 + 1] = acc2[1];
-      red2[(warp * kRows2 + g8 + 8) * kT + 2 * q4 + 1] = acc2[3];
-    }
-    __syncthreads();
-    if (threadIdx.x < kRows2 * kT) {
-      const int r = threadIdx.x % kRows2, t = threadIdx.x / kRows2;
-      float v = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += red2[(w * kRows2 + r) * kT + t];  // fixed order: deterministic
-      a.Y[static_cast<size_t>(t) * d + rb * kRows2 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    }
-    __syncthreads();
   }
   if (!ok) record_status(a.status, MOE_ERR_TIMEOUT);
 }
@@ -763,7 +916,7 @@ bool decode_supported(int T, int d, int I, int I_shared, int k) {
   if (T < 1 || T > kGemvMaxT || k > kMaxK || k < 1) return false;
   if (d % 64 || I % 64 || I_shared % 64 || I < 64) return false;
   const int Imax = I > I_shared ? I : I_shared;
-  if (Imax / 64 > 256) return false;  // a down-projection box covers every group of a row block
+  if (Imax / 64 > 256 || d / 64 > 256) return false;  // a parameter box covers every group of a row block
   const Layout L = layout(T, d, I, I_shared);
   return L.S2 >= 2 && L.total <= kSmemMax;
 }

@@ -53,7 +53,7 @@ constexpr int kDecodeRowsDown = 16;    // output rows per block (phase 2)
 // Tensor maps of one expert set for the decode kernel.
 struct DecodeMaps {
   CUtensorMap q_gate, q_up;    // codes [E][d/64][I*8], box (32 rows * 8 words, kDecodeChunkGroups groups, 1)
-  CUtensorMap sb_gate, sb_up;  // group parameters [E][d/64][I], box (32 rows, kDecodeChunkGroups groups, 1)
+  CUtensorMap sb_gate, sb_up;  // group parameters [E][d/64][I], box (32 rows, d/64 groups, 1)
   CUtensorMap q_down;          // codes [E][I/64][d*8], box (16 rows * 8 words, I/64 groups, 1)
   CUtensorMap sb_down;         // group parameters [E][I/64][d], box (16 rows, I/64 groups, 1)
 };

@@ -131,6 +131,12 @@ __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// A load whose value is not used: unlike a prefetch hint it always brings the
+// line into L2 (it bypasses L1).
+__device__ __forceinline__ void touch_l2(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+}
 
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -15,12 +15,75 @@
 
 namespace bm {
 
+// Monotone 32-bit key of a logit: a larger float gives a larger unsigned key;
+// -0.0 becomes +0.0 first, so equal floats always get equal keys.
+__device__ __forceinline__ uint32_t topk_key(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float topk_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Selection for E <= 256: lane l holds experts 8l .. 8l+7 as 64-bit values
+// (key << 32 | ~expert), so a larger value is a larger logit or, for equal
+// logits, a lower expert; it sorts them once (a 19-comparator network), and
+// each of the k rounds takes the largest head key over the lanes (the lowest
+// lane among equal heads holds the lowest expert, lanes holding contiguous
+// experts) and pops that lane's head.
+__device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict__ row, int E, int k, int lane,
+                                                        int& sel_i, float& sel_v, bool& all_finite) {
+  uint64_t v[8];
+  bool finite = true;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int e = 8 * lane + c;
+    float x = 0.0f;
+    if (e < E) x = __ldcg(row + e);
+    finite &= e >= E || isfinite(x);
+    v[c] = e < E ? (static_cast<uint64_t>(topk_key(x)) << 32) | static_cast<uint32_t>(~e) : 0ull;
+  }
+  all_finite = __all_sync(0xffffffffu, finite);
+  constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2}, {5, 6},
+                               {0, 4}, {1, 5}, {2, 6}, {3, 7}, {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const uint64_t a = v[kNet[c][0]], b = v[kNet[c][1]];
+    v[kNet[c][0]] = a > b ? a : b;
+    v[kNet[c][1]] = a > b ? b : a;
+  }
+  uint32_t sel_key = 0;
+  sel_i = 0;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t hk = static_cast<uint32_t>(v[0] >> 32);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk);
+    const unsigned cand = __ballot_sync(0xffffffffu, hk == kmax && v[0] != 0ull);
+    const int win = __ffs(cand) - 1;
+    const uint32_t wlow = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v[0]), win);
+    if (lane == j) {
+      sel_key = kmax;
+      sel_i = static_cast<int>(~wlow);
+    }
+    if (lane == win) {
+#pragma unroll
+      for (int c = 0; c < 7; ++c) v[c] = v[c + 1];
+      v[7] = 0ull;
+    }
+  }
+  sel_v = topk_key_value(sel_key);
+}
+
 // Selection.  row: E <= 32 * kPL fp32 logits.  On return lane j < k holds the
 // j-th selected expert (descending logit) in sel_i and its logit in sel_v;
 // every lane learns whether the row was all finite.
 template <int kPL>
 __device__ __forceinline__ void warp_topk_select(const float* __restrict__ row, int E, int k, int lane, int& sel_i,
                                                  float& sel_v, bool& all_finite) {
+  if constexpr (kPL == 8) {
+    warp_topk_select_sorted(row, E, k, lane, sel_i, sel_v, all_finite);
+    return;
+  }
   // Monotone 32-bit keys: a larger float gives a larger unsigned key.  -0.0
   // becomes +0.0 first, so equal floats always get equal keys.
   uint32_t key[kPL];
