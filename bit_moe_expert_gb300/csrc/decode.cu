@@ -188,6 +188,72 @@ __device__ __forceinline__ bool issued2_wait(const int* slot, int job) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Every routing output, as the routing kernel writes it for one chunk: ids
+// and weights, counts, exclusive offsets, the stable permutation and the tile
+// block map (experts ascending).  Run by the compute warps of one CTA.
+//   cnt: scratch of 3 * E + 2 ints in shared memory (E <= 256)
+__device__ __forceinline__ void write_routing_outputs(const DecodeArgs& a, const int* s_ids, const float* s_w, int* cnt,
+                                                   int na, int warp, int lane) {
+  int* off = cnt + a.E;       // [E + 1]
+  int* boff = off + a.E + 1;  // [E + 1]
+  for (int i = threadIdx.x; i < na; i += kCons) {
+    a.out.ids[i] = s_ids[i];
+    a.out.w[i] = s_w[i];
+  }
+  for (int e = threadIdx.x; e < a.E; e += kCons) cnt[e] = 0;
+  book_sync();
+  for (int i = threadIdx.x; i < na; i += kCons) atomicAdd(&cnt[s_ids[i]], 1);
+  book_sync();
+  if (warp == 0) {
+    int run = 0, brun = 0;
+    for (int e0 = 0; e0 < a.E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < a.E ? cnt[e] : 0;
+      const int b = (c + a.block_rows - 1) / a.block_rows;
+      int ic = c, ib = b;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int c2 = __shfl_up_sync(0xffffffffu, ic, o);
+        const int b2 = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+          ic += c2;
+          ib += b2;
+        }
+      }
+      if (e < a.E) {
+        off[e] = run + ic - c;
+        boff[e] = brun + ib - b;
+      }
+      run += __shfl_sync(0xffffffffu, ic, 31);
+      brun += __shfl_sync(0xffffffffu, ib, 31);
+    }
+    if (lane == 0) {
+      off[a.E] = run;
+      boff[a.E] = brun;
+      *a.out.num_blocks = brun;
+    }
+  }
+  book_sync();
+  for (int e = threadIdx.x; e < a.E; e += kCons) a.out.counts[e] = cnt[e];
+  for (int e = threadIdx.x; e <= a.E; e += kCons) a.out.offsets[e] = off[e];
+  for (int i = threadIdx.x; i < na; i += kCons) {
+    const int e = s_ids[i];
+    int r = 0;
+    for (int j = 0; j < i; ++j) r += s_ids[j] == e;
+    const int pos = off[e] + r;
+    a.out.perm[pos] = i;
+    a.out.inv_perm[i] = pos;
+  }
+  for (int e = threadIdx.x; e < a.E; e += kCons) {
+    const int c = cnt[e];
+    int b = boff[e];
+    for (int r = 0; r < c; r += a.block_rows, ++b) {
+      a.out.block_map[3 * b + 0] = e;
+      a.out.block_map[3 * b + 1] = off[e] + r;
+      a.out.block_map[3 * b + 2] = min(a.block_rows, c - r);
+    }
+  }
+}
+
 template <int kT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps mr, const __grid_constant__ DecodeMaps ms, const DecodeArgs a,
@@ -585,77 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cons_sync();
 
-    // Routing weights (fp64, slow on this GPU) are computed only by the CTA
-    // that writes the routing outputs; the others read them after the barrier.
+    // One CTA writes every routing output (its own copy of the weights, from
+    // the same arithmetic as the producer's).
     if (bookkeeper) {
       if (warp < kT) {
         const float w = warp_topk_weights(sel_v, a.k, lane);
         if (lane < a.k) s_w[warp * a.k + lane] = w;
       }
       book_sync();  // the weights are in s_w
-      // every routing output, as the routing kernel writes it for one chunk:
-      // ids and weights, counts, exclusive offsets, the stable permutation and
-      // the tile block map (experts ascending)
-      int* cnt = reinterpret_cast<int*>(smem + L.bk);  // [E]
-      int* off = cnt + a.E;                             // [E + 1]
-      int* boff = off + a.E + 1;                        // [E + 1]
-      for (int i = threadIdx.x; i < na; i += kCons) {
-        a.out.ids[i] = s_ids[i];
-        a.out.w[i] = s_w[i];
-      }
-      for (int e = threadIdx.x; e < a.E; e += kCons) cnt[e] = 0;
-      book_sync();
-      for (int i = threadIdx.x; i < na; i += kCons) atomicAdd(&cnt[s_ids[i]], 1);
-      book_sync();
-      if (warp == 0) {
-        int run = 0, brun = 0;
-        for (int e0 = 0; e0 < a.E; e0 += 32) {
-          const int e = e0 + lane;
-          const int c = e < a.E ? cnt[e] : 0;
-          const int b = (c + a.block_rows - 1) / a.block_rows;
-          int ic = c, ib = b;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int c2 = __shfl_up_sync(0xffffffffu, ic, o);
-            const int b2 = __shfl_up_sync(0xffffffffu, ib, o);
-            if (lane >= o) {
-              ic += c2;
-              ib += b2;
-            }
-          }
-          if (e < a.E) {
-            off[e] = run + ic - c;
-            boff[e] = brun + ib - b;
-          }
-          run += __shfl_sync(0xffffffffu, ic, 31);
-          brun += __shfl_sync(0xffffffffu, ib, 31);
-        }
-        if (lane == 0) {
-          off[a.E] = run;
-          boff[a.E] = brun;
-          *a.out.num_blocks = brun;
-        }
-      }
-      book_sync();
-      for (int e = threadIdx.x; e < a.E; e += kCons) a.out.counts[e] = cnt[e];
-      for (int e = threadIdx.x; e <= a.E; e += kCons) a.out.offsets[e] = off[e];
-      for (int i = threadIdx.x; i < na; i += kCons) {
-        const int e = s_ids[i];
-        int r = 0;
-        for (int j = 0; j < i; ++j) r += s_ids[j] == e;
-        const int pos = off[e] + r;
-        a.out.perm[pos] = i;
-        a.out.inv_perm[i] = pos;
-      }
-      for (int e = threadIdx.x; e < a.E; e += kCons) {
-        const int c = cnt[e];
-        int b = boff[e];
-        for (int r = 0; r < c; r += a.block_rows, ++b) {
-          a.out.block_map[3 * b + 0] = e;
-          a.out.block_map[3 * b + 1] = off[e] + r;
-          a.out.block_map[3 * b + 2] = min(a.block_rows, c - r);
-        }
-      }
+      write_routing_outputs(a, s_ids, s_w, reinterpret_cast<int*>(smem + L.bk), na, warp, lane);
     }
 
     // ------------------------------------------------------------ phase 1: h of this CTA's items
@@ -759,29 +763,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_begin = 1 + (p_begin - G2first) / G2;
       g_begin = (p_begin - G2first) % G2;
     }
+    // lane-constant offsets: codes of rows g8 and g8 + 8 (words), h of token g8 (halves)
+    const int lq = g8 * 8 + 2 * q4;
+    const size_t lh = static_cast<size_t>(g8) * L.Imax + 16 * q4;
+    const bool refills = total2 > L.S2;
     for (int rl = 0; rl < my_rbs; ++rl) {
       const int rb = cta + rl * nC;
       float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       int slot = s_begin, gr = g_begin;
+      int stage = (rl * nsl + s_begin) % L.S2, use = (rl * nsl + s_begin) / L.S2;  // job rl * nsl + slot
       for (int p = p_begin; p < p_end; ++slot, gr = 0) {
+        const int j2 = rl * nsl + slot;
         const int gx = slot == 0 ? G2first : G2;
         const int g_stop = min(gx, gr + (p_end - p));
-        const int j2 = rl * nsl + slot, stage = j2 % L.S2;
-        const uint32_t par = static_cast<uint32_t>(j2 / L.S2) & 1u;
         // A warp may reach a job two uses of its stage ahead of the job the
         // stage holds, where the parity wait would pass on the older phase:
-        // first wait until the job has been issued.
-        if (issued2_wait(issued2 + stage, j2)) ok = false;
-        ok &= mbar_wait(&full2c[stage], par, nullptr);
+        // with refills, first wait until the job has been issued.
+        if (refills && issued2_wait(issued2 + stage, j2)) ok = false;
+        ok &= mbar_wait(&full2c[stage], static_cast<uint32_t>(use) & 1u, nullptr);
         if (j2 < L.S2) ok &= mbar_wait(bar_h0, 0, nullptr);
-        else ok &= mbar_wait(&full2h[stage], static_cast<uint32_t>(j2 / L.S2 - 1) & 1u, nullptr);
+        else ok &= mbar_wait(&full2h[stage], static_cast<uint32_t>(use - 1) & 1u, nullptr);
         const uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
         const uint8_t* hr = hring + static_cast<size_t>(stage) * L.hrec;
-        const uint32_t* qm = reinterpret_cast<const uint32_t*>(st) + g8 * 8 + 2 * q4;
+        const uint32_t* qm = reinterpret_cast<const uint32_t*>(st) + lq;
         const uint32_t* sbm = reinterpret_cast<const uint32_t*>(st + L.st2_sb) + g8;
-        const uint16_t* hp = reinterpret_cast<const uint16_t*>(hr) + static_cast<size_t>(g8) * L.Imax + 16 * q4;
-        const float* hsp = reinterpret_cast<const float*>(hr + static_cast<size_t>(kT) * L.Imax * 2);
-        const float* hsa = hsp + (2 * q4) * L.hs_stride;
+        const uint16_t* hp = reinterpret_cast<const uint16_t*>(hr) + lh;
+        const float* hsa = reinterpret_cast<const float*>(hr + static_cast<size_t>(kT) * L.Imax * 2) + (2 * q4) * L.hs_stride;
         const float* hsb = hsa + L.hs_stride;
         float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // the slot's rows before its routing weight
         // one group of 64 columns: four MMA steps, then the group's affine map
@@ -797,11 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 1024.0f * s0;
           const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 1024.0f * s1;
           const float ha = 2 * q4 < kT ? hsa[2 * g] + hsa[2 * g + 1] : 0.0f;
-          const float hb = 2 * q4 + 1 < kT ? hsb[2 * g] + hsb[2 * g + 1] : 0.0f;
           sa[0] += fmaf(s0, dd[0], c0 * ha);
-          sa[1] += fmaf(s0, dd[1], c0 * hb);
           sa[2] += fmaf(s1, dd[2], c1 * ha);
-          sa[3] += fmaf(s1, dd[3], c1 * hb);
+          if (kT > 1) {
+            const float hb = 2 * q4 + 1 < kT ? hsb[2 * g] + hsb[2 * g + 1] : 0.0f;
+            sa[1] += fmaf(s0, dd[1], c0 * hb);
+            sa[3] += fmaf(s1, dd[3], c1 * hb);
+          }
         };
         int g = gr;
         for (; g + 1 < g_stop; g += 2) {  // two groups in flight
@@ -819,20 +828,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tokens not routed to the slot contribute nothing (their h is never used)
         if (slot == s_begin) ok &= mbar_wait(bar_w, 0, nullptr);
         const float ra = 2 * q4 < kT ? wt[slot * kT + 2 * q4] : 0.0f;
-        const float rb2 = 2 * q4 + 1 < kT ? wt[slot * kT + 2 * q4 + 1] : 0.0f;
         if (ra != 0.0f) {
           acc2[0] = fmaf(ra, sa[0], acc2[0]);
           acc2[2] = fmaf(ra, sa[2], acc2[2]);
         }
-        if (rb2 != 0.0f) {
-          acc2[1] = fmaf(rb2, sa[1], acc2[1]);
-          acc2[3] = fmaf(rb2, sa[3], acc2[3]);
+        if (kT > 1) {
+          const float rb2 = 2 * q4 + 1 < kT ? wt[slot * kT + 2 * q4 + 1] : 0.0f;
+          if (rb2 != 0.0f) {
+            acc2[1] = fmaf(rb2, sa[1], acc2[1]);
+            acc2[3] = fmaf(rb2, sa[3], acc2[3]);
+          }
         }
         // the last warp done with a stage releases it to the producer (only
         // needed when some job waits for a stage)
         const int done = g_stop - gr;
         p += done;
-        if (total2 > L.S2) {
+        if (refills) {
           __syncwarp();
           if (lane == 0) {
             const int old = atomicAdd(&cnt2[stage], done);
@@ -840,6 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = stage; jj <= j2; jj += L.S2) need += jj % nsl == 0 ? G2first : G2;
             if (old + done == need) mbar_arrive(&empty2[stage]);
           }
+        }
+        if (++stage == L.S2) {
+          stage = 0;
+          ++use;
         }
       }
       if (2 * q4 < kT) {
