@@ -651,17 +651,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cons_sync();
 
-    // One CTA writes every routing output (its own copy of the weights, from
-    // the same arithmetic as the producer's).
-    if (bookkeeper) {
-      if (warp < kT) {
-        const float w = warp_topk_weights(sel_v, a.k, lane);
-        if (lane < a.k) s_w[warp * a.k + lane] = w;
-      }
-      book_sync();  // the weights are in s_w
-      write_routing_outputs(a, s_ids, s_w, reinterpret_cast<int*>(smem + L.bk), na, warp, lane);
-    }
-
     // ------------------------------------------------------------ phase 1: h of this CTA's items
     const int mat = warp >> 3;  // 0: gate, 1: up
     const int gl = warp & 7;    // group inside a stage
@@ -751,6 +740,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_global();
     cons_sync();
     if (threadIdx.x == 0) red_release_gpu_add(&hdr->dec_count[gen & 1u], 1u);
+
+    // One CTA writes every routing output, after it has arrived (no CTA of the
+    // call reads them): its own copy of the weights, from the same arithmetic
+    // as the producer's.
+    if (bookkeeper) {
+      if (warp < kT) {
+        const float w = warp_topk_weights(sel_v, a.k, lane);
+        if (lane < a.k) s_w[warp * a.k + lane] = w;
+      }
+      book_sync();  // the weights are in s_w
+      write_routing_outputs(a, s_ids, s_w, reinterpret_cast<int*>(smem + L.bk), na, warp, lane);
+    }
 
     // ------------------------------------------------------------ phase 2: Y rows of this CTA
     // Warp w takes a contiguous run of the (slot, group) pairs of each row
