@@ -205,8 +205,10 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  *            and returns MOE_ERR_UNSUPPORTED otherwise
  * Preconditions: T >= 0 (T = 0 does nothing), d, I and I_shared multiples of
  * 64 (I_shared = 0 iff shared is NULL), 1 <= k <= min(E, 32), E <= 1024.
- * Path: T <= 4 runs the decode kernel (CUDA-core GEMV, every active expert's
- * bytes streamed once, one launch); larger T runs the grouped tensor-core GEMM
+ * Path: T <= 4 runs the decode kernel (every active expert's bytes streamed
+ * once, one launch; warp-level tensor-core MMAs fed from the 4-bit codes, the
+ * gate/up projections in bf16 with x exact, h rounded to fp16 for the down
+ * projection); larger T runs the grouped tensor-core GEMM
  * (tcgen05, dequantisation fused, SwiGLU and the weighted combine fused).  The
  * environment variable MOE_PATH=gemv|gemm overrides the choice (gemv with
  * T > 4 returns MOE_ERR_UNSUPPORTED; for A/B
@@ -229,7 +231,7 @@ size_t moe_layer_workspace_bytes(int T, int d, int I, int E, int k, int I_shared
  * output.  E = routed->n_experts.  When the decode kernel takes the call
  * (1 <= T <= 4, E <= 256, its shared-memory plan fits, MOE_PATH not "gemm")
  * this is ONE launch: every CTA of the decode kernel selects the tokens'
- * experts itself with the routing kernel's arithmetic, and one extra CTA pair
+ * experts itself with the routing kernel's arithmetic, and one of its CTAs
  * writes the routing outputs.  Otherwise it launches the routing kernel and
  * then the moe_forward kernels.  Device-side errors of both parts go to the
  * status word at the start of ws (read it with moe_check_status(ws, ...)). */
