@@ -36,13 +36,22 @@ __device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict_
                                                         int& sel_i, float& sel_v, bool& all_finite) {
   uint64_t v[8];
   bool finite = true;
+  float xv[8];
+  if (E == 256 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    // two 16-byte loads per lane: the warp reads the row as eight whole lines
+    const float4 lo = __ldcg(reinterpret_cast<const float4*>(row) + 2 * lane);
+    const float4 hi = __ldcg(reinterpret_cast<const float4*>(row) + 2 * lane + 1);
+    xv[0] = lo.x, xv[1] = lo.y, xv[2] = lo.z, xv[3] = lo.w;
+    xv[4] = hi.x, xv[5] = hi.y, xv[6] = hi.z, xv[7] = hi.w;
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) xv[c] = 8 * lane + c < E ? __ldcg(row + 8 * lane + c) : 0.0f;
+  }
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const int e = 8 * lane + c;
-    float x = 0.0f;
-    if (e < E) x = __ldcg(row + e);
-    finite &= e >= E || isfinite(x);
-    v[c] = e < E ? (static_cast<uint64_t>(topk_key(x)) << 32) | static_cast<uint32_t>(~e) : 0ull;
+    finite &= e >= E || isfinite(xv[c]);
+    v[c] = e < E ? (static_cast<uint64_t>(topk_key(xv[c])) << 32) | static_cast<uint32_t>(~e) : 0ull;
   }
   all_finite = __all_sync(0xffffffffu, finite);
   constexpr int kNet[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6}, {5, 7}, {1, 2}, {5, 6},
