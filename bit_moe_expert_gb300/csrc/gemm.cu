@@ -46,9 +46,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kDqWarp0 = 11;       // sixteen dequantisation warps (11..26)
 constexpr int kDqWarps = 16;
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
-constexpr uint32_t kBarDequant = 1;   // named barriers (0 is __syncthreads)
-constexpr uint32_t kBarEpilogue = 2;
+constexpr uint32_t kBarEpilogue = 1;  // named barrier of the epilogue warps (0 is __syncthreads)
 constexpr uint32_t kTmemCols = 512;
+static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns, 16 at a time");
 
 template <bool kGateUp>
 struct Cfg {
@@ -278,8 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a fixed stage-to-issuer map means every issuer waits on every phase of
     // the barriers it uses, so no wait can mistake an old phase for the next.
     const int who = warp - kMmaWarp0;
+    // shared-memory addresses stay below 2^18, so the descriptor's 14-bit
+    // address field never carries into its neighbours
+    const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(stages));
     int stage = 0, astage = 0, accb = 0;
-    uint32_t phase = 0, aphase = 0, accphase = 0;
+    uint32_t aphase = 0, accphase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < s.n_total && ok; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
@@ -296,30 +299,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < m.nk; ++kb) {
         const bool mine = kGateUp || ((stage & 1) == who);
         if (mine) {
-          if (!mbar_wait(&a_full[astage], aphase, abort_flag) || !mbar_wait(&full[stage], phase, abort_flag)) {
+          // a_full completes only after every dequantisation warp has seen
+          // full[stage] complete (the stage's token tile has landed) and
+          // arrived with release semantics, so waiting on a_full alone orders
+          // these MMAs after the tile's TMA writes as well
+          if (!mbar_wait(&a_full[astage], aphase, abort_flag)) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t b_addr = smem_u32(stages + stage * C::kStageBytes);
+          if (elect_one()) {
+            // the four K = 16 slices of the stage: 32 bytes apart in the
+            // swizzled token tile (2 in the descriptor's address field), 8
+            // columns apart in the A stage
+            const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (C::kStageBytes >> 4));
             const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 : 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              tc_mma_ts(d, a0 + kk * 8, smem_desc_sw128_kmajor(b_addr + kk * 32), idesc,
-                        (first && kk == 0) ? 0u : 1u);
-            }
+            tc_mma_ts(d, a0, bd, idesc, first ? 0u : 1u);
+            tc_mma_ts(d, a0 + 8, bd + 2, idesc, 1u);
+            tc_mma_ts(d, a0 + 16, bd + 4, idesc, 1u);
+            tc_mma_ts(d, a0 + 24, bd + 6, idesc, 1u);
             tc_commit(&empty[stage]);
             tc_commit(&a_empty[astage]);
           }
           __syncwarp();
           first = false;
         }
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (++stage == C::kStages) stage = 0;
         if (++astage == C::kAStages) {
           astage = 0;
           aphase ^= 1;
@@ -354,13 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
       for (int kb = 0; kb < m.nk; ++kb) {
-        // one warp polls the barriers; the other fifteen sleep in a named barrier
-        bool bad = false;
-        if (dq == 0) {
-          bad = !mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&a_empty[astage], aphase ^ 1, abort_flag);
-          if (bad && lane == 0) fail();
-        }
-        if (bar_sync_or(kBarDequant, kDqWarps * 32, bad)) {
+        // every warp waits for itself: no warp holds the others back, and the
+        // warps drift apart, so their bursts do not all compete for issue
+        // slots with the MMA issuer at once
+        if (!mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&a_empty[astage], aphase ^ 1, abort_flag)) {
+          if (lane == 0) fail();
           ok = false;
           break;
         }
@@ -444,14 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint16_t* H = (m.shared ? a.h_shared : a.h_routed) + static_cast<size_t>(m.row0) * Icur + n;
         const int c_valid = min(c_end, m.rows);
         bool range_ok = true;
-        for (int c0 = c_begin; c0 < c_end; c0 += 8) {
-          uint32_t g[8], u[8];
-          tmem_ld8(tbase + c0, g);
-          tmem_ld8(tbase + kGemmBN + c0, u);
+        // 16 columns of gate and up per TMEM round trip (the column ranges
+        // are multiples of 16: kGemmBN / 2 and the tile width both are)
+        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tbase + c0, g);
+          tmem_ld16(tbase + kGemmBN + c0, u);
           tc_wait_ld();
           if (n < Icur) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 16; ++c) {
               if (c0 + c < c_valid) {
                 const float gv = __uint_as_float(g[c]);
                 const float h = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
@@ -471,14 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t row_base = (m.shared ? static_cast<size_t>(a.T) * a.k : 0) + m.row0;
         float* Yp = a.ypart + row_base * a.d + n;
         const int c_valid = min(c_end, m.rows);
-        for (int c0 = c_begin; c0 < c_end; c0 += 8) {
-          uint32_t v0[8], v1[8];
-          tmem_ld8(tbase + h0 + c0, v0);
-          tmem_ld8(tbase + kGemmBN + c0, v1);
+        for (int c0 = c_begin; c0 < c_end; c0 += 16) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tbase + h0 + c0, v0);
+          tmem_ld16(tbase + kGemmBN + c0, v1);
           tc_wait_ld();
           if (n < a.d) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < 16; ++c)
               if (c0 + c < c_valid)
                 Yp[static_cast<size_t>(c0 + c) * a.d] = __uint_as_float(v0[c]) + (two ? __uint_as_float(v1[c]) : 0.0f);
           }
@@ -504,46 +510,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The gate/up GEMM's token operand: fp16 rows of X in the routing's permuted
 // order (row p = X[perm[p] / k]), followed by the T rows of X in token order
 // when there is a shared expert.  Values outside the fp16 range are recorded
-// as MOE_ERR_UNSUPPORTED.  16-byte pieces, four in flight per thread.
-__global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, int T, int d,
-                                int k, int rows, uint16_t* __restrict__ Xg, uint32_t* status) {
+// as MOE_ERR_UNSUPPORTED.  One warp per row: every lane's 16-byte pieces of
+// the row are loaded before any is converted.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherU = 8;  // 16-byte pieces per lane in flight (a 2048-wide row in one round)
+__global__ void __launch_bounds__(kGatherThreads)
+    x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* __restrict__ perm, int T, int d, int k, int rows,
+                    uint16_t* __restrict__ Xg, uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
-  constexpr int kU = 4;
   const int A = T * k;
   const int d8 = d / 8;
-  const size_t n = static_cast<size_t>(rows) * d8;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (kGatherThreads / 32);
   bool range_ok = true, idx_ok = true;
-  for (size_t base = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; base < n; base += stride * kU) {
-    uint4 v[kU];
-    bool ok[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const size_t i = base + u * stride;
-      ok[u] = false;
-      if (i < n) {
-        const int r = static_cast<int>(i / d8);
-        const int c = static_cast<int>(i - static_cast<size_t>(r) * d8);
-        const int t = r < A ? __ldg(perm + r) / k : r - A;
-        ok[u] = t >= 0 && t < T;
-        idx_ok &= ok[u];
-        if (ok[u]) v[u] = __ldg(reinterpret_cast<const uint4*>(X) + static_cast<size_t>(t) * d8 + c);
-      }
+  for (int r = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const int t = r < A ? __ldg(perm + r) / k : r - A;
+    if (t < 0 || t >= T) {
+      idx_ok = false;
+      continue;
     }
+    const uint4* src = reinterpret_cast<const uint4*>(X) + static_cast<size_t>(t) * d8;
+    uint4* dst = reinterpret_cast<uint4*>(Xg) + static_cast<size_t>(r) * d8;
+    for (int c0 = lane; c0 < d8; c0 += 32 * kGatherU) {
+      uint4 v[kGatherU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (!ok[u]) continue;
-      const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t out[4];
+      for (int u = 0; u < kGatherU; ++u)
+        if (c0 + 32 * u < d8) v[u] = __ldg(src + c0 + 32 * u);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(in[j] << 16);
-        const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
-        range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
-        out[j] = f32x2_to_f16x2(lo, hi);
+      for (int u = 0; u < kGatherU; ++u) {
+        if (c0 + 32 * u >= d8) continue;
+        const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(in[j] << 16);
+          const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
+          range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
+          out[j] = f32x2_to_f16x2(lo, hi);
+        }
+        dst[c0 + 32 * u] = make_uint4(out[0], out[1], out[2], out[3]);
       }
-      reinterpret_cast<uint4*>(Xg)[base + u * stride] = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
   if (!range_ok) record_status(status, MOE_ERR_UNSUPPORTED);
@@ -551,46 +558,64 @@ __global__ void x_gather_kernel(const uint16_t* __restrict__ X, const int32_t* _
 }
 
 // Y[t] = bf16( sum_j w[t][j] * yexp[inv_perm[t*k + j]] + yexp[A + t] ): the
-// weighted top-k combine plus the shared expert, summed in slot order.
-__global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ inv_perm,
-                               const float* __restrict__ w, int T, int d, int k, int has_shared,
-                               uint16_t* __restrict__ Y, uint32_t* status) {
+// weighted top-k combine plus the shared expert, summed in slot order.  One
+// CTA per token (grid-stride); each thread owns float4 columns and issues the
+// loads of every slot before it sums them in slot order.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineSlots = 8;  // slots whose rows are in flight together
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ inv_perm,
+                   const float* __restrict__ w, int T, int d, int k, int has_shared, uint16_t* __restrict__ Y,
+                   uint32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   const size_t A = static_cast<size_t>(T) * k;
   const int d4 = d / 4;
-  const size_t total4 = static_cast<size_t>(T) * d4;
   bool ok = true;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t t = i / d4;
-    const int n = static_cast<int>(i - t * d4) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int p = __ldg(inv_perm + t * k + j);
-      const float wj = __ldg(w + t * k + j);
-      if (p < 0 || static_cast<size_t>(p) >= A) {
-        ok = false;
-        continue;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int c = threadIdx.x; c < d4; c += kCombineThreads) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < k; j0 += kCombineSlots) {
+        float4 v[kCombineSlots];
+        float wj[kCombineSlots];
+        bool in[kCombineSlots];
+#pragma unroll
+        for (int u = 0; u < kCombineSlots; ++u) {
+          const int j = j0 + u;
+          in[u] = false;
+          if (j < k) {
+            const int p = __ldg(inv_perm + static_cast<size_t>(t) * k + j);
+            wj[u] = __ldg(w + static_cast<size_t>(t) * k + j);
+            if (p < 0 || static_cast<size_t>(p) >= A) {
+              ok = false;
+            } else {
+              in[u] = true;
+              v[u] = *reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d + 4 * c);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kCombineSlots; ++u) {
+          if (!in[u]) continue;
+          acc.x = fmaf(wj[u], v[u].x, acc.x);
+          acc.y = fmaf(wj[u], v[u].y, acc.y);
+          acc.z = fmaf(wj[u], v[u].z, acc.z);
+          acc.w = fmaf(wj[u], v[u].w, acc.w);
+        }
       }
-      const float4 v = *reinterpret_cast<const float4*>(ypart + static_cast<size_t>(p) * d + n);
-      acc.x = fmaf(wj, v.x, acc.x);
-      acc.y = fmaf(wj, v.y, acc.y);
-      acc.z = fmaf(wj, v.z, acc.z);
-      acc.w = fmaf(wj, v.w, acc.w);
+      if (has_shared) {
+        const float4 v = *reinterpret_cast<const float4*>(ypart + (A + t) * d + 4 * c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
+      const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
+                          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
+      *reinterpret_cast<uint2*>(Y + static_cast<size_t>(t) * d + 4 * c) = make_uint2(lo, hi);
     }
-    if (has_shared) {
-      const float4 v = *reinterpret_cast<const float4*>(ypart + (A + t) * d + n);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.x))) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16);
-    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.z))) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(Y + t * d + n) = make_uint2(lo, hi);
   }
   if (!ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
@@ -624,10 +649,11 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
 
   {
     cudaLaunchConfig_t c2 = cfg;
-    c2.gridDim = dim3(a.num_sms * 8);
-    c2.blockDim = dim3(256);
-    c2.dynamicSmemBytes = 0;
     const int rows = a.T * a.k + (a.I_shared > 0 ? a.T : 0);
+    constexpr int kRowsPerCta = kGatherThreads / 32;
+    c2.gridDim = dim3(max(1, min((rows + kRowsPerCta - 1) / kRowsPerCta, a.num_sms * 16)));
+    c2.blockDim = dim3(kGatherThreads);
+    c2.dynamicSmemBytes = 0;
     timer_begin(kKXGather, stream);
     cudaError_t e = cudaLaunchKernelEx(&c2, x_gather_kernel, a.X, a.perm, a.T, a.d, a.k, rows, a.Xh, a.status);
     timer_end(kKXGather, stream);
@@ -650,8 +676,8 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 
-  cfg.gridDim = dim3(a.num_sms * 4);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(max(1, min(a.T, a.num_sms * 8)));
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   timer_begin(kKCombine, stream);
   err = cudaLaunchKernelEx(&cfg, combine_kernel, static_cast<const float*>(a.ypart), a.inv_perm, a.w, a.T, a.d, a.k,

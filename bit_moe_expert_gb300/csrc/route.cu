@@ -4,13 +4,18 @@
 // dequantize in flight": histogram, prefix scan, scatter and block map after
 // every top-8 selection, kept inside one GPU submission).
 //
-// Each CTA routes a chunk of 32 tokens (one warp per token at a time): k rounds
-// of a warp-wide arg-max over the lane-strided logits.  It then writes its
+// Each routing CTA takes a chunk of 32 tokens (one warp per token at a time)
+// and selects their top k.  It then writes its
 // per-expert counts and, for every assignment, the rank among the chunk's
 // assignments to the same expert (computed in assignment order, so the result
 // is stable).  The last CTA to finish (an atomic ticket, no spin wait) reduces
 // the chunk counts into counts/offsets, turns them into per-chunk bases, places
 // every assignment, and writes the block map.
+//
+// The routing weights (a softmax in fp64, which is slow on this GPU) are not on
+// that chain: extra CTAs after the routing CTAs select the top k of 16 tokens
+// each again (the same function, so the same selection) and write only the
+// weights; they wait for nothing, so they run beside the routing CTAs.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,11 +39,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
                                                               WsHeader* hdr, uint32_t* status,
                                                               int32_t* __restrict__ chunk_hist,
                                                               int32_t* __restrict__ local_rank, int bases_in_smem,
-                                                              int gridsync) {
+                                                              int gridsync, int nroute) {
   extern __shared__ int32_t s_bases[];  // [nchunks][E] exclusive per-chunk bases (last CTA, when they fit)
   __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
-  __shared__ float s_v[kRouteTokensPerCta * kMaxK];    // selected logits
-  __shared__ double s_ex[kRouteTokensPerCta * kMaxK];  // exp(l_j - l_max)
   __shared__ int32_t s_rank[kRouteTokensPerCta * kMaxK];
   __shared__ int32_t s_cnt[kMaxE];
   __shared__ int32_t s_off[kMaxE + 1];
@@ -53,47 +56,66 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
-  const int nchunks = gridDim.x;
+  const int nchunks = nroute;
   const int t0 = chunk * kRouteTokensPerCta;
   const int ntok = max(0, min(kRouteTokensPerCta, T - t0));
   const int A = T * k;
 
+  if (chunk >= nroute) {
+    // ---- a weight CTA: one token per warp; the softmax over the selected
+    // logits in fp64, summed in selection order, rounded once
+    const int t = (chunk - nroute) * kRouteWarps + warp;
+    if (t < T) {
+      int sel_i;
+      float sel_v;
+      bool finite;
+      warp_topk_select<kPL>(logits + static_cast<size_t>(t) * E, E, k, lane, sel_i, sel_v, finite);
+      const float wj = warp_topk_weights(sel_v, k, lane);
+      if (lane < k) out.w[static_cast<size_t>(t) * k + lane] = wj;
+    }
+    return;
+  }
+
   for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
 
-  // ---- top-k, one warp per token: k rounds of a warp-wide arg-max
-  for (int tl = warp; tl < ntok; tl += kRouteWarps) {
-    const int t = t0 + tl;
-    const float* row = logits + static_cast<size_t>(t) * E;
-    int sel_i;
-    float sel_v;
-    bool finite;
-    warp_topk_select<kPL>(row, E, k, lane, sel_i, sel_v, finite);
+  // ---- top-k, one warp per token
+  auto publish = [&](int tl, int sel_i, bool finite) {
     if (!finite && lane == 0) record_status(status, MOE_ERR_NONFINITE);
     if (lane < k) {
-      out.ids[static_cast<size_t>(t) * k + lane] = sel_i;
+      out.ids[static_cast<size_t>(t0 + tl) * k + lane] = sel_i;
       s_ids[tl * k + lane] = sel_i;
-      s_v[tl * k + lane] = sel_v;
+    }
+  };
+  if constexpr (kPL == 8) {
+    // both of a warp's rows are in flight before either is selected
+    static_assert(kRouteTokensPerCta == 2 * kRouteWarps, "two tokens per warp");
+    float xv[2][8];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int tl = warp + u * kRouteWarps;
+      if (tl < ntok) topk_load_row8(logits + static_cast<size_t>(t0 + tl) * E, E, lane, xv[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int tl = warp + u * kRouteWarps;
+      if (tl < ntok) {
+        int sel_i;
+        float sel_v;
+        bool finite;
+        warp_topk_select_sorted_vals(xv[u], E, k, lane, sel_i, sel_v, finite);
+        publish(tl, sel_i, finite);
+      }
+    }
+  } else {
+    for (int tl = warp; tl < ntok; tl += kRouteWarps) {
+      int sel_i;
+      float sel_v;
+      bool finite;
+      warp_topk_select<kPL>(logits + static_cast<size_t>(t0 + tl) * E, E, k, lane, sel_i, sel_v, finite);
+      publish(tl, sel_i, finite);
     }
   }
   __syncthreads();
-  // ---- weights: softmax over each token's selected logits in fp64 (summed in
-  // selection order, rounded once).  One assignment per thread, so every lane
-  // of a warp works (fp64 is slow on this GPU; a warp per token would leave
-  // most lanes idle).
-  {
-    const int na_ = ntok * k;
-    for (int a = threadIdx.x; a < na_; a += kRouteThreads) {
-      const int tl = a / k;
-      s_ex[a] = exp(static_cast<double>(s_v[a]) - static_cast<double>(s_v[tl * k]));
-    }
-    __syncthreads();
-    for (int a = threadIdx.x; a < na_; a += kRouteThreads) {
-      const int tl = a / k;
-      double sum = 0.0;
-      for (int j = 0; j < k; ++j) sum += s_ex[tl * k + j];
-      out.w[static_cast<size_t>(t0) * k + a] = static_cast<float>(s_ex[a] / sum);
-    }
-  }
 
   // ---- stable per-chunk ranks: one warp walks the chunk's assignments in order
   const int na = ntok * k;
@@ -136,13 +158,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kRouteThreads) {
       int run = 0, mine = 0;
-      for (int c0 = 0; c0 < nchunks; c0 += 8) {
-        int h[8];
+      for (int c0 = 0; c0 < nchunks; c0 += 32) {  // 32 loads in flight per round trip
+        int h[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 32; ++i)
           h[i] = (c0 + i < nchunks) ? __ldcg(chunk_hist + static_cast<size_t>(c0 + i) * E + e) : 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 32; ++i) {
           if (c0 + i == chunk) mine = run;
           run += h[i];
         }
@@ -159,7 +181,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     __syncthreads();
     if (threadIdx.x == 0) {
       const unsigned ticket = atomicAdd(&hdr->ticket, 1u);
-      s_is_last = (ticket == gridDim.x - 1) ? 1 : 0;
+      s_is_last = (ticket == static_cast<unsigned>(nchunks - 1)) ? 1 : 0;
     }
     __syncthreads();
     if (!s_is_last) return;
@@ -348,8 +370,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   // Grid-synchronised mode when every chunk's CTA can be resident at once
   // (leaving room for other work); otherwise the last CTA finishes alone.
   const int gridsync = (nchunks > 1 && nchunks <= resident[E <= 256 ? 0 : 1] / 2) ? 1 : 0;
+  const int nweight = (T + kRouteWarps - 1) / kRouteWarps;  // weight CTAs, one token per warp
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nchunks);
+  cfg.gridDim = dim3(nchunks + nweight);
   cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = (bases_in_smem && !gridsync) ? bases_bytes : 0;
   cfg.stream = stream;
@@ -361,9 +384,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   timer_begin(kKRoute, stream);
   const cudaError_t err =
       E <= 256 ? cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, T, E, k, block_rows, out, hdr, status,
-                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync)
+                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync, nchunks)
                : cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, T, E, k, block_rows, out, hdr, status,
-                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync);
+                                    chunk_hist, local_rank, bases_in_smem && !gridsync, gridsync, nchunks);
   timer_end(kKRoute, stream);
   return err;
 }

@@ -26,17 +26,8 @@ __device__ __forceinline__ float topk_key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Selection for E <= 256: lane l holds experts 8l .. 8l+7 as 64-bit values
-// (key << 32 | ~expert), so a larger value is a larger logit or, for equal
-// logits, a lower expert; it sorts them once (a 19-comparator network), and
-// each of the k rounds takes the largest head key over the lanes (the lowest
-// lane among equal heads holds the lowest expert, lanes holding contiguous
-// experts) and pops that lane's head.
-__device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict__ row, int E, int k, int lane,
-                                                        int& sel_i, float& sel_v, bool& all_finite) {
-  uint64_t v[8];
-  bool finite = true;
-  float xv[8];
+// Lane l's eight logits 8l .. 8l+7 of a row of E <= 256 (zero past E).
+__device__ __forceinline__ void topk_load_row8(const float* __restrict__ row, int E, int lane, float (&xv)[8]) {
   if (E == 256 && (reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
     // two 16-byte loads per lane: the warp reads the row as eight whole lines
     const float4 lo = __ldcg(reinterpret_cast<const float4*>(row) + 2 * lane);
@@ -47,6 +38,18 @@ __device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict_
 #pragma unroll
     for (int c = 0; c < 8; ++c) xv[c] = 8 * lane + c < E ? __ldcg(row + 8 * lane + c) : 0.0f;
   }
+}
+
+// Selection for E <= 256 from the lanes' loaded logits: lane l holds experts
+// 8l .. 8l+7 as 64-bit values (key << 32 | ~expert), so a larger value is a
+// larger logit or, for equal logits, a lower expert; it sorts them once (a
+// 19-comparator network), and each of the k rounds takes the largest head key
+// over the lanes (the lowest lane among equal heads holds the lowest expert,
+// lanes holding contiguous experts) and pops that lane's head.
+__device__ __forceinline__ void warp_topk_select_sorted_vals(const float (&xv)[8], int E, int k, int lane,
+                                                             int& sel_i, float& sel_v, bool& all_finite) {
+  uint64_t v[8];
+  bool finite = true;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const int e = 8 * lane + c;
@@ -81,6 +84,13 @@ __device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict_
     }
   }
   sel_v = topk_key_value(sel_key);
+}
+
+__device__ __forceinline__ void warp_topk_select_sorted(const float* __restrict__ row, int E, int k, int lane,
+                                                        int& sel_i, float& sel_v, bool& all_finite) {
+  float xv[8];
+  topk_load_row8(row, E, lane, xv);
+  warp_topk_select_sorted_vals(xv, E, k, lane, sel_i, sel_v, all_finite);
 }
 
 // Selection.  row: E <= 32 * kPL fp32 logits.  On return lane j < k holds the
