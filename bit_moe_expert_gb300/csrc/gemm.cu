@@ -19,12 +19,14 @@
 // only the packed codes, the group parameters and the token tile (TMA gather4
 // of the expert's token rows).  Accumulators live in tensor memory.
 //
-// Roles (14 warps, one persistent CTA per SM):
-//   warps 0-7   dequantise codes -> fp16 A tiles in TMEM
-//   warps 8-11  epilogue: TMEM -> registers -> SwiGLU (gate/up) or weighted
-//               scatter of expert outputs (down)
-//   warp 12     TMA producer (codes, group parameters, token rows)
-//   warp 13     MMA issuer (one lane)
+// Roles (one persistent CTA per SM):
+//   warp 0       TMA producer (codes, group parameters, token rows)
+//   warps 1-2    MMA issuers (gate and up matrices; in the down GEMM, the
+//                k-blocks of one parity each), one elected lane each
+//   warps 3-10   epilogue: TMEM -> registers -> SwiGLU (gate/up) or the
+//                expert-output rows (down)
+//   warps 11-    dequantise codes -> fp16 A tiles in TMEM: four warps per
+//                matrix (gate/up: 8, down: 4), one per quarter of the rows
 // Synchronisation is by mbarriers; every wait is bounded (2 s) and records
 // MOE_ERR_TIMEOUT instead of hanging.
 #include <cuda_bf16.h>
@@ -38,14 +40,12 @@ namespace bm {
 
 namespace {
 
-// Warp roles (27 warps).
+// Warp roles.
 constexpr int kProducerWarp = 0;   // TMA of codes and group parameters; cp.async gather of the token tile
 constexpr int kMmaWarp0 = 1;       // two MMA issuers (warps 1 and 2)
 constexpr int kEpiWarp0 = 3;       // eight epilogue warps (3..10)
 constexpr int kEpiWarps = 8;
-constexpr int kDqWarp0 = 11;       // sixteen dequantisation warps (11..26)
-constexpr int kDqWarps = 16;
-constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr int kDqWarp0 = 11;       // dequantisation warps from 11: four per matrix, one per TMEM lane quarter
 constexpr uint32_t kBarEpilogue = 1;  // named barrier of the epilogue warps (0 is __syncthreads)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns, 16 at a time");
@@ -53,6 +53,8 @@ static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns,
 template <bool kGateUp>
 struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
+  static constexpr int kDqWarps = 4 * kMats;
+  static constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
   static constexpr int kStages = kGateUp ? 6 : 8;
   static constexpr int kAStages = kGateUp ? 2 : 4;
   static constexpr int kACols = 32 * kMats;  // 64 fp16 per lane per matrix = 32 columns
@@ -136,7 +138,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b
 }
 
 template <bool kGateUp>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kGateUp>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap q0_r, const __grid_constant__ CUtensorMap q1_r,
                     const __grid_constant__ CUtensorMap sb0_r, const __grid_constant__ CUtensorMap sb1_r,
                     const __grid_constant__ CUtensorMap q0_s, const __grid_constant__ CUtensorMap q1_s,
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[i], C::kEmptyArrivals);
     }
     for (int i = 0; i < C::kAStages; ++i) {
-      mbar_init(&a_full[i], kDqWarps);
+      mbar_init(&a_full[i], C::kDqWarps);
       mbar_init(&a_empty[i], C::kAEmptyArrivals);
     }
     for (int i = 0; i < 2; ++i) {
@@ -347,11 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kDqWarp0) {
     // ------------------------------------------------------------ dequantisation
-    const int dq = warp - kDqWarp0;
     const int lanegrp = warp & 3;
     const int row = lanegrp * 32 + lane;  // weight row inside the tile = TMEM lane
-    const int part = dq >> 2;             // gate/up: (matrix, 32-column half); down: 16-column quarter
-    const int mat = kGateUp ? (part >> 1) : 0;
+    const int mat = (warp - kDqWarp0) >> 2;
     const int swz = (row >> 2) & 1;
     int stage = 0, astage = 0;
     uint32_t phase = 0, aphase = 0;
@@ -370,31 +370,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint8_t* st = stages + stage * C::kStageBytes;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols;
+        // the warp's 32 rows of its matrix, all 64 columns: the row's 32 code
+        // bytes are two 16-byte halves, swapped in rows where the 32-byte
+        // swizzle flips bit 4 of the address; half h holds words 4h .. 4h+3 =
+        // columns 32h .. 32h+31
         const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes;
-        const uint32_t sbv =
-            *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes + mat * C::kSBBytes + row * 4);
+        const uint32_t sbv = *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes +
+                                                                mat * C::kSBBytes + row * 4);
         const float sf = __uint_as_float(sbv << 16);  // bf16 -> fp32 is exact
         const float bf = __uint_as_float(sbv & 0xFFFF0000u);
         const uint32_t s2 = f32x2_to_f16x2(sf, sf);
         const uint32_t b2 = f32x2_to_f16x2(bf, bf);
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols;
-        if constexpr (kGateUp) {
-          const int half = part & 1;  // words 4*half .. 4*half+3 = columns 32*half .. 32*half+31
-          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((half ^ swz) << 4));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
           uint32_t v[16];
           dequant_word(w.x, s2, b2, v + 0);
           dequant_word(w.y, s2, b2, v + 4);
           dequant_word(w.z, s2, b2, v + 8);
           dequant_word(w.w, s2, b2, v + 12);
-          tmem_st16(taddr + mat * 32 + half * 16, v);
-        } else {
-          const int quarter = part;  // words 2q, 2q+1 = columns 16q .. 16q+15
-          const uint2 w = *reinterpret_cast<const uint2*>(q_tile + row * 32 + (((quarter >> 1) ^ swz) << 4) +
-                                                          ((quarter & 1) << 3));
-          uint32_t v[8];
-          dequant_word(w.x, s2, b2, v + 0);
-          dequant_word(w.y, s2, b2, v + 4);
-          tmem_st8(taddr + quarter * 8, v);
+          tmem_st16(taddr + mat * 32 + h * 16, v);
         }
         tc_wait_st();
         tc_fence_before();
@@ -645,7 +641,6 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(a.num_sms);
-  cfg.blockDim = dim3(kThreads);
 
   {
     cudaLaunchConfig_t c2 = cfg;
@@ -661,6 +656,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   }
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CG::kSmemBytes;
+  cfg.blockDim = dim3(CG::kThreads);
   timer_begin(kKGemmGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
                                        routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
@@ -669,6 +665,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.dynamicSmemBytes = CD::kSmemBytes;
+  cfg.blockDim = dim3(CD::kThreads);
   timer_begin(kKGemmDown, stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false>, routed->q_down, routed->q_down, routed->sb_down,
                            routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
