@@ -514,7 +514,8 @@ def run_workload(wl, args, dist, peaks, clocks):
     shares = {k: {"launches": v[1], "avg_us": (v[0] / max(v[1], 1)) * 1e3,
                   "share": (v[0] / total_k if total_k else 0.0)} for k, v in kt.items() if v[1]}
     roof = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": None, "algorithmic_work_per_launch": work_desc,
+            "frac": achieved / peak, "traffic": profiled_traffic(kname), "traffic_unit": "B per launch",
+            "algorithmic_work_per_launch": work_desc,
             "avg_launch_us": avg_s * 1e6, "avg_launch_method": avg_method, "peak_source": peaks["source"] + (
                 " copy bandwidth" if bound == "hbm" else " cuBLAS bf16 GEMM (burst); fp16 MMA has the same rate")}
     out = {"value": value, "ms_per_step": ms / args.steps, "e2e": e2e, "roofline": roof, "kernels": shares,
@@ -532,6 +533,30 @@ def run_workload(wl, args, dist, peaks, clocks):
                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": fl / peaks["bf16_tflops"],
                                 "note": "whole step (routing, conversion, both GEMMs, combine), algorithmic FLOPs"}
     return out
+
+
+# DRAM bytes (read + write) per launch of each dominant kernel, from the ncu
+# captures summarised under profiles/, with a hash of the sources the kernel is
+# built from at the time of the capture.  A kernel whose sources changed since
+# reports null.
+_CSRC = os.path.join(ROOT, "bit_moe_expert_gb300", "csrc")
+PROFILED_TRAFFIC = {
+    # profiles/prefill4096_chunk_kernels.md: 87.341824 MB read + 2.673152 MB written
+    "gemm_gateup": (90_014_976, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "dc6374b7ee8294ac"),
+}
+
+
+def profiled_traffic(kname):
+    ent = PROFILED_TRAFFIC.get(kname)
+    if ent is None:
+        return None
+    nbytes, files, sha = ent
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return float(nbytes) if h.hexdigest()[:16] == sha else None
 
 
 def cpu_baseline(wl, budget_s):
