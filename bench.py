@@ -262,7 +262,7 @@ class DecodeWorkload(Workload):
         cfg = self.cfg
         return self.L * (cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared))
 
-    def dominant(self):
+    def dominant(self, peaks):
         cfg = self.cfg
         per_launch = cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared)
         return "decode", "hbm", per_launch, (
@@ -383,12 +383,30 @@ class PrefillWorkload(Workload):
         shared = 6 * cfg.d * cfg.I_shared
         return cfg.T * (cfg.k * per_tok_expert + shared)
 
-    def dominant(self):
+    def active_experts(self):
+        """Experts that chunk 0 routes to (every chunk of a workload has the same statistics)."""
+        cfg, C = self.cfg, self.chunk
+        self.bm.moe_route(self.logits[0][0:C], cfg.k, self.block_rows, self.r, self.ws_r)
+        return int((self.r.counts.cpu().numpy() > 0).sum())
+
+    def dominant(self, peaks):
+        """The gate/up GEMM, against the tensor-core peak when its arithmetic intensity (FLOPs per streamed
+        weight byte) is above the ridge point of the measured peaks, else against HBM on the weight bytes."""
         cfg = self.cfg
-        per_launch = self.chunk * (cfg.k * 4 * cfg.d * cfg.I + 4 * cfg.d * cfg.I_shared)
-        return "gemm_gateup", "tensor", per_launch, (
-            f"{self.chunk} tokens x ({cfg.k} routed + shared) x 2 matrices x 2*{cfg.d}*{cfg.I} FLOP "
-            f"= {per_launch / 1e9:.2f} GFLOP per launch")
+        flops = self.chunk * (cfg.k * 4 * cfg.d * cfg.I + 4 * cfg.d * cfg.I_shared)
+        n_act = self.active_experts()
+        # gate and up are two of the three equally sized matrices of an expert
+        nbytes = (2 * n_act * synth.ffn_bytes(cfg.d, cfg.I) + 2 * synth.ffn_bytes(cfg.d, cfg.I_shared)) // 3
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if flops / nbytes > ridge:
+            return "gemm_gateup", "tensor", flops, (
+                f"{self.chunk} tokens x ({cfg.k} routed + shared) x 2 matrices x 2*{cfg.d}*{cfg.I} FLOP "
+                f"= {flops / 1e9:.2f} GFLOP per launch ({flops / nbytes:.0f} FLOP per weight byte, "
+                f"ridge {ridge:.0f})")
+        return "gemm_gateup", "hbm", nbytes, (
+            f"gate and up matrices of the {n_act} active experts{' + shared' if cfg.I_shared else ''} "
+            f"(4-bit codes, bf16 scale/bias) = {nbytes} B per launch ({flops / nbytes:.0f} FLOP per weight byte, "
+            f"ridge {ridge:.0f})")
 
     def workload_desc(self):
         c = self.cfg
@@ -493,7 +511,7 @@ def run_workload(wl, args, dist, peaks, clocks):
            "note": f"public API per call ({wl.api_desc}), inputs copied from pinned host memory and Y "
                    "copied back every step, no CUDA graph"}
     kt = time_kernels(wl, min(args.steps, 200))
-    kname, bound, work, work_desc = wl.dominant()
+    kname, bound, work, work_desc = wl.dominant(peaks)
     kms, kn = kt[kname]
     avg_s = (kms / max(kn, 1)) / 1e3
     avg_method = "separate pass with events around every launch (no overlap between kernels)"
@@ -514,7 +532,7 @@ def run_workload(wl, args, dist, peaks, clocks):
     shares = {k: {"launches": v[1], "avg_us": (v[0] / max(v[1], 1)) * 1e3,
                   "share": (v[0] / total_k if total_k else 0.0)} for k, v in kt.items() if v[1]}
     roof = {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": profiled_traffic(kname), "traffic_unit": "B per launch",
+            "frac": achieved / peak, "traffic": profiled_traffic(wl.name, kname), "traffic_unit": "B per launch",
             "algorithmic_work_per_launch": work_desc,
             "avg_launch_us": avg_s * 1e6, "avg_launch_method": avg_method, "peak_source": peaks["source"] + (
                 " copy bandwidth" if bound == "hbm" else " cuBLAS bf16 GEMM (burst); fp16 MMA has the same rate")}
@@ -528,10 +546,21 @@ def run_workload(wl, args, dist, peaks, clocks):
                                  "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                                  "note": "whole layer (moe_layer: routing and both projections in one launch) inside the 40-layer graph"}
     else:
-        fl = wl.flops_per_step() / ((ms / args.steps) / 1e3) / 1e12
+        t_step = (ms / args.steps) / 1e3
+        fl = wl.flops_per_step() / t_step / 1e12
         out["step_roofline"] = {"bound": "tensor", "flops_per_step": wl.flops_per_step(), "achieved": fl,
                                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": fl / peaks["bf16_tflops"],
                                 "note": "whole step (routing, conversion, both GEMMs, combine), algorithmic FLOPs"}
+        if bound == "hbm":
+            cfg = wl.cfg
+            n_act = wl.active_experts()
+            wbytes = wl.nchunks * (n_act * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared))
+            gbs = wbytes / t_step / 1e9
+            out["step_roofline"] = {"bound": "hbm", "weight_bytes_per_step": wbytes, "achieved": gbs,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                    "flops_per_step": wl.flops_per_step(), "tflops": fl,
+                                    "note": f"whole step; the {n_act} active experts' three matrices"
+                                            f"{' and the shared expert' if cfg.I_shared else ''} streamed once per chunk"}
     return out
 
 
@@ -542,12 +571,14 @@ def run_workload(wl, args, dist, peaks, clocks):
 _CSRC = os.path.join(ROOT, "bit_moe_expert_gb300", "csrc")
 PROFILED_TRAFFIC = {
     # profiles/prefill4096_chunk_kernels.md: 87.341824 MB read + 2.673152 MB written
-    "gemm_gateup": (90_014_976, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "dc6374b7ee8294ac"),
+    "prefill4096/gemm_gateup": (90_014_976, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "dc6374b7ee8294ac"),
+    # profiles/decode_kernel_decode.md: median of five launches, 16,030,720 B read, 0 written
+    "decode/decode": (16_030_720, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "1a1a99f37a5a765d"),
 }
 
 
-def profiled_traffic(kname):
-    ent = PROFILED_TRAFFIC.get(kname)
+def profiled_traffic(workload, kname):
+    ent = PROFILED_TRAFFIC.get(f"{workload}/{kname}")
     if ent is None:
         return None
     nbytes, files, sha = ent
