@@ -123,6 +123,13 @@ def draw_x(cfg: LayerConfig, T: int, layer: int) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal(size=(T, cfg.d)).astype(np.float32))
 
 
+def draw_router(cfg: LayerConfig, layer: int) -> np.ndarray:
+    """Router weights Wr [E][d] as bf16 bit patterns, N(0, 1/d): with X ~ N(0, 1) the logits are about N(0, 1),
+    the scale of the logits drawn directly for the other workloads."""
+    rng = _rng(cfg.seed, layer, 3)
+    return f32_to_bf16_bits((rng.standard_normal(size=(cfg.E, cfg.d)) / np.sqrt(cfg.d)).astype(np.float32))
+
+
 def draw_experts(cfg: LayerConfig, layer: int, E: Optional[int] = None, I: Optional[int] = None,
                  tag: int = 10) -> dict:
     E = cfg.E if E is None else E

@@ -36,6 +36,8 @@ def lib():
         L.oracle_dequant.argtypes = [C.POINTER(QMat), C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]
         L.oracle_dequant_matrix.restype = None
         L.oracle_dequant_matrix.argtypes = [C.POINTER(QMat), C.c_int, C.c_int, C.c_int, C.c_void_p]
+        L.oracle_router_logits.restype = None
+        L.oracle_router_logits.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p]
         L.oracle_topk.restype = C.c_int
         L.oracle_topk.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.oracle_route_layout.restype = C.c_int
@@ -98,6 +100,19 @@ def dequant_matrix(qsb, e: int) -> np.ndarray:
     _, N, K8 = qsb[0].shape
     out = np.empty((N, K8 * 8), dtype=np.float64)
     lib().oracle_dequant_matrix(C.byref(m), N, K8 * 8, e, _ptr(out))
+    return out
+
+
+def router_logits(X: np.ndarray, Wr: np.ndarray) -> np.ndarray:
+    """fp64 logits [T][E] of bf16 X [T][d] (uint16 bit patterns) and bf16 Wr [E][d]."""
+    X = _c(X, np.uint16)
+    Wr = _c(Wr, np.uint16)
+    T, d = X.shape
+    E, d2 = Wr.shape
+    if d != d2:
+        raise ValueError("X and Wr disagree on d")
+    out = np.empty((T, E), np.float64)
+    lib().oracle_router_logits(_ptr(X), T, d, _ptr(Wr), E, _ptr(out))
     return out
 
 

@@ -64,6 +64,19 @@ typedef struct {
 } kv;
 
 /* Descending value; among equal values the lower index first. */
+/* [Lily-blog] "Why Qwen3.6-35B-A3B is a weird workload": the router scores
+ * every expert for a token.  The score is the dot product of the token's
+ * hidden state with the expert's router row, summed in index order. */
+void oracle_router_logits(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, double* logits) {
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += oracle_bf16_to_double(X[(size_t)t * d + i]) * oracle_bf16_to_double(Wr[(size_t)e * d + i]);
+      logits[(size_t)t * E + e] = acc;
+    }
+}
+
 static int kv_cmp(const void* pa, const void* pb) {
   const kv* a = (const kv*)pa;
   const kv* b = (const kv*)pb;

@@ -50,6 +50,13 @@ double oracle_dequant(const oracle_qmat* m, int N, int K, int e, int n, int k);
 /* Dequantise a whole [N][K] matrix of expert e into out (row-major). */
 void oracle_dequant_matrix(const oracle_qmat* m, int N, int K, int e, double* out);
 
+/* Router projection: logits[t][e] = sum_i X[t][i] * Wr[e][i] in fp64 over the
+ * exact bf16 values.  X uint16 [T][d], Wr uint16 [E][d] (bf16 bit patterns),
+ * logits double [T][E].  [Lily-blog] "Why Qwen3.6-35B-A3B is a weird
+ * workload": a router scores the 256 experts of each token; read here as a
+ * linear map of the token's hidden state. */
+void oracle_router_logits(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, double* logits);
+
 /* Router top-k and renormalised weights.  Returns 0, or -1 on a non-finite logit
  * or bad sizes.  ids/w are [T][k], ids in selection order (descending logit,
  * lower expert index first among equal logits). */

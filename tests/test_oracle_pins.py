@@ -134,6 +134,63 @@ def _check_topk_properties(logits, ids, k):
             assert np.all(tied > max(s for s in sel if logits[t, s] == worst))
 
 
+# ---------------------------------------------------------------- router projection
+
+def test_router_logits_one_hot_tokens_pick_router_columns(oracle):
+    # a token that is the i-th unit vector scores expert e with Wr[e][i] exactly
+    rng = np.random.default_rng(21)
+    d, E = 64, 16
+    Wr = synth.f32_to_bf16_bits(rng.standard_normal((E, d)).astype(np.float32))
+    cols = [0, 5, 63, 17]
+    X = np.zeros((len(cols), d), np.uint16)
+    for t, i in enumerate(cols):
+        X[t, i] = 0x3F80  # 1.0
+    lg = oracle.router_logits(X, Wr)
+    want = synth.bf16_bits_to_f32(Wr).astype(np.float64)[:, cols].T
+    assert np.array_equal(lg, want)
+
+
+def test_router_logits_exact_rational_brute_force(oracle):
+    # small integers and halves: every product and partial sum is exact in fp64,
+    # so the oracle must equal the exact rational dot products
+    from fractions import Fraction
+    rng = np.random.default_rng(22)
+    T, d, E = 3, 32, 8
+    xv = rng.integers(-8, 9, size=(T, d)) / 2.0
+    wv = rng.integers(-16, 17, size=(E, d)) / 4.0
+    X = synth.f32_to_bf16_bits(xv.astype(np.float32))
+    Wr = synth.f32_to_bf16_bits(wv.astype(np.float32))
+    lg = oracle.router_logits(X, Wr)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(xv[t, i])) * Fraction(float(wv[e, i])) for i in range(d))
+            assert Fraction(lg[t, e]) == exact, (t, e)
+
+
+def test_router_logits_linear_and_transposed_roles(oracle):
+    # scaling a token by 2 (exact in bf16) doubles its logits; swapping the roles of the
+    # token block and the router (both d-wide) transposes the result
+    rng = np.random.default_rng(23)
+    d = 128
+    A = synth.f32_to_bf16_bits(rng.standard_normal((6, d)).astype(np.float32))
+    B = synth.f32_to_bf16_bits(rng.standard_normal((6, d)).astype(np.float32))
+    lg = oracle.router_logits(A, B)
+    A2 = synth.f32_to_bf16_bits(2.0 * synth.bf16_bits_to_f32(A))
+    assert np.array_equal(oracle.router_logits(A2, B), 2.0 * lg)
+    assert np.allclose(oracle.router_logits(B, A), lg.T, rtol=0, atol=1e-12)
+
+
+def test_router_logits_scale_of_synthetic_router(oracle):
+    # the synthetic router (N(0, 1/d) rows) gives logits of about unit variance on
+    # N(0, 1) tokens, the scale of the logits the other workloads draw directly
+    cfg = synth.CONFIGS["decode"]
+    X = synth.draw_x(cfg, 16, 0)
+    Wr = synth.draw_router(cfg, 0)
+    lg = oracle.router_logits(X, Wr)
+    assert lg.shape == (16, cfg.E)
+    assert 0.8 < lg.std() < 1.25
+
+
 def test_topk_properties_random(oracle):
     rng = np.random.default_rng(3)
     for (T, E, k) in [(40, 16, 2), (25, 256, 8), (9, 128, 8), (7, 33, 5), (3, 5, 5)]:
