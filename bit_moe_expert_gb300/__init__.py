@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
+            "moe_router_logits", "moe_route_x",
             "moe_forward_workspace_bytes",
             "moe_forward", "moe_layer_workspace_bytes", "moe_layer", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
             "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
@@ -75,6 +76,11 @@ def lib(path: Optional[str] = None):
         L.moe_route.restype = C.c_int
         L.moe_route.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                 C.c_void_p, C.c_size_t, C.c_void_p]
+        L.moe_router_logits.restype = C.c_int
+        L.moe_router_logits.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
+        L.moe_route_x.restype = C.c_int
+        L.moe_route_x.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                  C.POINTER(_Routing), C.c_void_p, C.c_size_t, C.c_void_p]
         L.moe_route_noalloc.restype = C.c_int
         L.moe_route_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                         C.c_void_p]
@@ -227,6 +233,23 @@ def moe_route(logits, k: int, block_rows: int, out: Routing, ws, stream=None) ->
     r = out._c()
     _check("moe_route", lib().moe_route(_ptr(logits), T, E, k, block_rows, C.byref(r), _ptr(ws), ws.numel(),
                                         _stream(stream)))
+    out.block_rows = r.block_rows
+
+
+def moe_router_logits(X, W_r, logits, stream=None) -> None:
+    """logits [T][E] fp32 = X [T][d] bf16 (int16 storage) times W_r [E][d] bf16, transposed."""
+    T, d = X.shape
+    E = W_r.shape[0]
+    _check("moe_router_logits", lib().moe_router_logits(_ptr(X), T, d, _ptr(W_r), E, _ptr(logits), _stream(stream)))
+
+
+def moe_route_x(X, W_r, k: int, block_rows: int, out: Routing, ws, logits, stream=None) -> None:
+    """moe_router_logits into `logits`, then moe_route on them."""
+    T, d = X.shape
+    E = W_r.shape[0]
+    r = out._c()
+    _check("moe_route_x", lib().moe_route_x(_ptr(X), T, d, _ptr(W_r), E, k, block_rows, _ptr(logits), C.byref(r),
+                                            _ptr(ws), ws.numel(), _stream(stream)))
     out.block_rows = r.block_rows
 
 

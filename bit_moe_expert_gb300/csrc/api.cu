@@ -218,6 +218,35 @@ moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, m
   return MOE_OK;
 }
 
+moe_status moe_router_logits(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, float* logits,
+                             moe_stream stream) {
+  if (T < 0 || d < 64 || d % 64 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!X || !W_r || !logits)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W_r)) & 15u)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * E > (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;
+  const bool pdl = env_flag("MOE_PDL", true);
+  if (launch_router(X, T, d, W_r, E, logits, reinterpret_cast<cudaStream_t>(stream), pdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_route_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, int k, int block_rows,
+                       float* logits, moe_routing* out, void* ws, size_t ws_bytes, moe_stream stream) {
+  // every argument moe_route checks, before anything is launched
+  if (!out || T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (!out->counts || !out->offsets || !out->block_map || !out->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!out->ids || !out->w || !out->perm || !out->inv_perm)) return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < moe_route_workspace_bytes(T, E, k))
+    return MOE_ERR_WORKSPACE;
+  const moe_status st = moe_router_logits(X, T, d, W_r, E, logits, stream);
+  if (st != MOE_OK) return st;
+  return moe_route(logits, T, E, k, block_rows, out, ws, ws_bytes, stream);
+}
+
 size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shared) {
   if (T < 0 || d < 1 || I < 1 || E < 1 || k < 1 || I_shared < 0) return 0;
   return fwd_layout(T, d, I, k, I_shared).total;

@@ -15,7 +15,7 @@ namespace bm {
 enum KernelKind {
   kKRoute = 0,
   kKDecode,    // the fused decode kernel (gate/up + down)
-  kKReserved,  // unused
+  kKRouter,    // the router projection
   kKXGather,
   kKGemmGateUp,
   kKGemmDown,
@@ -44,6 +44,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
 cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream);
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream);
+
+// Router projection: logits [T][E] fp32 = X [T][d] bf16 times Wr [E][d] bf16
+// transposed (d a multiple of 32).
+cudaError_t launch_router(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, float* logits,
+                          cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- decode GEMV
 constexpr int kDecodeRowsGU = 32;      // gate/up rows per item (phase 1)

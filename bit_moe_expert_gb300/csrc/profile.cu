@@ -10,7 +10,7 @@
 namespace bm {
 namespace {
 
-const char* const kNames[kKernelKinds] = {"route", "decode", "unused", "x_gather",
+const char* const kNames[kKernelKinds] = {"route", "decode", "router", "x_gather",
                                           "gemm_gateup", "gemm_down", "combine", "prepack"};
 
 struct Pending {

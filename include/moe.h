@@ -220,6 +220,28 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
                        const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y,
                        void* ws, size_t ws_bytes, moe_stream stream);
 
+/* ------------------------------------------------------------------ router projection
+ * logits[t][e] = sum_i X[t][i] * W_r[e][i]: the router's score of expert e for
+ * token t ("Perplexity's Lily Beats MLX-LM on MacBook M5", section "Why
+ * Qwen3.6-35B-A3B is a weird workload": a router scores the 256 experts and
+ * picks 8; the score is read as a linear map of the token's hidden state).
+ *   X       bf16 [T][d] row-major (device)
+ *   W_r     bf16 [E][d] row-major, one row per expert (device, caller-owned)
+ *   logits  fp32 [T][E] row-major (device, caller-owned), written
+ * Preconditions: T >= 0 (T = 0 does nothing), d a multiple of 64,
+ * 1 <= E <= 1024, X and W_r 16-byte aligned.  Arithmetic: bf16 products
+ * accumulated in fp32 on the tensor cores; the additions are not in index
+ * order, so the logits agree with an exact sum to within fp32 accumulation
+ * error, not bit for bit.  Asynchronous on `stream`; allocates nothing. */
+moe_status moe_router_logits(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, float* logits,
+                             moe_stream stream);
+
+/* moe_router_logits, then moe_route on the logits it wrote (two launches on
+ * `stream`, the second started by the first on the device).  Same arguments,
+ * results and errors as the two calls; `logits` receives the scores. */
+moe_status moe_route_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, int k, int block_rows,
+                       float* logits, moe_routing* out, void* ws, size_t ws_bytes, moe_stream stream);
+
 /* ------------------------------------------------------------------ whole layer
  * Workspace bytes moe_layer needs (the forward workspace followed by a routing
  * workspace); same rules: zero-filled once, 256-byte aligned, one in-flight
