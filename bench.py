@@ -590,6 +590,55 @@ def profiled_traffic(workload, kname):
     return float(nbytes) if h.hexdigest()[:16] == sha else None
 
 
+def router_measure(dev, peaks):
+    """The router projection (moe_router_logits) at one decode token and at one 1024-token prefill chunk:
+    200 calls on 200 distinct 1 MB routers (beyond L2) in a CUDA graph, timed with events."""
+    import torch
+    import bit_moe_expert_gb300 as bm
+    cfg = synth.CONFIGS["decode"]
+    nw = 200
+    W = torch.empty((nw, cfg.E, cfg.d), dtype=torch.int16, device=dev)
+    for i in range(0, nw, 50):  # seeded synthetic routers, N(0, 1/d)
+        W[i] = torch.from_numpy(synth.draw_router(cfg, i).view(np.int16)).to(dev)
+    for i in range(nw):
+        if i % 50:
+            W[i] = W[i - i % 50]
+    out = {}
+    s = torch.cuda.Stream(device=dev)
+    for T in (1, 1024):
+        X = torch.from_numpy(synth.draw_x(cfg, T, 0).view(np.int16)).to(dev)
+        lg = torch.empty((T, cfg.E), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(s):
+            for i in range(3):
+                bm.moe_router_logits(X, W[i], lg)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(nw):
+                    bm.moe_router_logits(X, W[i], lg)
+            g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) / nw * 1e3
+        nbytes = cfg.E * cfg.d * 2 + T * cfg.d * 2 + T * cfg.E * 4
+        flops = 2 * T * cfg.E * cfg.d
+        ent = {"us_per_call": us, "bytes": nbytes, "gbs": nbytes / us / 1e3, "tflops": flops / us / 1e6}
+        if T == 1:
+            ent.update(bound="hbm", frac=ent["gbs"] / peaks["hbm_gbs"], peak=peaks["hbm_gbs"], unit="GB/s")
+        else:
+            ent.update(bound="tensor", frac=ent["tflops"] / peaks["bf16_tflops"], peak=peaks["bf16_tflops"],
+                       unit="TFLOP/s")
+        out[f"T{T}"] = ent
+    out["note"] = (f"logits = X W_r^T, d={cfg.d}, E={cfg.E}, bf16 in, fp32 out; 200 calls on distinct routers "
+                   "in one CUDA graph")
+    del W
+    return out
+
+
 def cpu_baseline(wl, budget_s):
     tokens, secs, desc = wl.cpu_sample(budget_s)
     return {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
@@ -737,6 +786,7 @@ def main():
         secondary = r2
         del wl2
         torch.cuda.empty_cache()
+    router = router_measure(dev, peaks) if (args.workload == "decode" and not args.no_secondary) else None
 
     if dist.rank == 0:
         line = {
@@ -755,6 +805,8 @@ def main():
                 line[key] = main_res[key]
         if secondary is not None:
             line["prefill4096"] = secondary
+        if router is not None:
+            line["router_projection"] = router
         print(json.dumps(line), flush=True)
     dist.close()
 

@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
-            "moe_router_logits", "moe_route_x",
+            "moe_router_logits", "moe_route_x", "moe_layer_x",
             "moe_forward_workspace_bytes",
             "moe_forward", "moe_layer_workspace_bytes", "moe_layer", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
             "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
@@ -96,6 +96,10 @@ def lib(path: Optional[str] = None):
         L.moe_layer.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                 C.POINTER(_Experts), C.POINTER(_Experts), C.c_int, C.POINTER(_Routing), C.c_void_p,
                                 C.c_void_p, C.c_size_t, C.c_void_p]
+        L.moe_layer_x.restype = C.c_int
+        L.moe_layer_x.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                  C.POINTER(_Experts), C.POINTER(_Experts), C.c_int, C.c_void_p, C.POINTER(_Routing),
+                                  C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
         L.moe_check_status.restype = C.c_int
         L.moe_check_status.argtypes = [C.c_void_p, C.c_void_p]
         L.moe_profile_enable.restype = C.c_int
@@ -295,6 +299,20 @@ def moe_layer(logits, X, routed: Experts, shared: Optional[Experts], k: int, blo
     _check("moe_layer", lib().moe_layer(_ptr(logits), _ptr(X), T, d, routed.I, k, block_rows, C.byref(re),
                                         C.byref(se) if se is not None else None, I_sh, C.byref(r), _ptr(Y),
                                         _ptr(ws), ws.numel(), _stream(stream)))
+    out.block_rows = r.block_rows
+
+
+def moe_layer_x(X, W_r, routed: Experts, shared: Optional[Experts], k: int, block_rows: int, logits, out: Routing,
+                Y, ws, stream=None) -> None:
+    """moe_router_logits into `logits`, then moe_layer on them: the layer from the hidden state."""
+    T, d = X.shape
+    re = routed._c()
+    se = shared._c() if shared is not None else None
+    I_sh = shared.I if shared is not None else 0
+    r = out._c()
+    _check("moe_layer_x", lib().moe_layer_x(_ptr(X), T, d, _ptr(W_r), routed.I, k, block_rows, C.byref(re),
+                                            C.byref(se) if se is not None else None, I_sh, _ptr(logits), C.byref(r),
+                                            _ptr(Y), _ptr(ws), ws.numel(), _stream(stream)))
     out.block_rows = r.block_rows
 
 

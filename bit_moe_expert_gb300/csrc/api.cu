@@ -432,6 +432,25 @@ moe_status moe_layer(const float* logits, const uint16_t* X, int T, int d, int I
   return forward_impl(X, T, d, I, k, routed, shared, I_shared, r, Y, ws, fbytes, stream, nullptr);
 }
 
+moe_status moe_layer_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int I, int k, int block_rows,
+                       const moe_experts* routed, const moe_experts* shared, int I_shared, float* logits,
+                       moe_routing* r, uint16_t* Y, void* ws, size_t ws_bytes, moe_stream stream) {
+  // moe_layer's argument checks, before anything is launched
+  if (!r || !experts_ok(routed) || T < 0 || k < 1 || d < 64 || d % 64) return MOE_ERR_INVALID_ARG;
+  const int E = routed->n_experts;
+  if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (block_rows < 1 || block_rows > kMaxBlockRows) return MOE_ERR_UNSUPPORTED;
+  if (!r->counts || !r->offsets || !r->block_map || !r->num_blocks) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !r->ids || !r->w || !r->perm || !r->inv_perm)) return MOE_ERR_INVALID_ARG;
+  const size_t fbytes = moe_forward_workspace_bytes(T, d, I, E, k, I_shared);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || fbytes == 0 ||
+      ws_bytes < moe_layer_workspace_bytes(T, d, I, E, k, I_shared))
+    return MOE_ERR_WORKSPACE;
+  const moe_status st = moe_router_logits(X, T, d, W_r, E, logits, stream);
+  if (st != MOE_OK) return st;
+  return moe_layer(logits, X, T, d, I, k, block_rows, routed, shared, I_shared, r, Y, ws, ws_bytes, stream);
+}
+
 moe_status moe_check_status(void* ws, moe_stream stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -261,6 +261,15 @@ moe_status moe_layer(const float* logits, const uint16_t* X, int T, int d, int I
                      const moe_experts* routed, const moe_experts* shared, int I_shared, moe_routing* r,
                      uint16_t* Y, void* ws, size_t ws_bytes, moe_stream stream);
 
+/* The whole layer from the hidden state: moe_router_logits(X, W_r) into
+ * `logits` (fp32 [T][E], caller-owned), then moe_layer on those logits (two
+ * launches on `stream`, or more when moe_layer takes more).  E =
+ * routed->n_experts; W_r is bf16 [E][d]; every other argument, result and
+ * error as for moe_router_logits and moe_layer. */
+moe_status moe_layer_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int I, int k, int block_rows,
+                       const moe_experts* routed, const moe_experts* shared, int I_shared, float* logits,
+                       moe_routing* r, uint16_t* Y, void* ws, size_t ws_bytes, moe_stream stream);
+
 /* Synchronises `stream`, returns the status recorded in the workspace of a
  * previous moe_route, moe_forward or moe_layer call (MOE_OK if none) and clears it.  For
  * tests and debugging; never needed on the hot path. */

@@ -141,3 +141,35 @@ def test_router_zero_tokens_and_bad_arguments():
     with pytest.raises(bm.MoeError) as ei:
         bm.moe_router_logits(X2, W2, torch.zeros((1, 1025), dtype=torch.float32, device="cuda"))
     assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"  # E above 1024
+
+
+@pytest.mark.parametrize("name,kw,br", [
+    ("T1_fused", dict(T=1, d=1024, E=64, k=8, I=256, I_shared=192), 32),
+    ("T4_fused", dict(T=4, d=512, E=40, k=6, I=128, I_shared=64), 8),
+    ("T40_gemm", dict(T=40, d=256, E=16, k=2, I=128, I_shared=128), 32),
+], ids=["T1_fused", "T4_fused", "T40_gemm"])
+def test_layer_x_from_hidden_state(name, kw, br):
+    """moe_layer_x: the logits within the accumulation bound, the routing of those
+    logits bit for bit, and Y within the layer tolerance of the oracle's layer on
+    that routing."""
+    cfg = synth.small_config(**kw)
+    layer = synth.draw_layer(cfg)
+    Wr = synth.f32_to_bf16_bits(
+        (np.random.default_rng(zlib.crc32(name.encode())).standard_normal((cfg.E, cfg.d)) /
+         np.sqrt(cfg.d)).astype(np.float32))
+    dl = G.DeviceLayer.from_host(layer)
+    Wd = torch.from_numpy(Wr.view(np.int16)).cuda()
+    T = cfg.T
+    lg = torch.empty((T, cfg.E), dtype=torch.float32, device="cuda")
+    r = bm.Routing.empty(T, cfg.E, cfg.k, br)
+    ws = bm.workspace(bm.moe_layer_workspace_bytes(T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared))
+    Y = torch.empty((T, cfg.d), dtype=torch.int16, device="cuda")
+    bm.moe_layer_x(dl.X, Wd, dl.routed, dl.shared, cfg.k, br, lg, r, Y, ws)
+    torch.cuda.synchronize()
+    assert bm.moe_check_status(ws) == 0
+    got_lg = lg.cpu().numpy()
+    _assert_logits_close(got_lg, layer.X, Wr)
+    ref = oracle.route(got_lg, cfg.k, br)
+    G.assert_routing_equal(G.routing_to_host(r), ref)
+    Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, ref["ids"], ref["w"])
+    G.assert_y_close(Y.cpu().numpy().view(np.uint16), Y64, name)
