@@ -639,6 +639,94 @@ def router_measure(dev, peaks):
     return out
 
 
+def uniform_logits(T, E, k):
+    """Logits that route token t to experts (k t + j) mod E, j = 0..k-1, in that order: over T = M E / k tokens
+    every expert receives exactly M rows."""
+    lg = np.full((T, E), -10.0, np.float32)
+    for t in range(T):
+        for j in range(k):
+            lg[t, (k * t + j) % E] = 10.0 - j
+    return lg
+
+
+def run_sweep(dev, peaks, args):
+    """Rows per expert (M) against the weight-streaming rate, at fixed weights (the decode layer's experts,
+    every expert active); then the canvas layer at B canvases of 256 tokens per call.  Each point is a CUDA
+    graph of `steps` calls rotating over 4 weight sets (1.8 GB, beyond L2), timed with events."""
+    import torch
+    import bit_moe_expert_gb300 as bm
+
+    def point(cfg, T, logits_np, sets, steps):
+        C = T
+        r = bm.Routing.empty(C, cfg.E, cfg.k, 96, dev)
+        ws_r = bm.workspace(bm.moe_route_workspace_bytes(C, cfg.E, cfg.k), dev)
+        ws_f = bm.workspace(bm.moe_forward_workspace_bytes(C, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
+        X = torch.from_numpy(synth.draw_x(cfg, C, 0).view(np.int16)).to(dev)
+        lg = torch.from_numpy(logits_np).to(dev)
+        Y = torch.empty((C, cfg.d), dtype=torch.int16, device=dev)
+
+        def call(i):
+            bm.moe_route(lg, cfg.k, 96, r, ws_r)
+            bm.moe_forward(X, sets[i % len(sets)][0], sets[i % len(sets)][1], r, Y, ws_f)
+
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            for i in range(3):
+                call(i)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(steps):
+                    call(i)
+            g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            e1.synchronize()
+        assert bm.moe_check_status(ws_f) == 0 and bm.moe_check_status(ws_r) == 0
+        t_call = e0.elapsed_time(e1) / steps / 1e3
+        counts = r.counts.cpu().numpy()
+        n_act = int((counts > 0).sum())
+        wbytes = n_act * synth.ffn_bytes(cfg.d, cfg.I) + (synth.ffn_bytes(cfg.d, cfg.I_shared) if cfg.I_shared else 0)
+        flops = 6 * T * cfg.d * (cfg.k * cfg.I + cfg.I_shared)
+        return {"T": T, "active_experts": n_act, "rows_per_expert_max": int(counts.max()),
+                "us_per_call": t_call * 1e6, "weight_bytes": wbytes, "gbs": wbytes / t_call / 1e9,
+                "hbm_frac": wbytes / t_call / 1e9 / peaks["hbm_gbs"], "tok_s": T / t_call,
+                "tflops": flops / t_call / 1e12}
+
+    steps = max(4, min(args.steps, 40))
+    cfg = synth.CONFIGS["decode"]
+    sets = [_dev_layer(cfg, l, dev)[2:] for l in range(4)]
+    sweep = []
+    for M in (1, 2, 4, 8, 16, 32, 64, 128):
+        T = M * cfg.E // cfg.k
+        pt = point(cfg, T, uniform_logits(T, cfg.E, cfg.k), sets, steps)
+        pt["M"] = M
+        sweep.append(pt)
+    del sets
+    torch.cuda.empty_cache()
+    ccfg = synth.CONFIGS["canvas"]
+    csets = [_dev_layer(ccfg, l, dev)[2:] for l in range(4)]
+    batching = []
+    for B in (1, 2, 4):
+        T = 256 * B
+        lg = np.concatenate([synth.draw_logits(ccfg, 256, b) for b in range(B)])
+        pt = point(ccfg, T, lg, csets, steps)
+        pt["B"] = B
+        batching.append(pt)
+    return {"metric": "4-bit expert weight-streaming rate against rows per expert; canvas tokens/s against canvases "
+                      "per call", "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "config": {"workload": f"sweep: decode layer dims (d={cfg.d}, E={cfg.E}, k={cfg.k}, I={cfg.I}, "
+                                   f"shared {cfg.I_shared}), T = M E / k tokens routed so that every expert gets "
+                                   f"exactly M rows, moe_route + moe_forward per call; canvas layer "
+                                   f"(d={ccfg.d}, E={ccfg.E}, I={ccfg.I}) at B x 256 tokens",
+                       "l2": "4 weight sets per point, rotated (beyond L2)"},
+            "data": "synthetic (seeded)", "sweep": sweep, "canvas_batching": batching,
+            "peak_hbm_gbs": peaks["hbm_gbs"], "clocks": None}
+
+
 def cpu_baseline(wl, budget_s):
     tokens, secs, desc = wl.cpu_sample(budget_s)
     return {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
@@ -726,7 +814,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS) + ["sweep"],
+                    help="sweep: rows-per-expert and canvas-batching measurements (one JSON line)")
     ap.add_argument("--no-secondary", action="store_true", help="skip the T=4096 prefill object")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--layers", type=int, default=0,
@@ -753,6 +842,14 @@ def main():
     peaks = measured_peaks()
     clocks = ClockSampler(dist.local_rank)
 
+    if args.workload == "sweep":
+        clocks.start()
+        res = run_sweep(dev, peaks, args)
+        res["clocks"] = clocks.stop()
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        dist.close()
+        return
     if args.workload == "decode":
         wl = DecodeWorkload(dev, layers=args.layers or None)
     else:
