@@ -38,6 +38,8 @@ def lib():
         L.oracle_dequant_matrix.argtypes = [C.POINTER(QMat), C.c_int, C.c_int, C.c_int, C.c_void_p]
         L.oracle_router_logits.restype = None
         L.oracle_router_logits.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p]
+        L.oracle_topk_wide.restype = C.c_int
+        L.oracle_topk_wide.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.oracle_topk.restype = C.c_int
         L.oracle_topk.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.oracle_route_layout.restype = C.c_int
@@ -114,6 +116,18 @@ def router_logits(X: np.ndarray, Wr: np.ndarray) -> np.ndarray:
     out = np.empty((T, E), np.float64)
     lib().oracle_router_logits(_ptr(X), T, d, _ptr(Wr), E, _ptr(out))
     return out
+
+
+def topk_wide(logits: np.ndarray, K: int):
+    """values [T][K] fp32 and indices [T][K] int32 of each row's K largest entries (descending, lower index
+    first among equal values)."""
+    lg = _c(logits, np.float32)
+    T, V = lg.shape
+    vals = np.empty((T, K), np.float32)
+    idx = np.empty((T, K), np.int32)
+    if lib().oracle_topk_wide(_ptr(lg), T, V, K, _ptr(vals), _ptr(idx)) != 0:
+        raise ValueError("oracle_topk_wide rejected its input")
+    return vals, idx
 
 
 def topk(logits: np.ndarray, k: int):

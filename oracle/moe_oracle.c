@@ -77,6 +77,46 @@ void oracle_router_logits(const uint16_t* X, int T, int d, const uint16_t* Wr, i
     }
 }
 
+typedef struct {
+  float v;
+  int32_t i;
+} wide_entry;
+
+/* Descending value, then ascending index; -0.0 and +0.0 compare equal. */
+static int wide_cmp(const void* pa, const void* pb) {
+  const wide_entry* a = (const wide_entry*)pa;
+  const wide_entry* b = (const wide_entry*)pb;
+  if (a->v > b->v) return -1;
+  if (a->v < b->v) return 1;
+  return (a->i > b->i) - (a->i < b->i);
+}
+
+/* [DGemma] "The optimizations that worked", item 1: the K best candidates of a
+ * position's logits.  Written as the plain definition: sort the whole row. */
+int oracle_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices) {
+  if (T < 0 || K < 1 || V < K) return -1;
+  wide_entry* row = (wide_entry*)malloc((size_t)V * sizeof(wide_entry));
+  if (!row) return -1;
+  for (int t = 0; t < T; ++t) {
+    for (int i = 0; i < V; ++i) {
+      const float v = logits[(size_t)t * V + i];
+      if (isnan(v)) {
+        free(row);
+        return -1;
+      }
+      row[i].v = v;
+      row[i].i = i;
+    }
+    qsort(row, (size_t)V, sizeof(wide_entry), wide_cmp);
+    for (int j = 0; j < K; ++j) {
+      values[(size_t)t * K + j] = row[j].v;
+      indices[(size_t)t * K + j] = row[j].i;
+    }
+  }
+  free(row);
+  return 0;
+}
+
 static int kv_cmp(const void* pa, const void* pb) {
   const kv* a = (const kv*)pa;
   const kv* b = (const kv*)pb;

@@ -57,6 +57,14 @@ void oracle_dequant_matrix(const oracle_qmat* m, int N, int K, int e, double* ou
  * linear map of the token's hidden state. */
 void oracle_router_logits(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, double* logits);
 
+/* Exact top-K of each row of a wide score matrix: values [T][K] and indices
+ * [T][K] of the K largest entries of logits [T][V], in descending order, a lower
+ * index first among equal values (-0.0 equals +0.0).  [DGemma] "The
+ * optimizations that worked", item 1: the sampler needs only the top ~64 of
+ * 262,144 logits per position.  The plain definition: a full sort of each row.
+ * Returns 0, or -1 on a NaN or bad sizes (1 <= K <= V). */
+int oracle_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices);
+
 /* Router top-k and renormalised weights.  Returns 0, or -1 on a non-finite logit
  * or bad sizes.  ids/w are [T][k], ids in selection order (descending logit,
  * lower expert index first among equal logits). */

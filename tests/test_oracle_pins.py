@@ -191,6 +191,76 @@ def test_router_logits_scale_of_synthetic_router(oracle):
     assert 0.8 < lg.std() < 1.25
 
 
+# ---------------------------------------------------------------- wide top-K (the sampler's candidates)
+
+def _stable_desc(row):
+    # library stable sort on the negated values (-0.0 made +0.0 first): equal values keep index order
+    r = np.where(row == 0.0, np.float32(0.0), row)
+    return np.argsort(-r.astype(np.float64), kind="stable")
+
+
+def test_topk_wide_matches_library_stable_sort(oracle):
+    rng = np.random.default_rng(31)
+    for (T, V, K) in [(3, 1000, 5), (2, 4096, 64), (1, 300, 300), (4, 257, 1)]:
+        lg = rng.standard_normal((T, V)).astype(np.float32)
+        vals, idx = oracle.topk_wide(lg, K)
+        for t in range(T):
+            want = _stable_desc(lg[t])[:K]
+            assert np.array_equal(idx[t], want)
+            assert np.array_equal(vals[t], lg[t][want])
+
+
+def test_topk_wide_ties_and_signed_zero(oracle):
+    lg = np.array([[1.0, 3.0, 3.0, -0.0, 0.0, 3.0, 2.0, 0.0]], np.float32)
+    vals, idx = oracle.topk_wide(lg, 6)
+    assert idx[0].tolist() == [1, 2, 5, 6, 0, 3]
+    lg2 = np.zeros((1, 50), np.float32)
+    _, idx2 = oracle.topk_wide(lg2, 7)
+    assert idx2[0].tolist() == list(range(7))
+
+
+def test_topk_wide_closed_form_ramp(oracle):
+    V, K = 262144, 64
+    lg = np.arange(V, dtype=np.float32)[None, :]  # exact in fp32 below 2^24
+    vals, idx = oracle.topk_wide(lg, K)
+    assert idx[0].tolist() == list(range(V - 1, V - 1 - K, -1))
+    assert np.array_equal(vals[0], lg[0][idx[0]])
+
+
+def _chunked_topk(row, K, chunk):
+    """The two-stage selection: chunk maxima, the K chunks with the largest maxima, then the top K of their
+    entries; the order is by (value, lower index), so every comparison is strict."""
+    V = row.size
+    keys = [(float(0.0 if v == 0 else v), -i) for i, v in enumerate(row)]
+    nch = -(-V // chunk)
+    cmax = [max(keys[c * chunk:(c + 1) * chunk]) for c in range(nch)]
+    best = sorted(range(nch), key=lambda c: cmax[c], reverse=True)[:K]
+    cand = [k for c in best for k in keys[c * chunk:(c + 1) * chunk]]
+    return [-i for _, i in sorted(cand, reverse=True)[:K]]
+
+
+def test_topk_wide_two_stage_selection_is_exact(oracle):
+    # the pages' argument: a top-K entry has fewer than K chunk maxima above it, so
+    # its chunk is among the K best chunks; checked on random rows, heavy ties and
+    # clustered maxima (all large values in one chunk)
+    rng = np.random.default_rng(32)
+    rows = [rng.standard_normal(2048).astype(np.float32),
+            rng.integers(-3, 4, size=2048).astype(np.float32),
+            np.concatenate([rng.standard_normal(256) + 10, rng.standard_normal(1792)]).astype(np.float32),
+            np.zeros(1000, np.float32)]
+    for row in rows:
+        for K in (1, 8, 64):
+            _, idx = oracle.topk_wide(row[None, :], K)
+            assert _chunked_topk(row, K, 64) == idx[0].tolist()
+
+
+def test_topk_wide_rejects_nan(oracle):
+    lg = np.zeros((1, 10), np.float32)
+    lg[0, 3] = np.nan
+    with pytest.raises(ValueError):
+        oracle.topk_wide(lg, 2)
+
+
 def test_topk_properties_random(oracle):
     rng = np.random.default_rng(3)
     for (T, E, k) in [(40, 16, 2), (25, 256, 8), (9, 128, 8), (7, 33, 5), (3, 5, 5)]:
