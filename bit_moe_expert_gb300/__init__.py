@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
-            "moe_router_logits", "moe_route_x", "moe_layer_x",
+            "moe_router_logits", "moe_route_x", "moe_layer_x", "moe_topk_wide",
             "moe_forward_workspace_bytes",
             "moe_forward", "moe_layer_workspace_bytes", "moe_layer", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
             "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
@@ -81,6 +81,8 @@ def lib(path: Optional[str] = None):
         L.moe_route_x.restype = C.c_int
         L.moe_route_x.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                   C.POINTER(_Routing), C.c_void_p, C.c_size_t, C.c_void_p]
+        L.moe_topk_wide.restype = C.c_int
+        L.moe_topk_wide.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p]
         L.moe_route_noalloc.restype = C.c_int
         L.moe_route_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                         C.c_void_p]
@@ -255,6 +257,12 @@ def moe_route_x(X, W_r, k: int, block_rows: int, out: Routing, ws, logits, strea
     _check("moe_route_x", lib().moe_route_x(_ptr(X), T, d, _ptr(W_r), E, k, block_rows, _ptr(logits), C.byref(r),
                                             _ptr(ws), ws.numel(), _stream(stream)))
     out.block_rows = r.block_rows
+
+
+def moe_topk_wide(logits, K: int, values, indices, stream=None) -> None:
+    """values [T][K] fp32 and indices [T][K] int32: each row's K largest entries of logits [T][V]."""
+    T, V = logits.shape
+    _check("moe_topk_wide", lib().moe_topk_wide(_ptr(logits), T, V, K, _ptr(values), _ptr(indices), _stream(stream)))
 
 
 def moe_route_noalloc(logits, k: int, block_rows: int, out: Routing, stream=None) -> None:

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libbitmoe.so")
-SOURCES = ["api.cu", "route.cu", "router.cu", "decode.cu", "gemm.cu", "profile.cu"]
+SOURCES = ["api.cu", "route.cu", "router.cu", "topk_wide.cu", "decode.cu", "gemm.cu", "profile.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

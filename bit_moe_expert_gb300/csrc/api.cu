@@ -247,6 +247,21 @@ moe_status moe_route_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int
   return moe_route(logits, T, E, k, block_rows, out, ws, ws_bytes, stream);
 }
 
+moe_status moe_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices,
+                         moe_stream stream) {
+  if (T < 0 || K < 1 || V < K) return MOE_ERR_INVALID_ARG;
+  if (K > 64 || V > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!logits || !values || !indices)) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) & 3u) return MOE_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const bool pdl = env_flag("MOE_PDL", true);
+  if (launch_topk_wide(logits, T, V, K, values, indices, sms, reinterpret_cast<cudaStream_t>(stream), pdl) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shared) {
   if (T < 0 || d < 1 || I < 1 || E < 1 || k < 1 || I_shared < 0) return 0;
   return fwd_layout(T, d, I, k, I_shared).total;

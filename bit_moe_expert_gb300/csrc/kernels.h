@@ -21,6 +21,7 @@ enum KernelKind {
   kKGemmDown,
   kKCombine,
   kKPrepack,
+  kKTopkWide,  // exact top-K of wide rows
   kKernelKinds
 };
 void timer_begin(int id, cudaStream_t s);
@@ -49,6 +50,12 @@ cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, i
 // transposed (d a multiple of 32).
 cudaError_t launch_router(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, float* logits,
                           cudaStream_t stream, bool pdl);
+
+// Exact top-K (K <= 64) of each row of logits [T][V] (V <= 2^20): values and
+// indices [T][K], descending, a lower index first among equal values.
+size_t topk_wide_smem_bytes(int V, int K);
+cudaError_t launch_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices,
+                             int num_sms, cudaStream_t stream, bool pdl);
 
 // ---------------------------------------------------------------- decode GEMV
 constexpr int kDecodeRowsGU = 32;      // gate/up rows per item (phase 1)

@@ -11,7 +11,8 @@ namespace bm {
 namespace {
 
 const char* const kNames[kKernelKinds] = {"route", "decode", "router", "x_gather",
-                                          "gemm_gateup", "gemm_down", "combine", "prepack"};
+                                          "gemm_gateup", "gemm_down", "combine", "prepack",
+                                          "topk_wide"};
 
 struct Pending {
   int id;

@@ -242,6 +242,23 @@ moe_status moe_router_logits(const uint16_t* X, int T, int d, const uint16_t* W_
 moe_status moe_route_x(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, int k, int block_rows,
                        float* logits, moe_routing* out, void* ws, size_t ws_bytes, moe_stream stream);
 
+/* ------------------------------------------------------------------ wide top-K
+ * The K largest entries of each row of logits [T][V] (fp32, row-major, device):
+ * values [T][K] (fp32) and indices [T][K] (int32), caller-owned device arrays,
+ * in descending order, a lower index first among equal values (-0.0 equals
+ * +0.0; a value is copied from its entry).  "Squeezing a 26B diffusion LLM onto
+ * a Mac", section "The optimizations that worked", item 1: the sampler needs
+ * only the top ~64 candidates of 262,144 logits per canvas position, found by
+ * a two-stage chunk-max selection that is exact.  Exact here too (no
+ * approximation): chunk maxima of 256 entries, the K best chunks, then the top
+ * K of their entries.
+ * Preconditions: T >= 0 (T = 0 does nothing), 1 <= K <= 64 (MOE_ERR_UNSUPPORTED
+ * above), K <= V <= 2^20 (MOE_ERR_UNSUPPORTED above), no NaN entries (a NaN
+ * orders above +inf), logits 4-byte aligned.  Asynchronous; allocates
+ * nothing. */
+moe_status moe_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices,
+                         moe_stream stream);
+
 /* ------------------------------------------------------------------ whole layer
  * Workspace bytes moe_layer needs (the forward workspace followed by a routing
  * workspace); same rules: zero-filled once, 256-byte aligned, one in-flight
