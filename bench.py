@@ -727,6 +727,43 @@ def run_sweep(dev, peaks, args):
             "peak_hbm_gbs": peaks["hbm_gbs"], "clocks": None}
 
 
+def topk_wide_measure(dev, peaks):
+    """The exact wide top-K (moe_topk_wide) at the canvas sampler's shape: 256 positions x 262,144 logits, K = 64
+    (268 MB of logits, beyond L2); 20 calls in a CUDA graph, timed with events."""
+    import torch
+    import bit_moe_expert_gb300 as bm
+    T, V, K = 256, 262144, 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    x = torch.randn((T, V), generator=gen, device=dev, dtype=torch.float32)
+    vals = torch.empty((T, K), device=dev, dtype=torch.float32)
+    idx = torch.empty((T, K), device=dev, dtype=torch.int32)
+    s = torch.cuda.Stream(device=dev)
+    n = 20
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            bm.moe_topk_wide(x, K, vals, idx)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                bm.moe_topk_wide(x, K, vals, idx)
+        g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        e1.synchronize()
+    us = e0.elapsed_time(e1) / n * 1e3
+    nbytes = T * V * 4 + T * K * 8
+    del x
+    return {"T": T, "V": V, "K": K, "us_per_call": us, "positions_per_s": T / (us * 1e-6), "bound": "hbm",
+            "achieved": nbytes / us / 1e3, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": nbytes / us / 1e3 / peaks["hbm_gbs"], "bytes_per_call": nbytes,
+            "note": "logits N(0,1) fp32 from a seeded device generator; one launch per call"}
+
+
 def cpu_baseline(wl, budget_s):
     tokens, secs, desc = wl.cpu_sample(budget_s)
     return {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
@@ -884,6 +921,7 @@ def main():
         del wl2
         torch.cuda.empty_cache()
     router = router_measure(dev, peaks) if (args.workload == "decode" and not args.no_secondary) else None
+    wide = topk_wide_measure(dev, peaks) if (args.workload == "decode" and not args.no_secondary) else None
 
     if dist.rank == 0:
         line = {
@@ -904,6 +942,8 @@ def main():
             line["prefill4096"] = secondary
         if router is not None:
             line["router_projection"] = router
+        if wide is not None:
+            line["topk_wide"] = wide
         print(json.dumps(line), flush=True)
     dist.close()
 
