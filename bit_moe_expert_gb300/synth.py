@@ -33,7 +33,6 @@ from typing import Optional
 import numpy as np
 
 GROUP = 64          # weights per (scale, bias) group along K
-CODES_PER_WORD = 8  # 4-bit codes per uint32
 
 
 @dataclasses.dataclass(frozen=True)
@@ -49,6 +48,7 @@ class LayerConfig:
     seed: int
     chunk: int = 0      # tokens per call when the prompt is processed in chunks (0 = T)
     zipf: bool = False  # skewed router logits
+    bits: int = 4       # bits per expert weight code (4 or 2)
 
     @property
     def tokens_per_call(self) -> int:
@@ -63,17 +63,19 @@ CONFIGS = {
     "prefill4096": LayerConfig("prefill4096", T=4096, d=2048, E=256, k=8, I=512, I_shared=512, layers=40,
                                seed=3, chunk=1024, zipf=True),
     "canvas": LayerConfig("canvas", T=256, d=2816, E=128, k=8, I=704, I_shared=0, layers=30, seed=4),
+    # the decode layer with 2-bit expert codes (the low-bit experts of the "next" steps)
+    "decode2b": LayerConfig("decode2b", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=6, bits=2),
 }
 
 
-def expert_bytes(N: int, K: int) -> int:
-    """Bytes of one packed matrix: K/2 per row of codes plus 2+2 bytes per group."""
-    return N * (K // 2) + 2 * 2 * N * (K // GROUP)
+def expert_bytes(N: int, K: int, bits: int = 4) -> int:
+    """Bytes of one packed matrix: K*bits/8 per row of codes plus 2+2 bytes per group."""
+    return N * (K * bits // 8) + 2 * 2 * N * (K // GROUP)
 
 
-def ffn_bytes(d: int, I: int) -> int:
+def ffn_bytes(d: int, I: int, bits: int = 4) -> int:
     """Bytes of one expert (gate, up, down)."""
-    return 2 * expert_bytes(I, d) + expert_bytes(d, I)
+    return 2 * expert_bytes(I, d, bits) + expert_bytes(d, I, bits)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -91,12 +93,18 @@ def _rng(seed: int, layer: int, tag: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, layer, tag])))
 
 
-def draw_qmat(rng: np.random.Generator, E: int, N: int, K: int):
-    """One stacked packed matrix: (q [E][N][K/8] u32, scale, bias [E][N][K/64] u16)."""
-    assert K % GROUP == 0
-    q = rng.integers(0, 2**32, size=(E, N, K // CODES_PER_WORD), dtype=np.uint64).astype(np.uint32)
-    s = f32_to_bf16_bits(rng.uniform(0.002, 0.02, size=(E, N, K // GROUP)).astype(np.float32))
-    b = f32_to_bf16_bits(bf16_bits_to_f32(s) * np.float32(-8.0))
+# Scale range and bias factor per code width: bias = -half the code range
+# times the scale (exact in bf16), so the weights are (q - 2^(bits-1)) * scale
+# and the 2-bit weights span about the same range as the 4-bit ones.
+SCALE_RANGE = {4: (0.002, 0.02), 2: (0.008, 0.08)}
+
+
+def draw_qmat(rng: np.random.Generator, E: int, N: int, K: int, bits: int = 4):
+    """One stacked packed matrix: (q [E][N][K*bits/32] u32, scale, bias [E][N][K/64] u16)."""
+    assert K % GROUP == 0 and bits in SCALE_RANGE
+    q = rng.integers(0, 2**32, size=(E, N, K * bits // 32), dtype=np.uint64).astype(np.uint32)
+    s = f32_to_bf16_bits(rng.uniform(*SCALE_RANGE[bits], size=(E, N, K // GROUP)).astype(np.float32))
+    b = f32_to_bf16_bits(bf16_bits_to_f32(s) * np.float32(-(1 << (bits - 1))))
     return q, s, b
 
 
@@ -135,9 +143,9 @@ def draw_experts(cfg: LayerConfig, layer: int, E: Optional[int] = None, I: Optio
     E = cfg.E if E is None else E
     I = cfg.I if I is None else I
     return {
-        "gate": draw_qmat(_rng(cfg.seed, layer, tag + 0), E, I, cfg.d),
-        "up": draw_qmat(_rng(cfg.seed, layer, tag + 1), E, I, cfg.d),
-        "down": draw_qmat(_rng(cfg.seed, layer, tag + 2), E, cfg.d, I),
+        "gate": draw_qmat(_rng(cfg.seed, layer, tag + 0), E, I, cfg.d, cfg.bits),
+        "up": draw_qmat(_rng(cfg.seed, layer, tag + 1), E, I, cfg.d, cfg.bits),
+        "down": draw_qmat(_rng(cfg.seed, layer, tag + 2), E, cfg.d, I, cfg.bits),
     }
 
 
@@ -163,13 +171,14 @@ def small_config(**kw) -> LayerConfig:
 # parity check copies the device bytes it needs back to the host.
 # ---------------------------------------------------------------------------
 
-def draw_qmat_torch(gen, E: int, N: int, K: int, device):
+def draw_qmat_torch(gen, E: int, N: int, K: int, device, bits: int = 4):
     import torch
-    q = torch.randint(-2**31, 2**31, (E, N, K // CODES_PER_WORD), generator=gen, device=device,
+    q = torch.randint(-2**31, 2**31, (E, N, K * bits // 32), generator=gen, device=device,
                       dtype=torch.int64).to(torch.int32)
-    s = torch.empty((E, N, K // GROUP), device=device, dtype=torch.float32).uniform_(0.002, 0.02, generator=gen)
+    s = torch.empty((E, N, K // GROUP), device=device, dtype=torch.float32).uniform_(*SCALE_RANGE[bits],
+                                                                                      generator=gen)
     s = s.to(torch.bfloat16)
-    b = (s.float() * -8.0).to(torch.bfloat16)
+    b = (s.float() * -float(1 << (bits - 1))).to(torch.bfloat16)
     return q, s.view(torch.int16), b.view(torch.int16)
 
 
@@ -181,19 +190,20 @@ def draw_experts_torch(cfg: LayerConfig, layer: int, device, E: Optional[int] = 
     gen = torch.Generator(device=device)
     gen.manual_seed(cfg.seed * 1_000_003 + layer * 1009 + tag)
     return {
-        "gate": draw_qmat_torch(gen, E, I, cfg.d, device),
-        "up": draw_qmat_torch(gen, E, I, cfg.d, device),
-        "down": draw_qmat_torch(gen, E, cfg.d, I, device),
+        "gate": draw_qmat_torch(gen, E, I, cfg.d, device, cfg.bits),
+        "up": draw_qmat_torch(gen, E, I, cfg.d, device, cfg.bits),
+        "down": draw_qmat_torch(gen, E, cfg.d, I, device, cfg.bits),
     }
 
 
 def config_summary(cfg: LayerConfig) -> dict:
-    per_expert = ffn_bytes(cfg.d, cfg.I)
+    per_expert = ffn_bytes(cfg.d, cfg.I, cfg.bits)
     return {
         "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "I_shared": cfg.I_shared,
         "layers": cfg.layers, "chunk": cfg.chunk, "zipf": cfg.zipf,
         "bytes_per_expert": per_expert,
-        "bytes_per_layer_all_experts": cfg.E * per_expert + (ffn_bytes(cfg.d, cfg.I_shared) if cfg.I_shared else 0),
+        "bytes_per_layer_all_experts": cfg.E * per_expert + (ffn_bytes(cfg.d, cfg.I_shared, cfg.bits)
+                                                              if cfg.I_shared else 0),
         "flops_per_token_per_expert": 6 * cfg.d * cfg.I,
         "log2_E": math.log2(cfg.E),
     }

@@ -16,7 +16,16 @@ _lib = None
 
 
 class QMat(C.Structure):
-    _fields_ = [("q", C.c_void_p), ("scale", C.c_void_p), ("bias", C.c_void_p)]
+    _fields_ = [("q", C.c_void_p), ("scale", C.c_void_p), ("bias", C.c_void_p), ("bits", C.c_int)]
+
+
+def code_bits(qsb) -> int:
+    """Bits per code of a packed matrix (q [E][N][K*bits/32], scale [E][N][K/64])."""
+    words, groups = qsb[0].shape[-1], qsb[1].shape[-1]
+    bits = 32 * words // (64 * groups)
+    if bits not in (2, 4) or 32 * words != bits * 64 * groups:
+        raise ValueError("codes and group parameters disagree on K")
+    return bits
 
 
 class Experts(C.Structure):
@@ -72,7 +81,7 @@ class _Keep:
     def qmat(self, qsb) -> QMat:
         q, s, b = (_c(qsb[0], np.uint32), _c(qsb[1], np.uint16), _c(qsb[2], np.uint16))
         self.arrays += [q, s, b]
-        return QMat(_ptr(q), _ptr(s), _ptr(b))
+        return QMat(_ptr(q), _ptr(s), _ptr(b), code_bits(qsb))
 
     def experts(self, ex: Optional[dict]) -> Optional[Experts]:
         if ex is None:
@@ -92,16 +101,16 @@ def double_to_bf16(x: float) -> int:
 def dequant(qsb, e: int, n: int, k: int) -> float:
     keep = _Keep()
     m = keep.qmat(qsb)
-    _, N, K8 = qsb[0].shape
-    return lib().oracle_dequant(C.byref(m), N, K8 * 8, e, n, k)
+    N, K = qsb[1].shape[1], qsb[1].shape[2] * 64
+    return lib().oracle_dequant(C.byref(m), N, K, e, n, k)
 
 
 def dequant_matrix(qsb, e: int) -> np.ndarray:
     keep = _Keep()
     m = keep.qmat(qsb)
-    _, N, K8 = qsb[0].shape
-    out = np.empty((N, K8 * 8), dtype=np.float64)
-    lib().oracle_dequant_matrix(C.byref(m), N, K8 * 8, e, _ptr(out))
+    N, K = qsb[1].shape[1], qsb[1].shape[2] * 64
+    out = np.empty((N, K), dtype=np.float64)
+    lib().oracle_dequant_matrix(C.byref(m), N, K, e, _ptr(out))
     return out
 
 

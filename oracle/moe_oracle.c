@@ -44,11 +44,16 @@ uint16_t oracle_double_to_bf16(double x) {
 
 /* [Lily-blog] "Prefill: keep routing on the GPU, dequantize in flight": every
  * group of 64 weights shares a bf16 scale and bias; [Lily-news]: the compressed
- * values carry a scale and bias used to reconstruct them.  w = q*scale + bias. */
+ * values carry a scale and bias used to reconstruct them.  w = q*scale + bias.
+ * [DGemma] "The physics ceiling: why 300+ tok/s is blocked" proposes the same
+ * groupwise format with 2-3 bit codes; the 2-bit form here packs 16 codes per
+ * word, low bits first along K, like the 4-bit one. */
 double oracle_dequant(const oracle_qmat* m, int N, int K, int e, int n, int k) {
+  const int bits = m->bits ? m->bits : 4;
+  const int per = 32 / bits; /* codes per word */
   size_t row = (size_t)e * N + n;
-  uint32_t word = m->q[row * (K / 8) + k / 8];
-  uint32_t code = (word >> (4 * (k % 8))) & 0xFu;
+  uint32_t word = m->q[row * (size_t)(K / per) + k / per];
+  uint32_t code = (word >> (bits * (k % per))) & ((1u << bits) - 1u);
   size_t g = row * (K / GROUP) + k / GROUP;
   return (double)code * oracle_bf16_to_double(m->scale[g]) + oracle_bf16_to_double(m->bias[g]);
 }
@@ -58,12 +63,6 @@ void oracle_dequant_matrix(const oracle_qmat* m, int N, int K, int e, double* ou
     for (int k = 0; k < K; ++k) out[(size_t)n * K + k] = oracle_dequant(m, N, K, e, n, k);
 }
 
-typedef struct {
-  float v;
-  int i;
-} kv;
-
-/* Descending value; among equal values the lower index first. */
 /* [Lily-blog] "Why Qwen3.6-35B-A3B is a weird workload": the router scores
  * every expert for a token.  The score is the dot product of the token's
  * hidden state with the expert's router row, summed in index order. */
@@ -117,6 +116,12 @@ int oracle_topk_wide(const float* logits, int T, int V, int K, float* values, in
   return 0;
 }
 
+typedef struct {
+  float v;
+  int i;
+} kv;
+
+/* Descending value; among equal values the lower index first. */
 static int kv_cmp(const void* pa, const void* pb) {
   const kv* a = (const kv*)pa;
   const kv* b = (const kv*)pb;

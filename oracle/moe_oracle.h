@@ -14,8 +14,9 @@
  *                for Qwen3.6-35B-A3B on Apple Silicon"
  *   [DGemma]     "Squeezing a 26B diffusion LLM onto a Mac"
  *
- * Weight layout (row-major, little-endian):
- *   q     uint32 [E][N][K/8]  code for column k in bits 4*(k%8) of word k/8
+ * Weight layout (row-major, little-endian), b = bits per code (4 or 2):
+ *   q     uint32 [E][N][K*b/32]  code for column k in bits b*(k%(32/b)) of
+ *                                word k/(32/b) (b = 4: 4*(k%8) of word k/8)
  *   scale uint16 [E][N][K/64] bf16 bit patterns, one per 64-column group
  *   bias  uint16 [E][N][K/64] bf16 bit patterns
  * gate/up: N = I, K = d.  down: N = d, K = I.
@@ -33,6 +34,7 @@ typedef struct {
   const uint32_t* q;
   const uint16_t* scale;
   const uint16_t* bias;
+  int bits; /* bits per code: 4 or 2 (0 means 4) */
 } oracle_qmat;
 
 typedef struct {
@@ -44,7 +46,8 @@ typedef struct {
 double oracle_bf16_to_double(uint16_t h);
 uint16_t oracle_double_to_bf16(double x);
 
-/* One dequantised weight: w = q * scale + bias of its group (exact in fp64). */
+/* One dequantised weight: w = q * scale + bias of its group (exact in fp64),
+ * q the code of m->bits bits. */
 double oracle_dequant(const oracle_qmat* m, int N, int K, int e, int n, int k);
 
 /* Dequantise a whole [N][K] matrix of expert e into out (row-major). */

@@ -97,11 +97,14 @@ def test_dequant_special_cases(oracle):
 
 
 def _numpy_dequant(qsb, e):
-    """Independent vectorised dequantisation (NumPy bit operations)."""
+    """Independent vectorised dequantisation (NumPy bit operations); the code
+    width follows from the shapes (K*bits/32 words and K/64 groups per row)."""
     q, s, b = qsb
+    bits = 32 * q.shape[-1] // (64 * s.shape[-1])
+    per = 32 // bits
     words = q[e].astype(np.uint64)
-    shifts = (4 * np.arange(8, dtype=np.uint64))[None, None, :]
-    codes = ((words[:, :, None] >> shifts) & 0xF).reshape(words.shape[0], -1).astype(np.float64)
+    shifts = (bits * np.arange(per, dtype=np.uint64))[None, None, :]
+    codes = ((words[:, :, None] >> shifts) & ((1 << bits) - 1)).reshape(words.shape[0], -1).astype(np.float64)
     sc = np.repeat(synth.bf16_bits_to_f32(s[e]).astype(np.float64), 64, axis=1)
     bi = np.repeat(synth.bf16_bits_to_f32(b[e]).astype(np.float64), 64, axis=1)
     return codes * sc + bi
@@ -109,9 +112,39 @@ def _numpy_dequant(qsb, e):
 
 def test_dequant_matches_independent_numpy(oracle):
     rng = np.random.default_rng(2)
-    qsb = synth.draw_qmat(rng, 3, 16, 192)
-    for e in range(3):
-        np.testing.assert_array_equal(oracle.dequant_matrix(qsb, e), _numpy_dequant(qsb, e))
+    for bits in (4, 2):
+        qsb = synth.draw_qmat(rng, 3, 16, 192, bits)
+        for e in range(3):
+            np.testing.assert_array_equal(oracle.dequant_matrix(qsb, e), _numpy_dequant(qsb, e))
+
+
+def test_dequant_two_bit_hand_worked_example(oracle):
+    # word 0xE4 = 0b11_10_01_00 holds codes 0, 1, 2, 3 for columns 0..3 (low bits first), then zeros;
+    # the second word's top code (column 31) is 3; scale 0.25 and bias -0.5 give q / 4 - 1 / 2
+    words = np.zeros((1, 1, 4), np.uint32)
+    words[0, 0, 0] = 0xE4
+    words[0, 0, 1] = 0xC0000000
+    s = np.full((1, 1, 1), 0x3E80, np.uint16)   # 0.25
+    b = np.full((1, 1, 1), 0xBF00, np.uint16)   # -0.5
+    qsb = (words, s, b)
+    want = {0: -0.5, 1: -0.25, 2: 0.0, 3: 0.25, 4: -0.5, 30: -0.5, 31: 0.25, 63: -0.5}
+    for k, v in want.items():
+        assert oracle.dequant(qsb, 0, 0, k) == v, k
+    row = oracle.dequant_matrix(qsb, 0)[0]
+    assert row.shape == (64,) and row[3] == 0.25 and row[31] == 0.25 and np.count_nonzero(row == 0.25) == 2
+
+
+def test_dequant_two_bit_special_cases(oracle):
+    rng = np.random.default_rng(3)
+    q, s, b = synth.draw_qmat(rng, 2, 8, 128, bits=2)
+    assert q.shape == (2, 8, 8)
+    bias = synth.bf16_bits_to_f32(b[1]).astype(np.float64)
+    np.testing.assert_array_equal(oracle.dequant_matrix((np.zeros_like(q), s, b), 1), np.repeat(bias, 64, axis=1))
+    # every code 2 with bias = -2*scale gives exactly zero; code 3 gives the scale
+    assert not np.any(oracle.dequant_matrix((np.full_like(q, 0xAAAAAAAA), s, b), 0))
+    sc = synth.bf16_bits_to_f32(s[0]).astype(np.float64)
+    np.testing.assert_array_equal(oracle.dequant_matrix((np.full_like(q, 0xFFFFFFFF), s, b), 0),
+                                  np.repeat(sc, 64, axis=1))
 
 
 # ---------------------------------------------------------------- top-k routing
@@ -426,7 +459,8 @@ def _dense_brute_force(layer, ids, w):
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(T=9, E=8, k=3, I=64, I_shared=0, d=128),
-                                dict(T=5, E=4, k=4, I=64, I_shared=192, d=64)])
+                                dict(T=5, E=4, k=4, I=64, I_shared=192, d=64),
+                                dict(T=7, E=6, k=2, I=128, I_shared=64, d=128, bits=2)])
 def test_forward_matches_dense_brute_force(oracle, kw):
     cfg = synth.small_config(**kw)
     layer = synth.draw_layer(cfg)
