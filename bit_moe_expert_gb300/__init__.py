@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_NONFINITE"}
 
 # Every symbol the headers in include/ declare.
-EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes", "moe_prepack_scales",
+EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes",
+            "moe_prepack_codes_bits", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
             "moe_router_logits", "moe_route_x", "moe_layer_x", "moe_topk_wide",
             "moe_forward_workspace_bytes",
@@ -39,7 +40,7 @@ class _QMat(C.Structure):
 
 
 class _Experts(C.Structure):
-    _fields_ = [("gate", _QMat), ("up", _QMat), ("down", _QMat), ("n_experts", C.c_int)]
+    _fields_ = [("gate", _QMat), ("up", _QMat), ("down", _QMat), ("n_experts", C.c_int), ("bits", C.c_int)]
 
 
 class _Routing(C.Structure):
@@ -67,6 +68,8 @@ def lib(path: Optional[str] = None):
         L.moe_prepack_bytes.argtypes = [C.c_int, C.c_int, C.c_int]
         L.moe_prepack_codes.restype = C.c_int
         L.moe_prepack_codes.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.moe_prepack_codes_bits.restype = C.c_int
+        L.moe_prepack_codes_bits.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.moe_prepack_scales.restype = C.c_int
         L.moe_prepack_scales.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.moe_route_max_blocks.restype = C.c_int
@@ -135,7 +138,7 @@ def _ptr(t) -> int:
 
 @dataclasses.dataclass
 class QMat:
-    """One stacked packed matrix on the device: q int32 [E][K/64][N][8] (group-major codes),
+    """One stacked packed matrix on the device: q int32 [E][K/64][N][2 bits] (group-major codes),
     sb int32 [E][K/64][N]."""
     q: "object"
     sb: "object"
@@ -158,8 +161,13 @@ class Experts:
     def I(self) -> int:
         return int(self.gate.sb.shape[2])
 
+    @property
+    def bits(self) -> int:
+        """Bits per code: the prepacked rows hold 2 x bits words per group."""
+        return int(self.gate.q.shape[3]) // 2
+
     def _c(self) -> _Experts:
-        return _Experts(self.gate._c(), self.up._c(), self.down._c(), self.n_experts)
+        return _Experts(self.gate._c(), self.up._c(), self.down._c(), self.n_experts, self.bits)
 
 
 @dataclasses.dataclass
@@ -212,10 +220,11 @@ def moe_prepack_bytes(E: int, N: int, K: int) -> int:
     return int(lib().moe_prepack_bytes(E, N, K))
 
 
-def moe_prepack_codes(q, qp, stream=None) -> None:
-    """q int32 [E][N][K/8] (row-major codes) -> qp int32 [E][K/64][N][8] (group-major)."""
-    E, N, K8 = q.shape
-    _check("moe_prepack_codes", lib().moe_prepack_codes(_ptr(q), E, N, K8 * 8, _ptr(qp), _stream(stream)))
+def moe_prepack_codes(q, qp, stream=None, bits: int = 4) -> None:
+    """q int32 [E][N][K*bits/32] (row-major codes) -> qp int32 [E][K/64][N][2 bits] (group-major)."""
+    E, N, W = q.shape
+    K = W * 32 // bits
+    _check("moe_prepack_codes_bits", lib().moe_prepack_codes_bits(_ptr(q), E, N, K, bits, _ptr(qp), _stream(stream)))
 
 
 def moe_prepack_scales(scale, bias, sb, stream=None) -> None:
@@ -353,9 +362,9 @@ def moe_profile_read() -> dict:
 def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
     """Device copy of one expert set in the kernels' format.
 
-    ex maps "gate", "up", "down" to (q, scale, bias): q uint32/int32 [E][N][K/8],
-    scale and bias uint16/int16 bf16 bits [E][N][K/64], as NumPy arrays or
-    torch tensors.  Codes and group parameters are reordered once with
+    ex maps "gate", "up", "down" to (q, scale, bias): q uint32/int32 [E][N][K*bits/32]
+    (4- or 2-bit codes, the width following from the shapes), scale and bias
+    uint16/int16 bf16 bits [E][N][K/64], as NumPy arrays or torch tensors.  Codes and group parameters are reordered once with
     moe_prepack_codes and moe_prepack_scales (a one-time layout change, like
     loading a checkpoint).
     """
@@ -374,10 +383,13 @@ def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
         sd = dev(s, np.int16, torch.int16)
         bd = dev(b, np.int16, torch.int16)
         E, N, G = sd.shape
+        bits = 32 * int(qd.shape[2]) // (64 * G)
+        if bits not in (2, 4) or bits * 64 * G != 32 * int(qd.shape[2]):
+            raise ValueError(f"{name}: codes [E][N][{qd.shape[2]}] do not match {G} groups of 4- or 2-bit codes")
         sb = torch.empty((E, G, N), dtype=torch.int32, device=device)
         moe_prepack_scales(sd, bd, sb, stream)
-        qp = torch.empty((E, G, N, 8), dtype=torch.int32, device=device)
-        moe_prepack_codes(qd, qp, stream)
+        qp = torch.empty((E, G, N, 2 * bits), dtype=torch.int32, device=device)
+        moe_prepack_codes(qd, qp, stream, bits)
         del qd
         mats[name] = QMat(qp, sb)
     return Experts(**mats)

@@ -39,28 +39,28 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
   return r == CUDA_SUCCESS;
 }
 
-// codes q [E][K/64][N][8] uint32 (group-major, moe_prepack_codes), seen as
-// a 3-D tensor [E*K/64][N][8]; a box covers box_rows rows of box_groups
-// consecutive groups
+// codes q [E][K/64][N][wpg] uint32 (group-major, moe_prepack_codes; wpg = 2 x
+// bits per code words per row and group), seen as a 3-D tensor
+// [E*K/64][N][wpg]; a box covers box_rows rows of box_groups consecutive groups
 bool encode_codes(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_rows,
-                  cuuint32_t box_groups, CUtensorMapSwizzle sw) {
+                  cuuint32_t box_groups, CUtensorMapSwizzle sw, int wpg) {
   const int G = K / 64;
-  const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E) * G};
-  const cuuint64_t strides[2] = {32, static_cast<cuuint64_t>(N) * 32};
-  const cuuint32_t box[3] = {8, box_rows, box_groups};
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(wpg), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(E) * G};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(wpg) * 4, static_cast<cuuint64_t>(N) * wpg * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(wpg), box_rows, box_groups};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, sw);
 }
 
-// The same codes seen as [E][K/64][N*8]: the pieces of consecutive rows of
-// one group are contiguous, so a box of box_rows rows (box_rows*32 bytes, at
-// most 1 KiB) is one line; box_groups consecutive groups of one expert
+// The same codes seen as [E][K/64][N*wpg]: the pieces of consecutive rows of
+// one group are contiguous, so a box of box_rows rows (box_rows*wpg*4 bytes,
+// at most 1 KiB) is one line; box_groups consecutive groups of one expert
 // (groups past the last read as zeros)
 bool encode_codes_rows(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_rows,
-                       cuuint32_t box_groups) {
+                       cuuint32_t box_groups, int wpg) {
   const int G = K / 64;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N) * 8, static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(E)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 32, static_cast<cuuint64_t>(N) * 32 * G};
-  const cuuint32_t box[3] = {box_rows * 8, box_groups, 1};
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N) * wpg, static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * wpg * 4, static_cast<cuuint64_t>(N) * wpg * 4 * G};
+  const cuuint32_t box[3] = {box_rows * static_cast<cuuint32_t>(wpg), box_groups, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -139,8 +139,11 @@ FwdLayout fwd_layout(int T, int d, int I, int k, int I_shared) {
 bool qmat_ok(const moe_qmat& m) { return m.q && m.sb && aligned16(m.q) && aligned16(m.sb); }
 
 bool experts_ok(const moe_experts* ex) {
-  return ex && qmat_ok(ex->gate) && qmat_ok(ex->up) && qmat_ok(ex->down) && ex->n_experts >= 1;
+  return ex && qmat_ok(ex->gate) && qmat_ok(ex->up) && qmat_ok(ex->down) && ex->n_experts >= 1 &&
+         (ex->bits == 0 || ex->bits == 4 || ex->bits == 2);
 }
+
+int code_bits(const moe_experts* ex) { return ex->bits == 2 ? 2 : 4; }
 
 }  // namespace
 
@@ -171,12 +174,18 @@ size_t moe_prepack_bytes(int E, int N, int K) {
   return static_cast<size_t>(E) * (K / 64) * N * 4;
 }
 
-moe_status moe_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, moe_stream stream) {
+moe_status moe_prepack_codes_bits(const uint32_t* q, int E, int N, int K, int bits, uint32_t* qp,
+                                  moe_stream stream) {
   if (!q || !qp || E < 1 || N < 1 || K < 64 || K % 64 != 0 || !aligned16(q) || !aligned16(qp))
     return MOE_ERR_INVALID_ARG;
-  if (launch_prepack_codes(q, E, N, K, qp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (bits != 4 && bits != 2) return MOE_ERR_INVALID_ARG;
+  if (launch_prepack_codes(q, E, N, K, bits, qp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, moe_stream stream) {
+  return moe_prepack_codes_bits(q, E, N, K, 4, qp, stream);
 }
 
 moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
@@ -279,6 +288,9 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
   if ((shared != nullptr) != (I_shared > 0)) return MOE_ERR_INVALID_ARG;
   if (!experts_ok(routed) || (shared && (!experts_ok(shared) || shared->n_experts != 1)))
     return MOE_ERR_INVALID_ARG;
+  const int bits = code_bits(routed);
+  if (shared && code_bits(shared) != bits) return MOE_ERR_INVALID_ARG;
+  const int wpg = 2 * bits;  // code words per row and group
   const int E = routed->n_experts;
   if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
   if (!r) return MOE_ERR_INVALID_ARG;
@@ -311,17 +323,17 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
   if (path == Path::kGemv) {
     DecodeMaps mr, ms;
     const cuuint32_t G1 = static_cast<cuuint32_t>(d / 64), G2 = static_cast<cuuint32_t>(I / 64);
-    bool ok = encode_codes_rows(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-              encode_codes_rows(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-              encode_codes_rows(&mr.q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2) &&
+    bool ok = encode_codes_rows(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+              encode_codes_rows(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+              encode_codes_rows(&mr.q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2, wpg) &&
               encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, G1) &&
               encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, G1) &&
               encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kDecodeRowsDown, G2);
     if (ok && shared) {
       const cuuint32_t G2s = static_cast<cuuint32_t>(I_shared / 64);
-      ok = encode_codes_rows(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-           encode_codes_rows(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups) &&
-           encode_codes_rows(&ms.q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s) &&
+      ok = encode_codes_rows(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+           encode_codes_rows(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+           encode_codes_rows(&ms.q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s, wpg) &&
            encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
            encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
            encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kDecodeRowsDown, G2s);
@@ -344,6 +356,7 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
     a.I_shared = I_shared;
     a.E = E;
     a.num_sms = sm_count();
+    a.bits = bits;
     if (a.num_sms <= 0) return MOE_ERR_CUDA;
     if (launch_decode(a, &mr, shared ? &ms : nullptr, ws, st, pdl) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
@@ -351,22 +364,25 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
 
   if (r->block_rows < 1 || r->block_rows > kGemmBN) return MOE_ERR_UNSUPPORTED;
   const int A = T * k;
+  // a row's codes of one group: 32 bytes (4-bit) read through a 32-byte
+  // swizzle, or 16 bytes (2-bit), already conflict-free
+  const CUtensorMapSwizzle code_swizzle = bits == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
   GemmMaps mr, ms;
   GemmActMaps act;
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
   uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
-  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            encode_codes(&mr.q_up, routed->up.q, E, I, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
-            encode_codes(&mr.q_down, routed->down.q, E, d, I, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kGemmBM, 1, code_swizzle, wpg) &&
+            encode_codes(&mr.q_up, routed->up.q, E, I, d, kGemmBM, 1, code_swizzle, wpg) &&
+            encode_codes(&mr.q_down, routed->down.q, E, d, I, kGemmBM, 1, code_swizzle, wpg) &&
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
             encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
   if (ok && shared)
-    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
-         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
-         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, kGemmBM, 1, CU_TENSOR_MAP_SWIZZLE_32B) &&
+    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmBM, 1, code_swizzle, wpg) &&
+         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmBM, 1, code_swizzle, wpg) &&
+         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, kGemmBM, 1, code_swizzle, wpg) &&
          encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&
@@ -375,6 +391,7 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
   if (!ok) return MOE_ERR_CUDA;
 
   GemmArgs a{};
+  a.bits = bits;
   a.perm = r->perm;
   a.inv_perm = r->inv_perm;
   a.block_map = r->block_map;

@@ -59,8 +59,13 @@ constexpr int kS1 = 5;                          // phase-1 stages
 constexpr int kSB1 = kS1;                       // phase-1 group-parameter buffers: one per stage
 constexpr int kS2Max = 12;                      // phase-2 stages at most
 constexpr int kMaxSlots = kMaxK * kGemvMaxT + 1;  // distinct experts of a call, plus the shared one
-constexpr uint32_t kCodeQ = kChunk * kRows1 * 32;  // bytes of one matrix's codes in a phase-1 stage
-constexpr uint32_t kSt1 = 2 * kCodeQ;               // phase-1 stage: gate codes, up codes
+// kBits bits per weight code (4 or 2): code words per row and 64-column group
+template <int kBits>
+constexpr int kWpg = 2 * kBits;
+template <int kBits>
+constexpr uint32_t kCodeQ = kChunk * kRows1 * 4 * kWpg<kBits>;  // bytes of one matrix's codes in a phase-1 stage
+template <int kBits>
+constexpr uint32_t kSt1 = 2 * kCodeQ<kBits>;  // phase-1 stage: gate codes, up codes
 constexpr size_t kSmemMax = 227 * 1024;
 
 static_assert(kWarps == 2 * kChunk, "phase 1 gives one warp to each (matrix, group) of a stage");
@@ -86,7 +91,7 @@ struct Layout {
 };
 
 // TMA and bulk-copy destinations start on 128 bytes.
-__host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
+__host__ __device__ inline Layout layout(int T, int d, int I, int I_shared, int bits) {
   Layout L;
   L.G1 = d / 64;
   L.nchunk = div_up(L.G1, kChunk);
@@ -94,11 +99,11 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
   const int G2max = L.Imax / 64;
   L.hs_stride = static_cast<int>(round_up(L.Imax / 32, 4));
   L.hrec = static_cast<size_t>(T) * L.Imax * 2 + static_cast<size_t>(T) * L.hs_stride * 4;
-  L.st2_sb = static_cast<size_t>(G2max) * kRows2 * 32;  // codes [G2][16 rows][8 words]
+  L.st2_sb = static_cast<size_t>(G2max) * kRows2 * 8 * bits;  // codes [G2][16 rows][2 bits words]
   L.st2 = round_up(L.st2_sb + static_cast<size_t>(G2max) * kRows2 * 4, 128);
   size_t o = 0;
   L.ring1 = o;
-  o += static_cast<size_t>(kS1) * kSt1;
+  o += static_cast<size_t>(kS1) * 2 * kChunk * kRows1 * 8 * bits;  // kSt1<bits>
   L.sb1 = round_up(2ull * L.G1 * kRows1 * 4, 128);
   L.sbuf1 = o;
   o += kSB1 * L.sb1;
@@ -139,22 +144,41 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared) {
 }
 
 // Four MMA steps over one 64-column group (see the K order above).
-//   wa, wb: words 2q, 2q+1 of rows g and g+8; b: the activation operand of
-//   the four steps (columns 16q .. 16q+15 of the group, token g).
-template <bool kBF16>
+//   wa, wb: the codes of columns 16q .. 16q+15 of rows g and g+8 (4-bit
+//   codes: words 2q, 2q+1; 2-bit codes: word q, in .x); b: the activation
+//   operand of the four steps (the same columns, token g).  Step m takes
+//   columns 16q + 4m .. 16q + 4m + 3: two pairs of adjacent codes, each
+//   formed by one mask from the interleaved word.
+template <bool kBF16, int kBits>
 __device__ __forceinline__ void mma_group(uint2 wa, uint2 wb, const uint32_t (&b)[8], float (&dd)[4]) {
   constexpr uint32_t magic = kBF16 ? 0x43004300u : 0x64006400u;  // pairs (128, 128) / (1024, 1024)
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const uint32_t xa = m < 2 ? wa.x : wa.y;
-    const uint32_t xb = m < 2 ? wb.x : wb.y;
-    const int sh = (m & 1) * 8;
-    const uint32_t a0 = lop3_and_or(xa >> sh, 0x000F000Fu, magic);
-    const uint32_t a1 = lop3_and_or(xb >> sh, 0x000F000Fu, magic);
-    const uint32_t a2 = lop3_and_or(xa >> (sh + 4), 0x000F000Fu, magic);
-    const uint32_t a3 = lop3_and_or(xb >> (sh + 4), 0x000F000Fu, magic);
+    uint32_t a0, a1, a2, a3;
+    if constexpr (kBits == 4) {
+      const uint32_t xa = m < 2 ? wa.x : wa.y;
+      const uint32_t xb = m < 2 ? wb.x : wb.y;
+      const int sh = (m & 1) * 8;
+      a0 = lop3_and_or(xa >> sh, 0x000F000Fu, magic);
+      a1 = lop3_and_or(xb >> sh, 0x000F000Fu, magic);
+      a2 = lop3_and_or(xa >> (sh + 4), 0x000F000Fu, magic);
+      a3 = lop3_and_or(xb >> (sh + 4), 0x000F000Fu, magic);
+    } else {
+      a0 = lop3_and_or(wa.x >> (4 * m), 0x00030003u, magic);  // code pair 2m
+      a1 = lop3_and_or(wb.x >> (4 * m), 0x00030003u, magic);
+      a2 = lop3_and_or(wa.x >> (4 * m + 2), 0x00030003u, magic);  // code pair 2m + 1
+      a3 = lop3_and_or(wb.x >> (4 * m + 2), 0x00030003u, magic);
+    }
     mma_16816<kBF16>(dd, a0, a1, a2, a3, b[2 * m], b[2 * m + 1]);
   }
+}
+
+// The codes of columns 16q .. 16q+15 of one row: 4-bit codes, two words;
+// 2-bit codes, one word (in .x).
+template <int kBits>
+__device__ __forceinline__ uint2 load_codes(const uint32_t* row, int q) {
+  if constexpr (kBits == 4) return *reinterpret_cast<const uint2*>(row + 2 * q);
+  return make_uint2(row[q], 0u);
 }
 
 // The activation operand: 16 consecutive 16-bit values at p (zero when the
@@ -254,14 +278,15 @@ __device__ __forceinline__ void write_routing_outputs(const DecodeArgs& a, const
   }
 }
 
-template <int kT>
+template <int kT, int kBits>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps mr, const __grid_constant__ DecodeMaps ms, const DecodeArgs a,
                   WsHeader* hdr) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int d = a.d;
-  const Layout L = layout(kT, d, a.I, a.I_shared);
+  constexpr int kW = kWpg<kBits>;  // code words per row and group
+  const Layout L = layout(kT, d, a.I, a.I_shared, kBits);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, q4 = lane & 3;  // MMA fragment row group and column pair
   const int nC = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
@@ -333,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool sh = has_shared && slot == 0;
     const int e = sh ? 0 : slot_e[slot];
     const DecodeMaps& m = sh ? ms : mr;
-    uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1;
+    uint8_t* st = ring1 + static_cast<size_t>(stage) * kSt1<kBits>;
     uint64_t* bar = &full1[stage];
     const uint32_t sbb = static_cast<uint32_t>(L.G1) * kRows1 * 4;
-    mbar_arrive_expect_tx(bar, kSt1 + (ch == 0 ? 2 * sbb : 0u));
-    tma_load_3d(st, &m.q_gate, bar, rb * kRows1 * 8, ch * kChunk, e);
-    tma_load_3d(st + kCodeQ, &m.q_up, bar, rb * kRows1 * 8, ch * kChunk, e);
+    mbar_arrive_expect_tx(bar, kSt1<kBits> + (ch == 0 ? 2 * sbb : 0u));
+    tma_load_3d(st, &m.q_gate, bar, rb * kRows1 * kW, ch * kChunk, e);
+    tma_load_3d(st + kCodeQ<kBits>, &m.q_up, bar, rb * kRows1 * kW, ch * kChunk, e);
     if (ch == 0) {
       uint8_t* sbd = smem + L.sbuf1 + static_cast<size_t>(stage) * L.sb1;
       tma_load_3d(sbd, &m.sb_gate, bar, rb * kRows1, 0, e);
@@ -355,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const DecodeMaps& m = sh ? ms : mr;
     uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
     uint64_t* bar = &full2c[stage];
-    mbar_arrive_expect_tx(bar, gx * kRows2 * (32 + 4));
-    tma_load_3d(st, &m.q_down, bar, rb * kRows2 * 8, 0, e);
+    mbar_arrive_expect_tx(bar, gx * kRows2 * (4 * kW + 4));
+    tma_load_3d(st, &m.q_down, bar, rb * kRows2 * kW, 0, e);
     tma_load_3d(st + L.st2_sb, &m.sb_down, bar, rb * kRows2, 0, e);
   };
   auto issue2h = [&](int j2, int nsl) {
@@ -376,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbb = static_cast<uint32_t>(L.G1) * kRows1 * 4;
     if (lane < n) {
       const int j = j0 + lane;
-      mbar_arrive_expect_tx(&full1[j % kS1], kSt1 + (j % L.nchunk == 0 ? 2 * sbb : 0u));
+      mbar_arrive_expect_tx(&full1[j % kS1], kSt1<kBits> + (j % L.nchunk == 0 ? 2 * sbb : 0u));
     }
     __syncwarp();
     const int i = lane >> 2, c = lane & 3;
@@ -390,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int stage = j % kS1;
       uint64_t* bar = &full1[stage];
       if (c < 2) {
-        tma_load_3d(ring1 + static_cast<size_t>(stage) * kSt1 + c * kCodeQ, c == 0 ? &m.q_gate : &m.q_up, bar,
-                    rb * kRows1 * 8, ch * kChunk, e);
+        tma_load_3d(ring1 + static_cast<size_t>(stage) * kSt1<kBits> + c * kCodeQ<kBits>,
+                    c == 0 ? &m.q_gate : &m.q_up, bar, rb * kRows1 * kW, ch * kChunk, e);
       } else {
         tma_load_3d(smem + L.sbuf1 + static_cast<size_t>(stage) * L.sb1 + (c - 2) * sbb, c == 2 ? &m.sb_gate : &m.sb_up,
                     bar, rb * kRows1, 0, e);
@@ -404,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane < n) {
       const int j2 = j0 + lane, slot = j2 % nsl;
       const uint32_t gx = static_cast<uint32_t>(has_shared && slot == 0 ? G2s : G2);
-      mbar_arrive_expect_tx(&full2c[j2 % L.S2], gx * kRows2 * (32 + 4));
+      mbar_arrive_expect_tx(&full2c[j2 % L.S2], gx * kRows2 * (4 * kW + 4));
     }
     __syncwarp();
     const int i = lane >> 1, c = lane & 1;
@@ -415,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = sh ? 0 : slot_e[slot];
       const DecodeMaps& m = sh ? ms : mr;
       uint8_t* st = ring2 + static_cast<size_t>(stage) * L.st2;
-      if (c == 0) tma_load_3d(st, &m.q_down, &full2c[stage], rb * kRows2 * 8, 0, e);
+      if (c == 0) tma_load_3d(st, &m.q_down, &full2c[stage], rb * kRows2 * kW, 0, e);
       else tma_load_3d(st + L.st2_sb, &m.sb_down, &full2c[stage], rb * kRows2, 0, e);
     }
   };
@@ -668,8 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
         const int gi = ch * kChunk + gl;  // this warp's group
         if (gi < L.G1) {
-          const uint32_t* qm = reinterpret_cast<const uint32_t*>(ring1 + static_cast<size_t>(stage) * kSt1 + mat * kCodeQ) +
-                               gl * kRows1 * 8;
+          const uint32_t* qm =
+              reinterpret_cast<const uint32_t*>(ring1 + static_cast<size_t>(stage) * kSt1<kBits> + mat * kCodeQ<kBits>) +
+              gl * kRows1 * kW;
           const uint32_t* sbm = sbi + gi * kRows1;
           uint32_t b[8];
           load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
@@ -679,9 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int tile = 0; tile < 2; ++tile) {
             const int r0 = tile * 16 + g8;
-            const uint2 wa = *reinterpret_cast<const uint2*>(qm + r0 * 8 + 2 * q4);
-            const uint2 wb = *reinterpret_cast<const uint2*>(qm + (r0 + 8) * 8 + 2 * q4);
-            mma_group<true>(wa, wb, b, dd[tile]);
+            const uint2 wa = load_codes<kBits>(qm + r0 * kW, q4);
+            const uint2 wb = load_codes<kBits>(qm + (r0 + 8) * kW, q4);
+            mma_group<true, kBits>(wa, wb, b, dd[tile]);
           }
 #pragma unroll
           for (int tile = 0; tile < 2; ++tile) {
@@ -765,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       g_begin = (p_begin - G2first) % G2;
     }
     // lane-constant offsets: codes of rows g8 and g8 + 8 (words), h of token g8 (halves)
-    const int lq = g8 * 8 + 2 * q4;
+    const int lq = g8 * kW;
     const size_t lh = static_cast<size_t>(g8) * L.Imax + 16 * q4;
     const bool refills = total2 > L.S2;
     for (int rl = 0; rl < my_rbs; ++rl) {
@@ -796,9 +822,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto group = [&](int g, float (&dd)[4]) {
           uint32_t b[8];
           load_b(hp + g * 64, g8 < kT, b);
-          const uint2 wa = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8);
-          const uint2 wb = *reinterpret_cast<const uint2*>(qm + g * kRows2 * 8 + 64);
-          mma_group<false>(wa, wb, b, dd);
+          const uint2 wa = load_codes<kBits>(qm + g * kRows2 * kW, q4);
+          const uint2 wb = load_codes<kBits>(qm + g * kRows2 * kW + 8 * kW, q4);
+          mma_group<false, kBits>(wa, wb, b, dd);
         };
         auto fold = [&](int g, const float (&dd)[4]) {
           const uint32_t p0 = sbm[g * kRows2], p1 = sbm[g * kRows2 + 8];
@@ -888,18 +914,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // CTAs of this kernel that can be resident at once on the current device (0
 // on error).  The barrier over the grid needs every CTA resident together.
-template <int kT>
+template <int kT, int kBits>
 int max_ctas(size_t smem, int num_sms) {
   static int cached_dev = -1, cached = 0;
   static size_t cached_smem = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev == cached_dev && smem == cached_smem) return cached;
-  if (cudaFuncSetAttribute(decode_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_kernel<kT, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemMax)) != cudaSuccess)
     return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kT>, kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kT, kBits>, kThreads, smem) != cudaSuccess)
     return 0;
   cached_dev = dev;
   cached_smem = smem;
@@ -907,10 +933,10 @@ int max_ctas(size_t smem, int num_sms) {
   return cached;
 }
 
-template <int kT>
+template <int kT, int kBits>
 cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
                      size_t smem, cudaStream_t stream, bool pdl) {
-  const int resident = max_ctas<kT>(smem, a.num_sms);
+  const int resident = max_ctas<kT, kBits>(smem, a.num_sms);
   if (resident < 1) return cudaErrorInvalidConfiguration;
   const int grid = want < resident ? want : resident;
   cudaLaunchAttribute attr[1];
@@ -923,7 +949,7 @@ cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const Decode
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kT>, *routed, *sh, a, hdr);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kT, kBits>, *routed, *sh, a, hdr);
 }
 
 }  // namespace
@@ -933,7 +959,7 @@ bool decode_supported(int T, int d, int I, int I_shared, int k) {
   if (d % 64 || I % 64 || I_shared % 64 || I < 64) return false;
   const int Imax = I > I_shared ? I : I_shared;
   if (Imax / 64 > 256 || d / 64 > 256) return false;  // a parameter box covers every group of a row block
-  const Layout L = layout(T, d, I, I_shared);
+  const Layout L = layout(T, d, I, I_shared, 4);  // 2-bit codes need less shared memory
   return L.S2 >= 2 && L.total <= kSmemMax;
 }
 
@@ -947,7 +973,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const D
                           cudaStream_t stream, bool pdl) {
   if (!decode_supported(a.T, a.d, a.I, a.I_shared, a.k)) return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(a.hbuf) & 15u) return cudaErrorInvalidValue;
-  const Layout L = layout(a.T, a.d, a.I, a.I_shared);
+  if (a.bits != 4 && a.bits != 2) return cudaErrorInvalidValue;
+  const Layout L = layout(a.T, a.d, a.I, a.I_shared, a.bits);
   const DecodeMaps* sh = shared ? shared : routed;  // never read without a shared expert
   const int distinct = a.T * a.k < a.E ? a.T * a.k : a.E;
   const int items = a.I_shared / kRows1 + distinct * (a.I / kRows1);
@@ -958,11 +985,20 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const D
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   timer_begin(kKDecode, stream);
   cudaError_t err;
-  switch (a.T) {
-    case 1: err = launch_t<1>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-    case 2: err = launch_t<2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-    case 3: err = launch_t<3>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-    default: err = launch_t<4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+  if (a.bits == 2) {
+    switch (a.T) {
+      case 1: err = launch_t<1, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      case 2: err = launch_t<2, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      case 3: err = launch_t<3, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      default: err = launch_t<4, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+    }
+  } else {
+    switch (a.T) {
+      case 1: err = launch_t<1, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      case 2: err = launch_t<2, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      case 3: err = launch_t<3, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+      default: err = launch_t<4, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
+    }
   }
   timer_end(kKDecode, stream);
   return err;

@@ -50,7 +50,7 @@ constexpr uint32_t kBarEpilogue = 1;  // named barrier of the epilogue warps (0 
 constexpr uint32_t kTmemCols = 512;
 static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns, 16 at a time");
 
-template <bool kGateUp>
+template <bool kGateUp, int kBits>
 struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
   static constexpr int kDqWarps = 4 * kMats;
@@ -67,7 +67,8 @@ struct Cfg {
   // and A-stage rings must then agree on parity
   static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "stage rings must have even length");
   static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to kGemmBN rows x 64 fp16 (128-byte swizzle)
-  static constexpr int kQBytes = kGemmBM * 32;   // 128 rows x 8 code words (32-byte swizzle)
+  // 128 rows x (2 kBits) code words: 4-bit codes with a 32-byte swizzle, 2-bit codes (16 bytes a row) plain
+  static constexpr int kQBytes = kGemmBM * 8 * kBits;
   static constexpr int kSBBytes = kGemmBM * 4;
   static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
   static constexpr int kStageBytes = (kStageTxBytes + 1023) / 1024 * 1024;
@@ -137,14 +138,34 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b
   out[3] = f16x2_fma(f16x2_fma(v3, sixteenth, minus_64), s2, b2);
 }
 
-template <bool kGateUp>
-__global__ void __launch_bounds__(Cfg<kGateUp>::kThreads, 1)
+// Sixteen 2-bit codes of one word in the interleaved order of the prepacked
+// layout (code 2p in bits 2p, code 2p+1 in bits 2p+16) -> eight f16x2 values
+// of q*scale + bias, adjacent columns paired.  A mask leaves pair p at bits 2p
+// as the f16 pair 1024 + 4^p q, exact for p <= 4 (at most 1792); one fp16 FMA
+// by 4^-p recovers q exactly, one more applies scale and bias.  Pairs 5..7
+// take one shift first.
+__device__ __forceinline__ void dequant_word2(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* out) {
+  const uint32_t magic = 0x64006400u;  // f16 pair (1024, 1024)
+  // f16 pairs (4^-p, 4^-p) and (-1024 * 4^-p, ...) for p = 0..4
+  constexpr uint32_t kScale[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+  constexpr uint32_t kShift[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
+  const uint32_t w10 = w >> 10;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int pp = p < 5 ? p : p - 5;
+    const uint32_t v = lop3_and_or(p < 5 ? w : w10, 0x00030003u << (2 * pp), magic);
+    out[p] = f16x2_fma(f16x2_fma(v, kScale[pp], kShift[pp]), s2, b2);
+  }
+}
+
+template <bool kGateUp, int kBits>
+__global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap q0_r, const __grid_constant__ CUtensorMap q1_r,
                     const __grid_constant__ CUtensorMap sb0_r, const __grid_constant__ CUtensorMap sb1_r,
                     const __grid_constant__ CUtensorMap q0_s, const __grid_constant__ CUtensorMap q1_s,
                     const __grid_constant__ CUtensorMap sb0_s, const __grid_constant__ CUtensorMap sb1_s,
                     const __grid_constant__ CUtensorMap act0, const __grid_constant__ CUtensorMap act1, GemmArgs a) {
-  using C = Cfg<kGateUp>;
+  using C = Cfg<kGateUp, kBits>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -382,15 +403,27 @@ __global__ void __launch_bounds__(Cfg<kGateUp>::kThreads, 1)
         const float bf = __uint_as_float(sbv & 0xFFFF0000u);
         const uint32_t s2 = f32x2_to_f16x2(sf, sf);
         const uint32_t b2 = f32x2_to_f16x2(bf, bf);
+        if constexpr (kBits == 4) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
+            uint32_t v[16];
+            dequant_word(w.x, s2, b2, v + 0);
+            dequant_word(w.y, s2, b2, v + 4);
+            dequant_word(w.z, s2, b2, v + 8);
+            dequant_word(w.w, s2, b2, v + 12);
+            tmem_st16(taddr + mat * 32 + h * 16, v);
+          }
+        } else {
+          // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
+          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
           uint32_t v[16];
-          dequant_word(w.x, s2, b2, v + 0);
-          dequant_word(w.y, s2, b2, v + 4);
-          dequant_word(w.z, s2, b2, v + 8);
-          dequant_word(w.w, s2, b2, v + 12);
-          tmem_st16(taddr + mat * 32 + h * 16, v);
+          dequant_word2(w.x, s2, b2, v + 0);
+          dequant_word2(w.y, s2, b2, v + 8);
+          tmem_st16(taddr + mat * 32, v);
+          dequant_word2(w.z, s2, b2, v + 0);
+          dequant_word2(w.w, s2, b2, v + 8);
+          tmem_st16(taddr + mat * 32 + 16, v);
         }
         tc_wait_st();
         tc_fence_before();
@@ -616,21 +649,20 @@ __global__ void __launch_bounds__(kCombineThreads)
   if (!ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
 
-bool g_gemm_attr = false;
-
-}  // namespace
-
-cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
-                        cudaStream_t stream, bool pdl) {
-  using CG = Cfg<true>;
-  using CD = Cfg<false>;
-  if (!g_gemm_attr) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int kBits>
+cudaError_t launch_gemm_t(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared,
+                          const GemmActMaps* act, cudaStream_t stream, bool pdl) {
+  using CG = Cfg<true, kBits>;
+  using CD = Cfg<false, kBits>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<true, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CG::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(moe_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, CD::kSmemBytes);
+    e = cudaFuncSetAttribute(moe_gemm_kernel<false, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CD::kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_gemm_attr = true;
+    attr_set = true;
   }
   const GemmMaps* sh = shared ? shared : routed;
   cudaLaunchAttribute attr[1];
@@ -658,7 +690,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.dynamicSmemBytes = CG::kSmemBytes;
   cfg.blockDim = dim3(CG::kThreads);
   timer_begin(kKGemmGateUp, stream);
-  cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, routed->q_gate, routed->q_up, routed->sb_gate,
+  cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true, kBits>, routed->q_gate, routed->q_up, routed->sb_gate,
                                        routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
   timer_end(kKGemmGateUp, stream);
   if (err != cudaSuccess) return err;
@@ -667,7 +699,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
   cfg.dynamicSmemBytes = CD::kSmemBytes;
   cfg.blockDim = dim3(CD::kThreads);
   timer_begin(kKGemmDown, stream);
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false>, routed->q_down, routed->q_down, routed->sb_down,
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false, kBits>, routed->q_down, routed->q_down, routed->sb_down,
                            routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
                            act->h_shared, a);
   timer_end(kKGemmDown, stream);
@@ -681,6 +713,15 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMap
                            a.I_shared > 0 ? 1 : 0, a.Y, a.status);
   timer_end(kKCombine, stream);
   return err;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
+                        cudaStream_t stream, bool pdl) {
+  if (a.bits == 2) return launch_gemm_t<2>(a, routed, shared, act, stream, pdl);
+  if (a.bits == 4) return launch_gemm_t<4>(a, routed, shared, act, stream, pdl);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace bm

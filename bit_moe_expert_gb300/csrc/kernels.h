@@ -42,7 +42,8 @@ size_t route_hist_elems(int T, int E);
 // status: where device-side errors go (null: the workspace header's status word)
 cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out, void* ws,
                          cudaStream_t stream, bool pdl, uint32_t* status = nullptr);
-cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream);
+cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, int bits, uint32_t* qp,
+                                 cudaStream_t stream);
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream);
 
@@ -64,9 +65,9 @@ constexpr int kDecodeRowsDown = 16;    // output rows per block (phase 2)
 
 // Tensor maps of one expert set for the decode kernel.
 struct DecodeMaps {
-  CUtensorMap q_gate, q_up;    // codes [E][d/64][I*8], box (32 rows * 8 words, kDecodeChunkGroups groups, 1)
+  CUtensorMap q_gate, q_up;    // codes [E][d/64][I*wpg], box (32 rows * wpg words, kDecodeChunkGroups groups, 1)
   CUtensorMap sb_gate, sb_up;  // group parameters [E][d/64][I], box (32 rows, d/64 groups, 1)
-  CUtensorMap q_down;          // codes [E][I/64][d*8], box (16 rows * 8 words, I/64 groups, 1)
+  CUtensorMap q_down;          // codes [E][I/64][d*wpg], box (16 rows * wpg words, I/64 groups, 1)
   CUtensorMap sb_down;         // group parameters [E][I/64][d], box (16 rows, I/64 groups, 1)
 };
 
@@ -82,6 +83,7 @@ struct DecodeArgs {
   uint8_t* hbuf;          // h records of the call's slots, decode_scratch_bytes, 16-byte aligned
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms;
+  int bits;  // bits per weight code: 4 or 2
 };
 
 bool decode_supported(int T, int d, int I, int I_shared, int k);
@@ -95,7 +97,7 @@ constexpr int kGemmBK = 64;    // K per stage = one quantisation group
 constexpr int kGemmBN = 96;    // max tokens per tile (MMA N); two double-buffered accumulators fit TMEM
 
 struct GemmMaps {
-  CUtensorMap q_gate, q_up, q_down;     // codes, box (8 words, 128 rows, 1), 32-byte swizzle
+  CUtensorMap q_gate, q_up, q_down;     // codes, box (wpg words, 128 rows, 1); 32-byte swizzle for 4-bit codes
   CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (128 rows, 1, 1)
 };
 
@@ -113,6 +115,7 @@ struct GemmArgs {
   uint16_t* Y;                // [T][d] bf16
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms, max_blocks;
+  int bits;  // bits per weight code: 4 or 2
 };
 
 struct GemmActMaps {

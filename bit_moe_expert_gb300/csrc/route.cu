@@ -434,8 +434,27 @@ __device__ __forceinline__ uint4 interleave_nibbles(uint4 v) {
 // codes [E][N][K/8] -> [E][K/64][N][8]: each row's 32-byte piece of one group
 // moves next to the same group's piece of the next row; the codes of every
 // word are interleaved (interleave_nibbles)
+// 2-bit codes: inside a word, codes k = 0..15 (k at bits 2k) are reordered so
+// that code 2p sits at bits 2p and code 2p+1 at bits 2p+16: one mask again
+// takes a pair of adjacent codes into the two halves of a register.
+__device__ __forceinline__ uint32_t interleave_pairs2(uint32_t w) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int k = 2 * (i & 7) + (i >> 3);
+    r |= ((w >> (2 * k)) & 0x3u) << (2 * i);
+  }
+  return r;
+}
+__device__ __forceinline__ uint4 interleave_pairs2(uint4 v) {
+  return make_uint4(interleave_pairs2(v.x), interleave_pairs2(v.y), interleave_pairs2(v.z), interleave_pairs2(v.w));
+}
+
+// one row's piece of one group: 32 bytes (4-bit codes) or 16 bytes (2-bit)
+template <int kBits>
 __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, int G, uint4* __restrict__ qp) {
-  const size_t total = static_cast<size_t>(E) * G * N;  // 32-byte pieces
+  constexpr int kU4 = kBits / 2;  // 16-byte units per piece
+  const size_t total = static_cast<size_t>(E) * G * N;
   for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
        o += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int n = static_cast<int>(o % N);
@@ -443,21 +462,27 @@ __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, 
     const int g = static_cast<int>(eg % G);
     const int e = static_cast<int>(eg / G);
     const size_t i = (static_cast<size_t>(e) * N + n) * G + g;
-    qp[2 * o] = interleave_nibbles(q[2 * i]);
-    qp[2 * o + 1] = interleave_nibbles(q[2 * i + 1]);
+#pragma unroll
+    for (int u = 0; u < kU4; ++u)
+      qp[kU4 * o + u] = kBits == 4 ? interleave_nibbles(q[kU4 * i + u]) : interleave_pairs2(q[kU4 * i + u]);
   }
 }
 }  // namespace
 
-cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, cudaStream_t stream) {
+cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, int bits, uint32_t* qp,
+                                 cudaStream_t stream) {
   const int G = K / 64;
   const size_t total = static_cast<size_t>(E) * G * N;
   const int threads = 256;
   const size_t blocks = (total + threads - 1) / threads;
   const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
   timer_begin(kKPrepack, stream);
-  prepack_codes_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(q), E, N, G,
-                                                      reinterpret_cast<uint4*>(qp));
+  if (bits == 2)
+    prepack_codes_kernel<2><<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(q), E, N, G,
+                                                          reinterpret_cast<uint4*>(qp));
+  else
+    prepack_codes_kernel<4><<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(q), E, N, G,
+                                                          reinterpret_cast<uint4*>(qp));
   const cudaError_t err = cudaGetLastError();
   timer_end(kKPrepack, stream);
   return err;
