@@ -200,15 +200,15 @@ def _dev_layer(cfg, layer, dev, with_shared=True):
 
 
 class DecodeWorkload(Workload):
-    name = "decode"
     dtype = "f32"
     api_desc = "moe_layer"
 
-    def __init__(self, dev, layers=None):
+    def __init__(self, dev, layers=None, name="decode"):
         import torch
         import bit_moe_expert_gb300 as bm
         self.bm = bm
-        self.cfg = cfg = synth.CONFIGS["decode"]
+        self.name = name
+        self.cfg = cfg = synth.CONFIGS[name]
         self.L = layers or cfg.layers
         self.T = cfg.T
         self.dev = dev
@@ -260,19 +260,19 @@ class DecodeWorkload(Workload):
     # algorithmic work
     def bytes_per_step(self):
         cfg = self.cfg
-        return self.L * (cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared))
+        return self.L * (cfg.k * synth.ffn_bytes(cfg.d, cfg.I, cfg.bits) + synth.ffn_bytes(cfg.d, cfg.I_shared, cfg.bits))
 
     def dominant(self, peaks):
         cfg = self.cfg
-        per_launch = cfg.k * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared)
+        per_launch = cfg.k * synth.ffn_bytes(cfg.d, cfg.I, cfg.bits) + synth.ffn_bytes(cfg.d, cfg.I_shared, cfg.bits)
         return "decode", "hbm", per_launch, (
-            f"({cfg.k} routed + 1 shared) experts x (gate+up+down) 4-bit codes and bf16 scale/bias "
+            f"({cfg.k} routed + 1 shared) experts x (gate+up+down) {cfg.bits}-bit codes and bf16 scale/bias "
             f"= {per_launch} B per launch")
 
     def workload_desc(self):
         c = self.cfg
-        return (f"decode: T={c.T}, d={c.d}, E={c.E}, top-{c.k} + shared expert, I={c.I}; {self.L} distinct chained "
-                f"layers per step (CUDA graph); 4-bit codes + bf16 scale/bias per 64")
+        return (f"{self.name}: T={c.T}, d={c.d}, E={c.E}, top-{c.k} + shared expert, I={c.I}; {self.L} distinct "
+                f"chained layers per step (CUDA graph); {c.bits}-bit codes + bf16 scale/bias per 64")
 
     def cpu_sample(self, budget_s):
         """Oracle (routing + layer) on the host for the first layers until the budget is spent."""
@@ -887,8 +887,8 @@ def main():
             print(json.dumps(res), flush=True)
         dist.close()
         return
-    if args.workload == "decode":
-        wl = DecodeWorkload(dev, layers=args.layers or None)
+    if args.workload in ("decode", "decode2b"):
+        wl = DecodeWorkload(dev, layers=args.layers or None, name=args.workload)
     else:
         wl = PrefillWorkload(dev, args.workload, sets=args.layers or None)
     if args.only_graph:
