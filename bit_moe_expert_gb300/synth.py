@@ -16,6 +16,10 @@ Layout used throughout (row-major, all integers little-endian):
   scale  uint16 [E][N][K/64]  bf16 bit patterns
   bias   uint16 [E][N][K/64]  bf16 bit patterns
 gate and up are [E][I][d] (N=I, K=d); down is [E][d][I] (N=d, K=I).
+Low-bit variants keep the layout with b = 3 or 2 bits per code: q is
+[E][N][K*b/32], each row one bit stream with code k at bits b*k .. b*k+b-1
+(a 3-bit code may straddle two words); codes uniform on 0..2^b-1, scale ~
+U(0.004, 0.04) (b = 3) or U(0.008, 0.08) (b = 2), bias = -2^(b-1) * scale.
 
 Value distributions (synthetic stand-ins for the pages' workloads):
   X ~ N(0,1) rounded to bf16 (round to nearest even); router logits ~ N(0,1)
@@ -48,7 +52,7 @@ class LayerConfig:
     seed: int
     chunk: int = 0      # tokens per call when the prompt is processed in chunks (0 = T)
     zipf: bool = False  # skewed router logits
-    bits: int = 4       # bits per expert weight code (4 or 2)
+    bits: int = 4       # bits per expert weight code (4, 3 or 2)
 
     @property
     def tokens_per_call(self) -> int:
@@ -63,7 +67,8 @@ CONFIGS = {
     "prefill4096": LayerConfig("prefill4096", T=4096, d=2048, E=256, k=8, I=512, I_shared=512, layers=40,
                                seed=3, chunk=1024, zipf=True),
     "canvas": LayerConfig("canvas", T=256, d=2816, E=128, k=8, I=704, I_shared=0, layers=30, seed=4),
-    # the decode layer with 2-bit expert codes (the low-bit experts of the "next" steps)
+    # the decode layer with 3- and 2-bit expert codes (the low-bit experts of the "next" steps)
+    "decode3b": LayerConfig("decode3b", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=7, bits=3),
     "decode2b": LayerConfig("decode2b", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=6, bits=2),
 }
 
@@ -96,7 +101,7 @@ def _rng(seed: int, layer: int, tag: int) -> np.random.Generator:
 # Scale range and bias factor per code width: bias = -half the code range
 # times the scale (exact in bf16), so the weights are (q - 2^(bits-1)) * scale
 # and the 2-bit weights span about the same range as the 4-bit ones.
-SCALE_RANGE = {4: (0.002, 0.02), 2: (0.008, 0.08)}
+SCALE_RANGE = {4: (0.002, 0.02), 3: (0.004, 0.04), 2: (0.008, 0.08)}
 
 
 def draw_qmat(rng: np.random.Generator, E: int, N: int, K: int, bits: int = 4):

@@ -23,7 +23,7 @@ def code_bits(qsb) -> int:
     """Bits per code of a packed matrix (q [E][N][K*bits/32], scale [E][N][K/64])."""
     words, groups = qsb[0].shape[-1], qsb[1].shape[-1]
     bits = 32 * words // (64 * groups)
-    if bits not in (2, 4) or 32 * words != bits * 64 * groups:
+    if bits not in (2, 3, 4) or 32 * words != bits * 64 * groups:
         raise ValueError("codes and group parameters disagree on K")
     return bits
 

@@ -46,14 +46,18 @@ uint16_t oracle_double_to_bf16(double x) {
  * group of 64 weights shares a bf16 scale and bias; [Lily-news]: the compressed
  * values carry a scale and bias used to reconstruct them.  w = q*scale + bias.
  * [DGemma] "The physics ceiling: why 300+ tok/s is blocked" proposes the same
- * groupwise format with 2-3 bit codes; the 2-bit form here packs 16 codes per
- * word, low bits first along K, like the 4-bit one. */
+ * groupwise format with 2-3 bit codes; here 2- and 3-bit codes are packed like
+ * the 4-bit ones, low bits first along K. */
 double oracle_dequant(const oracle_qmat* m, int N, int K, int e, int n, int k) {
   const int bits = m->bits ? m->bits : 4;
-  const int per = 32 / bits; /* codes per word */
-  size_t row = (size_t)e * N + n;
-  uint32_t word = m->q[row * (size_t)(K / per) + k / per];
-  uint32_t code = (word >> (bits * (k % per))) & ((1u << bits) - 1u);
+  /* a row's codes are one bit stream, low bits first: code k starts at bit
+   * bits*k (K*bits/32 words per row; a 3-bit code may straddle two words) */
+  const size_t row = (size_t)e * N + n;
+  const uint32_t* words = m->q + row * (size_t)(K / 32 * bits);
+  const size_t bit = (size_t)bits * (size_t)k;
+  uint64_t window = words[bit / 32];
+  if (bit % 32 + (size_t)bits > 32) window |= (uint64_t)words[bit / 32 + 1] << 32;
+  const uint32_t code = (uint32_t)(window >> (bit % 32)) & ((1u << bits) - 1u);
   size_t g = row * (K / GROUP) + k / GROUP;
   return (double)code * oracle_bf16_to_double(m->scale[g]) + oracle_bf16_to_double(m->bias[g]);
 }

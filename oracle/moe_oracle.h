@@ -14,9 +14,11 @@
  *                for Qwen3.6-35B-A3B on Apple Silicon"
  *   [DGemma]     "Squeezing a 26B diffusion LLM onto a Mac"
  *
- * Weight layout (row-major, little-endian), b = bits per code (4 or 2):
- *   q     uint32 [E][N][K*b/32]  code for column k in bits b*(k%(32/b)) of
- *                                word k/(32/b) (b = 4: 4*(k%8) of word k/8)
+ * Weight layout (row-major, little-endian), b = bits per code (4, 3 or 2):
+ *   q     uint32 [E][N][K*b/32]  each row one bit stream, low bits first:
+ *                                the code of column k starts at bit b*k (b = 4:
+ *                                bits 4*(k%8) of word k/8; b = 3: a code may
+ *                                straddle two words)
  *   scale uint16 [E][N][K/64] bf16 bit patterns, one per 64-column group
  *   bias  uint16 [E][N][K/64] bf16 bit patterns
  * gate/up: N = I, K = d.  down: N = d, K = I.
@@ -34,7 +36,7 @@ typedef struct {
   const uint32_t* q;
   const uint16_t* scale;
   const uint16_t* bias;
-  int bits; /* bits per code: 4 or 2 (0 means 4) */
+  int bits; /* bits per code: 4, 3 or 2 (0 means 4) */
 } oracle_qmat;
 
 typedef struct {

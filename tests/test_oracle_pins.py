@@ -97,14 +97,17 @@ def test_dequant_special_cases(oracle):
 
 
 def _numpy_dequant(qsb, e):
-    """Independent vectorised dequantisation (NumPy bit operations); the code
-    width follows from the shapes (K*bits/32 words and K/64 groups per row)."""
+    """Independent vectorised dequantisation: each row's words unpacked into
+    its bit stream (np.unpackbits, least significant bit first), then read
+    `bits` bits per column; the code width follows from the shapes (K*bits/32
+    words and K/64 groups per row)."""
     q, s, b = qsb
     bits = 32 * q.shape[-1] // (64 * s.shape[-1])
-    per = 32 // bits
-    words = q[e].astype(np.uint64)
-    shifts = (bits * np.arange(per, dtype=np.uint64))[None, None, :]
-    codes = ((words[:, :, None] >> shifts) & ((1 << bits) - 1)).reshape(words.shape[0], -1).astype(np.float64)
+    N = q.shape[1]
+    stream = np.unpackbits(np.ascontiguousarray(q[e]).astype("<u4").view(np.uint8).reshape(N, -1), axis=1,
+                           bitorder="little")
+    weights = (1 << np.arange(bits)).astype(np.float64)
+    codes = stream.reshape(N, -1, bits).astype(np.float64) @ weights
     sc = np.repeat(synth.bf16_bits_to_f32(s[e]).astype(np.float64), 64, axis=1)
     bi = np.repeat(synth.bf16_bits_to_f32(b[e]).astype(np.float64), 64, axis=1)
     return codes * sc + bi
@@ -112,7 +115,7 @@ def _numpy_dequant(qsb, e):
 
 def test_dequant_matches_independent_numpy(oracle):
     rng = np.random.default_rng(2)
-    for bits in (4, 2):
+    for bits in (4, 3, 2):
         qsb = synth.draw_qmat(rng, 3, 16, 192, bits)
         for e in range(3):
             np.testing.assert_array_equal(oracle.dequant_matrix(qsb, e), _numpy_dequant(qsb, e))
@@ -145,6 +148,40 @@ def test_dequant_two_bit_special_cases(oracle):
     sc = synth.bf16_bits_to_f32(s[0]).astype(np.float64)
     np.testing.assert_array_equal(oracle.dequant_matrix((np.full_like(q, 0xFFFFFFFF), s, b), 0),
                                   np.repeat(sc, 64, axis=1))
+
+
+def test_dequant_three_bit_hand_worked_example(oracle):
+    # a row of 64 three-bit codes is 192 bits in 6 words, low bits first; code k starts at bit 3k, so
+    # code 10 (bits 30..32) and code 21 (bits 63..65) straddle words.  Codes: 7 at column 0, 5 at
+    # column 10, 6 at column 21, 3 at column 63, zero elsewhere; scale 0.25 and bias -1 give q / 4 - 1
+    words = np.zeros((1, 1, 6), np.uint32)
+    words[0, 0, 0] = 0x40000007   # bits 0..2 = 7; bit 30 = low bit of code 10
+    words[0, 0, 1] = 0x00000001   # bit 32 = top bit of code 10 (5 = 0b101); bit 63 (low bit of code 21) = 0
+    words[0, 0, 2] = 0x00000003   # bits 64, 65 = upper bits of code 21 (6 = 0b110)
+    words[0, 0, 5] = 0x60000000   # bits 189, 190 = code 63 (3 = 0b011)
+    s = np.full((1, 1, 1), 0x3E80, np.uint16)   # 0.25
+    b = np.full((1, 1, 1), 0xBF80, np.uint16)   # -1.0
+    qsb = (words, s, b)
+    want = {0: 0.75, 1: -1.0, 9: -1.0, 10: 0.25, 11: -1.0, 20: -1.0, 21: 0.5, 22: -1.0, 62: -1.0, 63: -0.25}
+    for k, v in want.items():
+        assert oracle.dequant(qsb, 0, 0, k) == v, k
+    row = oracle.dequant_matrix(qsb, 0)[0]
+    assert row.shape == (64,) and np.count_nonzero(row != -1.0) == 4
+
+
+def test_dequant_three_bit_special_cases(oracle):
+    rng = np.random.default_rng(4)
+    q, s, b = synth.draw_qmat(rng, 2, 8, 128, bits=3)
+    assert q.shape == (2, 8, 12)
+    bias = synth.bf16_bits_to_f32(b[1]).astype(np.float64)
+    np.testing.assert_array_equal(oracle.dequant_matrix((np.zeros_like(q), s, b), 1), np.repeat(bias, 64, axis=1))
+    # every code 4 (bit stream 001 repeated: the words cycle through 0x24924924, 0x49249249, 0x92492492)
+    # with bias = -4*scale gives exactly zero; every code 7 gives 3*scale
+    fours = np.tile(np.array([0x24924924, 0x49249249, 0x92492492], np.uint32), 4)
+    assert not np.any(oracle.dequant_matrix((np.broadcast_to(fours, q.shape).copy(), s, b), 0))
+    sc = synth.bf16_bits_to_f32(s[0]).astype(np.float64)
+    np.testing.assert_array_equal(oracle.dequant_matrix((np.full_like(q, 0xFFFFFFFF), s, b), 0),
+                                  np.repeat(3.0 * sc, 64, axis=1))
 
 
 # ---------------------------------------------------------------- top-k routing
@@ -460,7 +497,8 @@ def _dense_brute_force(layer, ids, w):
 
 @pytest.mark.parametrize("kw", [dict(), dict(T=9, E=8, k=3, I=64, I_shared=0, d=128),
                                 dict(T=5, E=4, k=4, I=64, I_shared=192, d=64),
-                                dict(T=7, E=6, k=2, I=128, I_shared=64, d=128, bits=2)])
+                                dict(T=7, E=6, k=2, I=128, I_shared=64, d=128, bits=2),
+                                dict(T=6, E=5, k=2, I=192, I_shared=64, d=128, bits=3)])
 def test_forward_matches_dense_brute_force(oracle, kw):
     cfg = synth.small_config(**kw)
     layer = synth.draw_layer(cfg)
