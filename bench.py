@@ -887,7 +887,7 @@ def main():
             print(json.dumps(res), flush=True)
         dist.close()
         return
-    if args.workload in ("decode", "decode2b"):
+    if args.workload in ("decode", "decode3b", "decode2b"):
         wl = DecodeWorkload(dev, layers=args.layers or None, name=args.workload)
     else:
         wl = PrefillWorkload(dev, args.workload, sets=args.layers or None)

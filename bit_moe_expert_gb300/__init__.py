@@ -363,7 +363,7 @@ def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
     """Device copy of one expert set in the kernels' format.
 
     ex maps "gate", "up", "down" to (q, scale, bias): q uint32/int32 [E][N][K*bits/32]
-    (4- or 2-bit codes, the width following from the shapes), scale and bias
+    (4-, 3- or 2-bit codes, the width following from the shapes), scale and bias
     uint16/int16 bf16 bits [E][N][K/64], as NumPy arrays or torch tensors.  Codes and group parameters are reordered once with
     moe_prepack_codes and moe_prepack_scales (a one-time layout change, like
     loading a checkpoint).
@@ -384,8 +384,8 @@ def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
         bd = dev(b, np.int16, torch.int16)
         E, N, G = sd.shape
         bits = 32 * int(qd.shape[2]) // (64 * G)
-        if bits not in (2, 4) or bits * 64 * G != 32 * int(qd.shape[2]):
-            raise ValueError(f"{name}: codes [E][N][{qd.shape[2]}] do not match {G} groups of 4- or 2-bit codes")
+        if bits not in (2, 3, 4) or bits * 64 * G != 32 * int(qd.shape[2]):
+            raise ValueError(f"{name}: codes [E][N][{qd.shape[2]}] do not match {G} groups of 4-, 3- or 2-bit codes")
         sb = torch.empty((E, G, N), dtype=torch.int32, device=device)
         moe_prepack_scales(sd, bd, sb, stream)
         qp = torch.empty((E, G, N, 2 * bits), dtype=torch.int32, device=device)

@@ -64,6 +64,18 @@ bool encode_codes_rows(CUtensorMap* map, const uint32_t* q, int E, int N, int K,
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// 3-bit codes q [E][K/64][N][6] uint32 seen as [E*K/64][N*3] 8-byte units:
+// a row's 24 bytes are three units, so a box of box_rows rows (box_rows*3
+// units, at most 256) starts on a 16-byte boundary whenever its first row is
+// even; rows past N read as zeros
+bool encode_codes3(CUtensorMap* map, const uint32_t* q, int E, int N, int K, cuuint32_t box_rows) {
+  const int G = K / 64;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N) * 3, static_cast<cuuint64_t>(E) * G};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 24};
+  const cuuint32_t box[2] = {box_rows * 3, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // fp16 activations [rows][cols]: boxes of 64 columns (128 bytes) x kGemmBN
 // rows, 128-byte swizzle (the K-major operand layout of the tensor cores)
 bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols) {
@@ -140,10 +152,10 @@ bool qmat_ok(const moe_qmat& m) { return m.q && m.sb && aligned16(m.q) && aligne
 
 bool experts_ok(const moe_experts* ex) {
   return ex && qmat_ok(ex->gate) && qmat_ok(ex->up) && qmat_ok(ex->down) && ex->n_experts >= 1 &&
-         (ex->bits == 0 || ex->bits == 4 || ex->bits == 2);
+         (ex->bits == 0 || (ex->bits >= 2 && ex->bits <= 4));
 }
 
-int code_bits(const moe_experts* ex) { return ex->bits == 2 ? 2 : 4; }
+int code_bits(const moe_experts* ex) { return ex->bits == 0 ? 4 : ex->bits; }
 
 }  // namespace
 
@@ -178,7 +190,7 @@ moe_status moe_prepack_codes_bits(const uint32_t* q, int E, int N, int K, int bi
                                   moe_stream stream) {
   if (!q || !qp || E < 1 || N < 1 || K < 64 || K % 64 != 0 || !aligned16(q) || !aligned16(qp))
     return MOE_ERR_INVALID_ARG;
-  if (bits != 4 && bits != 2) return MOE_ERR_INVALID_ARG;
+  if (bits < 2 || bits > 4) return MOE_ERR_INVALID_ARG;
   if (launch_prepack_codes(q, E, N, K, bits, qp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -365,24 +377,29 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
   if (r->block_rows < 1 || r->block_rows > kGemmBN) return MOE_ERR_UNSUPPORTED;
   const int A = T * k;
   // a row's codes of one group: 32 bytes (4-bit) read through a 32-byte
-  // swizzle, or 16 bytes (2-bit), already conflict-free
+  // swizzle, or 16 bytes (2-bit), already conflict-free; 24 bytes (3-bit) in
+  // two boxes of 64 rows, read as 8-byte units (conflict-free too)
   const CUtensorMapSwizzle code_swizzle = bits == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  auto enc_q = [&](CUtensorMap* map, const uint32_t* q, int ne, int N, int K) {
+    return bits == 3 ? encode_codes3(map, q, ne, N, K, kGemmBM / 2)
+                     : encode_codes(map, q, ne, N, K, kGemmBM, 1, code_swizzle, wpg);
+  };
   GemmMaps mr, ms;
   GemmActMaps act;
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
   uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
-  bool ok = encode_codes(&mr.q_gate, routed->gate.q, E, I, d, kGemmBM, 1, code_swizzle, wpg) &&
-            encode_codes(&mr.q_up, routed->up.q, E, I, d, kGemmBM, 1, code_swizzle, wpg) &&
-            encode_codes(&mr.q_down, routed->down.q, E, d, I, kGemmBM, 1, code_swizzle, wpg) &&
+  bool ok = enc_q(&mr.q_gate, routed->gate.q, E, I, d) &&
+            enc_q(&mr.q_up, routed->up.q, E, I, d) &&
+            enc_q(&mr.q_down, routed->down.q, E, d, I) &&
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
             encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
             encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
   if (ok && shared)
-    ok = encode_codes(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmBM, 1, code_swizzle, wpg) &&
-         encode_codes(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmBM, 1, code_swizzle, wpg) &&
-         encode_codes(&ms.q_down, shared->down.q, 1, d, I_shared, kGemmBM, 1, code_swizzle, wpg) &&
+    ok = enc_q(&ms.q_gate, shared->gate.q, 1, I_shared, d) &&
+         enc_q(&ms.q_up, shared->up.q, 1, I_shared, d) &&
+         enc_q(&ms.q_down, shared->down.q, 1, d, I_shared) &&
          encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
          encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&

@@ -59,7 +59,7 @@ constexpr int kS1 = 5;                          // phase-1 stages
 constexpr int kSB1 = kS1;                       // phase-1 group-parameter buffers: one per stage
 constexpr int kS2Max = 12;                      // phase-2 stages at most
 constexpr int kMaxSlots = kMaxK * kGemvMaxT + 1;  // distinct experts of a call, plus the shared one
-// kBits bits per weight code (4 or 2): code words per row and 64-column group
+// kBits bits per weight code (4, 3 or 2): code words per row and 64-column group
 template <int kBits>
 constexpr int kWpg = 2 * kBits;
 template <int kBits>
@@ -145,10 +145,17 @@ __host__ __device__ inline Layout layout(int T, int d, int I, int I_shared, int 
 
 // Four MMA steps over one 64-column group (see the K order above).
 //   wa, wb: the codes of columns 16q .. 16q+15 of rows g and g+8 (4-bit
-//   codes: words 2q, 2q+1; 2-bit codes: word q, in .x); b: the activation
+//   codes: words 2q, 2q+1; 2-bit codes: word q, in .x; 3-bit codes: the
+//   low-bit word q in .x, the high-bit word shifted so that the pair
+//   (2p, 2p+1)'s high bits sit at bits p and p+16, in .y); b: the activation
 //   operand of the four steps (the same columns, token g).  Step m takes
 //   columns 16q + 4m .. 16q + 4m + 3: two pairs of adjacent codes, each
-//   formed by one mask from the interleaved word.
+//   formed by one mask from the interleaved word (3-bit codes: a second
+//   mask adds the high bits as bit 2 of each half).
+// x moved so that its bits P and P+16 land at bits 2 and 18 (P a constant
+// once the caller's loop is unrolled)
+__device__ __forceinline__ uint32_t shift_to_bit2(uint32_t x, int P) { return P < 2 ? x << (2 - P) : x >> (P - 2); }
+
 template <bool kBF16, int kBits>
 __device__ __forceinline__ void mma_group(uint2 wa, uint2 wb, const uint32_t (&b)[8], float (&dd)[4]) {
   constexpr uint32_t magic = kBF16 ? 0x43004300u : 0x64006400u;  // pairs (128, 128) / (1024, 1024)
@@ -168,16 +175,24 @@ __device__ __forceinline__ void mma_group(uint2 wa, uint2 wb, const uint32_t (&b
       a1 = lop3_and_or(wb.x >> (4 * m), 0x00030003u, magic);
       a2 = lop3_and_or(wa.x >> (4 * m + 2), 0x00030003u, magic);  // code pair 2m + 1
       a3 = lop3_and_or(wb.x >> (4 * m + 2), 0x00030003u, magic);
+      if constexpr (kBits == 3) {  // high bits of pair P at bits P, P+16 -> bits 2, 18
+        a0 = lop3_and_or(shift_to_bit2(wa.y, 2 * m), 0x00040004u, a0);
+        a1 = lop3_and_or(shift_to_bit2(wb.y, 2 * m), 0x00040004u, a1);
+        a2 = lop3_and_or(shift_to_bit2(wa.y, 2 * m + 1), 0x00040004u, a2);
+        a3 = lop3_and_or(shift_to_bit2(wb.y, 2 * m + 1), 0x00040004u, a3);
+      }
     }
     mma_16816<kBF16>(dd, a0, a1, a2, a3, b[2 * m], b[2 * m + 1]);
   }
 }
 
 // The codes of columns 16q .. 16q+15 of one row: 4-bit codes, two words;
-// 2-bit codes, one word (in .x).
+// 2-bit codes, one word (in .x); 3-bit codes, low-bit word q and high-bit
+// word 4 + q/2 shifted down by 8(q&1).
 template <int kBits>
 __device__ __forceinline__ uint2 load_codes(const uint32_t* row, int q) {
   if constexpr (kBits == 4) return *reinterpret_cast<const uint2*>(row + 2 * q);
+  if constexpr (kBits == 3) return make_uint2(row[q], row[4 + (q >> 1)] >> (8 * (q & 1)));
   return make_uint2(row[q], 0u);
 }
 
@@ -969,11 +984,22 @@ size_t decode_scratch_bytes(int T, int I, int I_shared) {
   return static_cast<size_t>(kMaxSlots) * (static_cast<size_t>(T) * Imax * 2 + static_cast<size_t>(T) * hs * 4);
 }
 
+template <int kBits>
+cudaError_t launch_bits(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
+                        size_t smem, cudaStream_t stream, bool pdl) {
+  switch (a.T) {
+    case 1: return launch_t<1, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
+    case 2: return launch_t<2, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
+    case 3: return launch_t<3, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
+    default: return launch_t<4, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
+  }
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
                           cudaStream_t stream, bool pdl) {
   if (!decode_supported(a.T, a.d, a.I, a.I_shared, a.k)) return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(a.hbuf) & 15u) return cudaErrorInvalidValue;
-  if (a.bits != 4 && a.bits != 2) return cudaErrorInvalidValue;
+  if (a.bits < 2 || a.bits > 4) return cudaErrorInvalidValue;
   const Layout L = layout(a.T, a.d, a.I, a.I_shared, a.bits);
   const DecodeMaps* sh = shared ? shared : routed;  // never read without a shared expert
   const int distinct = a.T * a.k < a.E ? a.T * a.k : a.E;
@@ -985,21 +1011,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const D
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   timer_begin(kKDecode, stream);
   cudaError_t err;
-  if (a.bits == 2) {
-    switch (a.T) {
-      case 1: err = launch_t<1, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      case 2: err = launch_t<2, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      case 3: err = launch_t<3, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      default: err = launch_t<4, 2>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-    }
-  } else {
-    switch (a.T) {
-      case 1: err = launch_t<1, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      case 2: err = launch_t<2, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      case 3: err = launch_t<3, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-      default: err = launch_t<4, 4>(a, routed, sh, hdr, want, L.total, stream, pdl); break;
-    }
-  }
+  if (a.bits == 2)
+    err = launch_bits<2>(a, routed, sh, hdr, want, L.total, stream, pdl);
+  else if (a.bits == 3)
+    err = launch_bits<3>(a, routed, sh, hdr, want, L.total, stream, pdl);
+  else
+    err = launch_bits<4>(a, routed, sh, hdr, want, L.total, stream, pdl);
   timer_end(kKDecode, stream);
   return err;
 }

@@ -67,7 +67,8 @@ struct Cfg {
   // and A-stage rings must then agree on parity
   static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "stage rings must have even length");
   static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to kGemmBN rows x 64 fp16 (128-byte swizzle)
-  // 128 rows x (2 kBits) code words: 4-bit codes with a 32-byte swizzle, 2-bit codes (16 bytes a row) plain
+  // 128 rows x (2 kBits) code words: 4-bit codes with a 32-byte swizzle, 2- and 3-bit codes (16 or 24
+  // bytes a row) plain
   static constexpr int kQBytes = kGemmBM * 8 * kBits;
   static constexpr int kSBBytes = kGemmBM * 4;
   static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
@@ -158,6 +159,33 @@ __device__ __forceinline__ void dequant_word2(uint32_t w, uint32_t s2, uint32_t 
   }
 }
 
+// Sixteen 3-bit codes of one 16-column block (lo: its low two bits in the
+// 2-bit interleaved order; hi: its high bits, pair p's at bits p and p+16)
+// -> eight f16x2 values of q*scale + bias.  The masks leave the f16 pairs
+// 1024 + 4^pp lo (pair p in place in lo, or in lo >> 10: pp = p or p - 5) and
+// 1024 + 2^p hi; the first FMA turns the second into 4 hi - 1024 4^-pp, the
+// second adds lo + 1024 4^-pp, so q = lo + 4 hi comes out exactly (every
+// intermediate is an integer or a short binary fraction below 2048), and the
+// third applies scale and bias.
+__device__ __forceinline__ void dequant_word3(uint32_t lo, uint32_t hi, uint32_t s2, uint32_t b2, uint32_t* out) {
+  const uint32_t magic = 0x64006400u;  // f16 pair (1024, 1024)
+  constexpr uint32_t kScale[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};  // 4^-pp
+  // f16 pairs (4 * 2^-p, ...) and (-(4096 * 2^-p + 1024 * 4^-pp), ...) for p = 0..7
+  constexpr uint32_t kHiScale[8] = {0x44004400u, 0x40004000u, 0x3C003C00u, 0x38003800u,
+                                    0x34003400u, 0x30003000u, 0x2C002C00u, 0x28002800u};
+  constexpr uint32_t kHiShift[8] = {0xED00ED00u, 0xE880E880u, 0xE440E440u, 0xE020E020u,
+                                    0xDC10DC10u, 0xE480E480u, 0xDD00DD00u, 0xD600D600u};
+  const uint32_t lo10 = lo >> 10;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int pp = p < 5 ? p : p - 5;
+    const uint32_t vl = lop3_and_or(p < 5 ? lo : lo10, 0x00030003u << (2 * pp), magic);
+    const uint32_t vh = lop3_and_or(hi, 0x00010001u << p, magic);
+    const uint32_t t = f16x2_fma(vh, kHiScale[p], kHiShift[p]);
+    out[p] = f16x2_fma(f16x2_fma(vl, kScale[pp], t), s2, b2);
+  }
+}
+
 template <bool kGateUp, int kBits>
 __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap q0_r, const __grid_constant__ CUtensorMap q1_r,
@@ -234,6 +262,15 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
   s.n_routed = s.nb * s.mt_r;
   s.n_total = s.n_routed + s.nsb * s.mt_s;
 
+  // one k-block's codes of one 128-row tile: 4- and 2-bit codes one 3-D box;
+  // 3-bit codes (24 bytes a row, a line of 8-byte units [E*K/64][N*3]) two
+  // boxes of 64 rows, `half` choosing one
+  auto load_codes = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int mt, int eg, int half) {
+    if constexpr (kBits == 3)
+      tma_load_2d(dst + half * (C::kQBytes / 2), map, bar, (mt * kGemmBM + half * (kGemmBM / 2)) * 3, eg);
+    else
+      tma_load_3d(dst, map, bar, 0, mt * kGemmBM, eg);
+  };
   auto fail = [&]() {
     record_status(a.status, MOE_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -267,13 +304,18 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
           uint8_t* st = stages + stage * C::kStageBytes;
           uint8_t* q_tile = st + C::kBBytes;
           uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
+          const int eg = m.e * m.nk + kb;
           mbar_arrive_expect_tx(&full[stage], C::kStageTxBytes);
           tma_load_2d(st, mb, &full[stage], kb * 64, brow);
-          tma_load_3d(q_tile, mq0, &full[stage], 0, m.mt * kGemmBM, m.e * m.nk + kb);
+          load_codes(q_tile, mq0, &full[stage], m.mt, eg, 0);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
-            tma_load_3d(q_tile + C::kQBytes, mq1, &full[stage], 0, m.mt * kGemmBM, m.e * m.nk + kb);
+            load_codes(q_tile + C::kQBytes, mq1, &full[stage], m.mt, eg, 0);
             tma_load_3d(sb_tile + C::kSBBytes, msb1, &full[stage], m.mt * kGemmBM, kb, m.e);
+          }
+          if (kBits == 3) {
+            load_codes(q_tile, mq0, &full[stage], m.mt, eg, 1);
+            if (kGateUp) load_codes(q_tile + C::kQBytes, mq1, &full[stage], m.mt, eg, 1);
           }
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -414,6 +456,18 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
             dequant_word(w.w, s2, b2, v + 12);
             tmem_st16(taddr + mat * 32 + h * 16, v);
           }
+        } else if constexpr (kBits == 3) {
+          // the row's 24 code bytes: low-bit words j = 0..3 (columns 16j .. 16j+15), then the high-bit
+          // words of blocks 0, 1 and 2, 3 (block 2i+1 in the upper byte of each half)
+          const uint2* rp = reinterpret_cast<const uint2*>(q_tile + row * 24);
+          const uint2 l01 = rp[0], l23 = rp[1], hh = rp[2];
+          uint32_t v[16];
+          dequant_word3(l01.x, hh.x, s2, b2, v + 0);
+          dequant_word3(l01.y, hh.x >> 8, s2, b2, v + 8);
+          tmem_st16(taddr + mat * 32, v);
+          dequant_word3(l23.x, hh.y, s2, b2, v + 0);
+          dequant_word3(l23.y, hh.y >> 8, s2, b2, v + 8);
+          tmem_st16(taddr + mat * 32 + 16, v);
         } else {
           // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
           const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
@@ -720,6 +774,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, const GemmMaps* routed, const GemmM
 cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,
                         cudaStream_t stream, bool pdl) {
   if (a.bits == 2) return launch_gemm_t<2>(a, routed, shared, act, stream, pdl);
+  if (a.bits == 3) return launch_gemm_t<3>(a, routed, shared, act, stream, pdl);
   if (a.bits == 4) return launch_gemm_t<4>(a, routed, shared, act, stream, pdl);
   return cudaErrorInvalidValue;
 }

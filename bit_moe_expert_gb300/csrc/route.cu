@@ -450,6 +450,50 @@ __device__ __forceinline__ uint4 interleave_pairs2(uint4 v) {
   return make_uint4(interleave_pairs2(v.x), interleave_pairs2(v.y), interleave_pairs2(v.z), interleave_pairs2(v.w));
 }
 
+// 3-bit codes: one row's 64 codes of a group (192 bits, code c at bits 3c of
+// the six words) -> two planes in the same six words.  Words 0..3: the low
+// two bits in the 2-bit interleaved order (word j = columns 16j .. 16j+15,
+// column 16j+2p+h at bits 2p+16h).  Words 4, 5: the high bits, column
+// 16j+2p+h at bit 16h + 8(j&1) + p of word 4 + j/2, so that the high bits of
+// the code pair (2p, 2p+1) of 16-column block j sit p bits above bit 0 and
+// bit 16 once the word is shifted right by 8(j&1).
+__device__ __forceinline__ void repack3(const uint32_t (&in)[6], uint32_t (&out)[6]) {
+#pragma unroll
+  for (int i = 0; i < 6; ++i) out[i] = 0u;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    const int bit = 3 * c, wi = bit >> 5, sh = bit & 31;
+    uint32_t code = in[wi] >> sh;
+    if (sh > 29) code |= in[wi + 1] << (32 - sh);
+    code &= 7u;
+    const int j = c >> 4, p = (c & 15) >> 1, h = c & 1;
+    out[j] |= (code & 3u) << (2 * p + 16 * h);
+    out[4 + (j >> 1)] |= (code >> 2) << (16 * h + 8 * (j & 1) + p);
+  }
+}
+
+__global__ void prepack_codes3_kernel(const uint2* __restrict__ q, int E, int N, int G, uint2* __restrict__ qp) {
+  const size_t total = static_cast<size_t>(E) * G * N;
+  for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
+       o += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int n = static_cast<int>(o % N);
+    const size_t eg = o / N;
+    const int g = static_cast<int>(eg % G);
+    const int e = static_cast<int>(eg / G);
+    const size_t i = (static_cast<size_t>(e) * N + n) * G + g;  // the piece's 24 bytes: three 8-byte units
+    uint32_t in[6], out[6];
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const uint2 v = q[3 * i + u];
+      in[2 * u] = v.x;
+      in[2 * u + 1] = v.y;
+    }
+    repack3(in, out);
+#pragma unroll
+    for (int u = 0; u < 3; ++u) qp[3 * o + u] = make_uint2(out[2 * u], out[2 * u + 1]);
+  }
+}
+
 // one row's piece of one group: 32 bytes (4-bit codes) or 16 bytes (2-bit)
 template <int kBits>
 __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, int G, uint4* __restrict__ qp) {
@@ -477,7 +521,10 @@ cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, int bit
   const size_t blocks = (total + threads - 1) / threads;
   const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
   timer_begin(kKPrepack, stream);
-  if (bits == 2)
+  if (bits == 3)
+    prepack_codes3_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint2*>(q), E, N, G,
+                                                        reinterpret_cast<uint2*>(qp));
+  else if (bits == 2)
     prepack_codes_kernel<2><<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(q), E, N, G,
                                                           reinterpret_cast<uint4*>(qp));
   else

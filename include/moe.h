@@ -61,7 +61,7 @@ const char* moe_status_string(moe_status s);
 
 /* ------------------------------------------------------------------ weights
  * One stacked packed matrix of E experts with N rows and K columns (K a
- * multiple of 64), b = 4 or 2 bits per code:
+ * multiple of 64), b = 4, 3 or 2 bits per code:
  *   q   uint32 [E][K/64][N][2b]  the codes, group-major: the 2b words of row
  *                            n, columns 64g .. 64g+63 sit at [e][g][n][..];
  *                            inside a word the codes are interleaved so that
@@ -71,11 +71,16 @@ const char* moe_status_string(moe_status s);
  *                            column 8j+2p+1 in bits 4p+16 (p = 0..3); with
  *                            2-bit codes the code of column 16j+2p sits in
  *                            bits 2p and that of column 16j+2p+1 in bits
- *                            2p+16 (p = 0..7).  Build it once per weight set
- *                            with moe_prepack_codes (4-bit) or
- *                            moe_prepack_codes_bits from the row-major
- *                            [E][N][K*b/32] checkpoint layout (low bits
- *                            first along K);
+ *                            2p+16 (p = 0..7).  3-bit codes are two planes
+ *                            in the row's six words: words 0..3 hold the low
+ *                            two bits exactly as 2-bit codes, and the high
+ *                            bit of column 16j+2p+h (h = 0, 1) sits in bit
+ *                            16h + 8(j%2) + p of word 4 + j/2.  Build it once
+ *                            per weight set with moe_prepack_codes (4-bit)
+ *                            or moe_prepack_codes_bits from the row-major
+ *                            [E][N][K*b/32] checkpoint layout (each row one
+ *                            bit stream, code k at bits b*k .. b*k+b-1, so a
+ *                            3-bit code may straddle two words);
  *   sb  uint32 [E][K/64][N]  the group parameters, transposed so one group of
  *                            many rows is contiguous: bits 0..15 hold the bf16
  *                            scale and bits 16..31 the bf16 bias of rows n,
@@ -94,8 +99,8 @@ typedef struct {
   moe_qmat up;
   moe_qmat down;
   int n_experts;
-  int bits; /* bits per code of all three matrices: 4 (or 0) or 2; a shared
-               expert has the routed experts' width */
+  int bits; /* bits per code of all three matrices: 4 (or 0), 3 or 2; a
+               shared expert has the routed experts' width */
 } moe_experts;
 
 /* Bytes of the sb array for E experts of an N x K matrix: E * (K/64) * N * 4. */
@@ -112,9 +117,10 @@ size_t moe_prepack_bytes(int E, int N, int K);
  * size or pointer. */
 moe_status moe_prepack_codes(const uint32_t* q, int E, int N, int K, uint32_t* qp, moe_stream stream);
 
-/* moe_prepack_codes for b = `bits` bits per code (4 or 2): q [E][N][K*b/32]
- * -> qp [E][K/64][N][2b], the codes of each word interleaved (see above);
- * E*N*K*b/8 bytes.  MOE_ERR_INVALID_ARG for any other width. */
+/* moe_prepack_codes for b = `bits` bits per code (4, 3 or 2): q
+ * [E][N][K*b/32] -> qp [E][K/64][N][2b], the codes of each word interleaved
+ * (3-bit codes split into planes; see above); E*N*K*b/8 bytes.
+ * MOE_ERR_INVALID_ARG for any other width. */
 moe_status moe_prepack_codes_bits(const uint32_t* q, int E, int N, int K, int bits, uint32_t* qp,
                                   moe_stream stream);
 
