@@ -396,7 +396,8 @@ class PrefillWorkload(Workload):
         flops = self.chunk * (cfg.k * 4 * cfg.d * cfg.I + 4 * cfg.d * cfg.I_shared)
         n_act = self.active_experts()
         # gate and up are two of the three equally sized matrices of an expert
-        nbytes = (2 * n_act * synth.ffn_bytes(cfg.d, cfg.I) + 2 * synth.ffn_bytes(cfg.d, cfg.I_shared)) // 3
+        nbytes = (2 * n_act * synth.ffn_bytes(cfg.d, cfg.I, cfg.bits)
+                  + 2 * synth.ffn_bytes(cfg.d, cfg.I_shared, cfg.bits)) // 3
         ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
         if flops / nbytes > ridge:
             return "gemm_gateup", "tensor", flops, (
@@ -405,7 +406,7 @@ class PrefillWorkload(Workload):
                 f"ridge {ridge:.0f})")
         return "gemm_gateup", "hbm", nbytes, (
             f"gate and up matrices of the {n_act} active experts{' + shared' if cfg.I_shared else ''} "
-            f"(4-bit codes, bf16 scale/bias) = {nbytes} B per launch ({flops / nbytes:.0f} FLOP per weight byte, "
+            f"({cfg.bits}-bit codes, bf16 scale/bias) = {nbytes} B per launch ({flops / nbytes:.0f} FLOP per weight byte, "
             f"ridge {ridge:.0f})")
 
     def workload_desc(self):
@@ -413,7 +414,7 @@ class PrefillWorkload(Workload):
         return (f"{self.name}: T={c.T} as {self.nchunks} chunk(s) of {self.chunk}, d={c.d}, E={c.E}, top-{c.k}"
                 f"{' + shared' if c.I_shared else ''}, I={c.I}{', Zipf-skewed routing' if c.zipf else ''}; "
                 f"chunk c uses weight set c ({self.sets} sets x "
-                f"{(c.E * synth.ffn_bytes(c.d, c.I)) / 1e6:.0f} MB)")
+                f"{(c.E * synth.ffn_bytes(c.d, c.I, c.bits)) / 1e6:.0f} MB, {c.bits}-bit codes)")
 
     def cpu_sample(self, budget_s):
         import oracle
@@ -554,7 +555,8 @@ def run_workload(wl, args, dist, peaks, clocks):
         if bound == "hbm":
             cfg = wl.cfg
             n_act = wl.active_experts()
-            wbytes = wl.nchunks * (n_act * synth.ffn_bytes(cfg.d, cfg.I) + synth.ffn_bytes(cfg.d, cfg.I_shared))
+            wbytes = wl.nchunks * (n_act * synth.ffn_bytes(cfg.d, cfg.I, cfg.bits)
+                                   + synth.ffn_bytes(cfg.d, cfg.I_shared, cfg.bits))
             gbs = wbytes / t_step / 1e9
             out["step_roofline"] = {"bound": "hbm", "weight_bytes_per_step": wbytes, "achieved": gbs,
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
@@ -570,10 +572,12 @@ def run_workload(wl, args, dist, peaks, clocks):
 # reports null.
 _CSRC = os.path.join(ROOT, "bit_moe_expert_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    # profiles/prefill4096_chunk_kernels.md: 87.335680 MB read + 2.643456 MB written
-    "prefill4096/gemm_gateup": (89_979_136, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "b0fe617b051c5ef2"),
+    # profiles/prefill4096_chunk_kernels.md: 87.344384 MB read + 2.607872 MB written
+    "prefill4096/gemm_gateup": (89_952_256, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "0ff914f5b9c1ae3a"),
     # profiles/decode_kernel_decode.md: median of five launches, 16,030,720 B read, 0 written
-    "decode/decode": (16_030_720, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "67b88330edd3e521"),
+    "decode/decode": (16_030_720, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "701771da065854f2"),
+    # profiles/decode_kernel_decode.md (3-bit codes): median of five launches, 12,494,080 B read, 0 written
+    "decode3b/decode": (12_494_080, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "701771da065854f2"),
 }
 
 
@@ -689,7 +693,8 @@ def run_sweep(dev, peaks, args):
         t_call = e0.elapsed_time(e1) / steps / 1e3
         counts = r.counts.cpu().numpy()
         n_act = int((counts > 0).sum())
-        wbytes = n_act * synth.ffn_bytes(cfg.d, cfg.I) + (synth.ffn_bytes(cfg.d, cfg.I_shared) if cfg.I_shared else 0)
+        wbytes = n_act * synth.ffn_bytes(cfg.d, cfg.I, cfg.bits) + (synth.ffn_bytes(cfg.d, cfg.I_shared, cfg.bits)
+                                                                     if cfg.I_shared else 0)
         flops = 6 * T * cfg.d * (cfg.k * cfg.I + cfg.I_shared)
         return {"T": T, "active_experts": n_act, "rows_per_expert_max": int(counts.max()),
                 "us_per_call": t_call * 1e6, "weight_bytes": wbytes, "gbs": wbytes / t_call / 1e9,

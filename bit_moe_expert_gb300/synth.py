@@ -59,7 +59,7 @@ class LayerConfig:
         return self.chunk if self.chunk else self.T
 
 
-# The five synthetic workloads.
+# The synthetic workloads: the five of the 4-bit layer, then low-bit variants.
 CONFIGS = {
     "tiny": LayerConfig("tiny", T=16, d=256, E=16, k=2, I=128, I_shared=128, layers=1, seed=0),
     "decode": LayerConfig("decode", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=1),
@@ -70,6 +70,12 @@ CONFIGS = {
     # the decode layer with 3- and 2-bit expert codes (the low-bit experts of the "next" steps)
     "decode3b": LayerConfig("decode3b", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=7, bits=3),
     "decode2b": LayerConfig("decode2b", T=1, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=6, bits=2),
+    # the 512-token prefill layer (every expert active, the tensor-core path bound by the weight stream)
+    # with 3- and 2-bit expert codes
+    "prefill512b3": LayerConfig("prefill512b3", T=512, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=8,
+                                bits=3),
+    "prefill512b2": LayerConfig("prefill512b2", T=512, d=2048, E=256, k=8, I=512, I_shared=512, layers=40, seed=9,
+                                bits=2),
 }
 
 
