@@ -230,12 +230,16 @@ class DecodeWorkload(Workload):
         self.ws = bm.workspace(bm.moe_layer_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
         self.Y = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16, device=dev)
         self.tokens_per_step = self.L * self.T
-        # pinned host buffers for the end-to-end measurement
-        self.X_pin = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in self.X_host]
-        self.lg_pin = [torch.from_numpy(x).pin_memory() for x in self.logits_host]
+        # pinned host buffers for the end-to-end measurement: the step's inputs (every layer's X and
+        # logits) and its result (every layer's Y), each moved in one copy per step
+        self.X_pin = torch.from_numpy(np.stack([x.view(np.int16) for x in self.X_host])).pin_memory()
+        self.lg_pin = torch.from_numpy(np.stack(self.logits_host)).pin_memory()
         self.Y_pin = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16).pin_memory()
-        self.X_e2e = torch.empty_like(self.X[0])
-        self.lg_e2e = torch.empty_like(self.logits[0])
+        self.X_e2e = torch.empty(self.X_pin.shape, dtype=torch.int16, device=dev)
+        self.lg_e2e = torch.empty(self.lg_pin.shape, dtype=torch.float32, device=dev)
+        self.X_e2e_l = [self.X_e2e[l] for l in range(self.L)]
+        self.lg_e2e_l = [self.lg_e2e[l] for l in range(self.L)]
+        self.Y_l = [self.Y[l] for l in range(self.L)]
         self.h2d_bytes = self.L * (self.X_host[0].nbytes + self.logits_host[0].nbytes)
         self.d2h_bytes = self.L * self.T * cfg.d * 2
 
@@ -246,16 +250,16 @@ class DecodeWorkload(Workload):
         bm, cfg = self.bm, self.cfg
         for l in range(self.L):
             bm.moe_layer(self.logits[l], self.X[l], self.routed[l], self.shared[l], cfg.k, self.block_rows, self.r,
-                         self.Y[l], self.ws)
+                         self.Y_l[l], self.ws)
 
     def e2e_step(self):
         bm, cfg = self.bm, self.cfg
+        self.X_e2e.copy_(self.X_pin, non_blocking=True)
+        self.lg_e2e.copy_(self.lg_pin, non_blocking=True)
         for l in range(self.L):
-            self.X_e2e.copy_(self.X_pin[l], non_blocking=True)
-            self.lg_e2e.copy_(self.lg_pin[l], non_blocking=True)
-            bm.moe_layer(self.lg_e2e, self.X_e2e, self.routed[l], self.shared[l], cfg.k, self.block_rows, self.r,
-                         self.Y[l], self.ws)
-            self.Y_pin[l].copy_(self.Y[l], non_blocking=True)
+            bm.moe_layer(self.lg_e2e_l[l], self.X_e2e_l[l], self.routed[l], self.shared[l], cfg.k, self.block_rows,
+                         self.r, self.Y_l[l], self.ws)
+        self.Y_pin.copy_(self.Y, non_blocking=True)
 
     # algorithmic work
     def bytes_per_step(self):
@@ -344,11 +348,14 @@ class PrefillWorkload(Workload):
         self.ws_f = bm.workspace(bm.moe_forward_workspace_bytes(C, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
         self.Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
         self.tokens_per_step = cfg.T
+        # pinned host buffers for the end-to-end measurement: the prompt's X and each chunk's logits (from
+        # the chunk's weight set) in one copy each per step, Y in one copy
         self.X_pin = torch.from_numpy(self.X_host.view(np.int16)).pin_memory()
-        self.lg_pin = [torch.from_numpy(x).pin_memory() for x in self.logits_host]
+        self.lg_pin = torch.from_numpy(np.concatenate(
+            [self.logits_host[self._set(c)][c * C:(c + 1) * C] for c in range(self.nchunks)])).pin_memory()
         self.Y_pin = torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory()
-        self.X_e2e = torch.empty((C, cfg.d), dtype=torch.int16, device=dev)
-        self.lg_e2e = torch.empty((C, cfg.E), dtype=torch.float32, device=dev)
+        self.X_e2e = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
+        self.lg_e2e = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=dev)
         self.h2d_bytes = self.X_host.nbytes + self.nchunks * C * cfg.E * 4
         self.d2h_bytes = cfg.T * cfg.d * 2
         self._flops = None
@@ -369,13 +376,14 @@ class PrefillWorkload(Workload):
 
     def e2e_step(self):
         bm, cfg, C = self.bm, self.cfg, self.chunk
+        self.X_e2e.copy_(self.X_pin, non_blocking=True)
+        self.lg_e2e.copy_(self.lg_pin, non_blocking=True)
         for c in range(self.nchunks):
             s = self._set(c)
-            self.X_e2e.copy_(self.X_pin[c * C:(c + 1) * C], non_blocking=True)
-            self.lg_e2e.copy_(self.lg_pin[s][c * C:(c + 1) * C], non_blocking=True)
-            bm.moe_route(self.lg_e2e, cfg.k, self.block_rows, self.r, self.ws_r)
-            bm.moe_forward(self.X_e2e, self.routed[s], self.shared[s], self.r, self.Y[c * C:(c + 1) * C], self.ws_f)
-            self.Y_pin[c * C:(c + 1) * C].copy_(self.Y[c * C:(c + 1) * C], non_blocking=True)
+            bm.moe_route(self.lg_e2e[c * C:(c + 1) * C], cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X_e2e[c * C:(c + 1) * C], self.routed[s], self.shared[s], self.r,
+                           self.Y[c * C:(c + 1) * C], self.ws_f)
+        self.Y_pin.copy_(self.Y, non_blocking=True)
 
     def flops_per_step(self):
         cfg = self.cfg
@@ -509,8 +517,8 @@ def run_workload(wl, args, dist, peaks, clocks):
     ms_e2e = dist.reduce(time_e2e(wl, args.steps, args.warmup, dist), "max")
     e2e = {"value": tok / (ms_e2e / 1e3), "unit": "tok/s", "h2d_bytes_per_step": wl.h2d_bytes,
            "d2h_bytes_per_step": wl.d2h_bytes, "ms_per_step": ms_e2e / args.steps,
-           "note": f"public API per call ({wl.api_desc}), inputs copied from pinned host memory and Y "
-                   "copied back every step, no CUDA graph"}
+           "note": f"public API per call ({wl.api_desc}); every step copies its inputs from pinned host memory "
+                   "(one copy per input tensor) and its Y back (one copy), no CUDA graph"}
     kt = time_kernels(wl, min(args.steps, 200))
     kname, bound, work, work_desc = wl.dominant(peaks)
     kms, kn = kt[kname]

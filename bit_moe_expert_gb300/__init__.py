@@ -144,7 +144,13 @@ class QMat:
     sb: "object"
 
     def _c(self) -> _QMat:
-        return _QMat(_ptr(self.q), _ptr(self.sb))
+        # the C struct is built once and reused while q and sb are the same tensors (a call marshals
+        # three matrices per expert set; rebuilding them cost several microseconds per call)
+        c = self.__dict__.get("_cc")
+        if c is None or c[0] is not self.q or c[1] is not self.sb:
+            c = (self.q, self.sb, _QMat(_ptr(self.q), _ptr(self.sb)))
+            self.__dict__["_cc"] = c
+        return c[2]
 
 
 @dataclasses.dataclass
@@ -167,7 +173,20 @@ class Experts:
         return int(self.gate.q.shape[3]) // 2
 
     def _c(self) -> _Experts:
-        return _Experts(self.gate._c(), self.up._c(), self.down._c(), self.n_experts, self.bits)
+        # rebuilt only when a matrix or one of its tensors was replaced (identity checks only)
+        c = self.__dict__.get("_cc")
+        g, u, dn = self.gate, self.up, self.down
+        if (c is None or c[0] is not g or c[1] is not u or c[2] is not dn or c[3] is not g.q or c[4] is not g.sb
+                or c[5] is not u.q or c[6] is not u.sb or c[7] is not dn.q or c[8] is not dn.sb):
+            c = (g, u, dn, g.q, g.sb, u.q, u.sb, dn.q, dn.sb,
+                 _Experts(g._c(), u._c(), dn._c(), self.n_experts, self.bits), self.I)
+            self.__dict__["_cc"] = c
+        return c[9]
+
+    def _c_and_I(self):
+        """The C struct and the intermediate width, from the same cache."""
+        st = self._c()
+        return st, self.__dict__["_cc"][10]
 
 
 @dataclasses.dataclass
@@ -196,8 +215,17 @@ class Routing:
                        block_rows=block_rows)
 
     def _c(self) -> _Routing:
-        return _Routing(_ptr(self.ids), _ptr(self.w), _ptr(self.counts), _ptr(self.offsets), _ptr(self.perm),
-                        _ptr(self.inv_perm), _ptr(self.block_map), _ptr(self.num_blocks), self.block_rows)
+        c = self.__dict__.get("_cc")
+        if (c is None or c[0] is not self.ids or c[1] is not self.w or c[2] is not self.counts
+                or c[3] is not self.offsets or c[4] is not self.perm or c[5] is not self.inv_perm
+                or c[6] is not self.block_map or c[7] is not self.num_blocks):
+            bufs = (self.ids, self.w, self.counts, self.offsets, self.perm, self.inv_perm, self.block_map,
+                    self.num_blocks)
+            c = bufs + (_Routing(*(_ptr(b) for b in bufs), self.block_rows),)
+            self.__dict__["_cc"] = c
+        st = c[8]
+        st.block_rows = self.block_rows
+        return st
 
 
 def workspace(nbytes: int, device="cuda"):
@@ -309,11 +337,10 @@ def moe_layer(logits, X, routed: Experts, shared: Optional[Experts], k: int, blo
               stream=None) -> None:
     """moe_route + moe_forward in one call (one launch on the decode path)."""
     T, d = X.shape
-    re = routed._c()
-    se = shared._c() if shared is not None else None
-    I_sh = shared.I if shared is not None else 0
+    re, I = routed._c_and_I()
+    se, I_sh = shared._c_and_I() if shared is not None else (None, 0)
     r = out._c()
-    _check("moe_layer", lib().moe_layer(_ptr(logits), _ptr(X), T, d, routed.I, k, block_rows, C.byref(re),
+    _check("moe_layer", lib().moe_layer(_ptr(logits), _ptr(X), T, d, I, k, block_rows, C.byref(re),
                                         C.byref(se) if se is not None else None, I_sh, C.byref(r), _ptr(Y),
                                         _ptr(ws), ws.numel(), _stream(stream)))
     out.block_rows = r.block_rows

@@ -30,8 +30,63 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
+// Encoded tensor maps, reused across calls: a map is a pure function of its
+// arguments, and a layer call encodes a dozen of them (about a microsecond of
+// host time each), which is most of the host cost of a decode-layer call.  A
+// direct-mapped table keyed by every argument; a hit copies the stored map.
+struct MapKey {
+  const void* ptr;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3];
+  int rank, dt, sw;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCache = 256;
+MapEntry g_maps[kMapCache];
+std::mutex g_maps_mu;
+
 bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));  // padding bytes take part in the comparison
+  const bool cacheable = rank >= 1 && rank <= 3;
+  if (cacheable) {
+    key.ptr = ptr;
+    for (int i = 0; i < rank; ++i) {
+      key.dims[i] = dims[i];
+      key.box[i] = box[i];
+      if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    key.rank = rank;
+    key.dt = static_cast<int>(dt);
+    key.sw = static_cast<int>(sw);
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(&key);
+    for (size_t i = 0; i < sizeof(key); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+    const int slot = static_cast<int>(h % kMapCache);
+    {
+      std::lock_guard<std::mutex> lock(g_maps_mu);
+      if (g_maps[slot].used && g_maps[slot].key == key) {
+        *map = g_maps[slot].map;
+        return true;
+      }
+    }
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = g_encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(g_maps_mu);
+    g_maps[slot].key = key;
+    g_maps[slot].map = *map;
+    g_maps[slot].used = true;
+    return true;
+  }
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = g_encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
