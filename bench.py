@@ -356,6 +356,13 @@ class PrefillWorkload(Workload):
         self.Y_pin = torch.empty((cfg.T, cfg.d), dtype=torch.int16).pin_memory()
         self.X_e2e = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device=dev)
         self.lg_e2e = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=dev)
+        # copies run on their own stream, overlapped with the chunks' kernels: chunk c's inputs land
+        # while earlier chunks compute, and its Y leaves while later chunks compute
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.ev_step = torch.cuda.Event()
+        self.ev_in = [torch.cuda.Event() for _ in range(self.nchunks)]
+        self.ev_out = [torch.cuda.Event() for _ in range(self.nchunks)]
+        self.ev_done = torch.cuda.Event()
         self.h2d_bytes = self.X_host.nbytes + self.nchunks * C * cfg.E * 4
         self.d2h_bytes = cfg.T * cfg.d * 2
         self._flops = None
@@ -375,15 +382,28 @@ class PrefillWorkload(Workload):
                            self.Y[c * C:(c + 1) * C], self.ws_f)
 
     def e2e_step(self):
+        import torch
         bm, cfg, C = self.bm, self.cfg, self.chunk
-        self.X_e2e.copy_(self.X_pin, non_blocking=True)
-        self.lg_e2e.copy_(self.lg_pin, non_blocking=True)
+        main, cs = torch.cuda.current_stream(), self.copy_stream
+        self.ev_step.record(main)  # the previous step's kernels are done with the input buffers
+        cs.wait_event(self.ev_step)
+        with torch.cuda.stream(cs):
+            for c in range(self.nchunks):
+                rows = slice(c * C, (c + 1) * C)
+                self.X_e2e[rows].copy_(self.X_pin[rows], non_blocking=True)
+                self.lg_e2e[rows].copy_(self.lg_pin[rows], non_blocking=True)
+                self.ev_in[c].record(cs)
         for c in range(self.nchunks):
-            s = self._set(c)
-            bm.moe_route(self.lg_e2e[c * C:(c + 1) * C], cfg.k, self.block_rows, self.r, self.ws_r)
-            bm.moe_forward(self.X_e2e[c * C:(c + 1) * C], self.routed[s], self.shared[s], self.r,
-                           self.Y[c * C:(c + 1) * C], self.ws_f)
-        self.Y_pin.copy_(self.Y, non_blocking=True)
+            s, rows = self._set(c), slice(c * C, (c + 1) * C)
+            main.wait_event(self.ev_in[c])
+            bm.moe_route(self.lg_e2e[rows], cfg.k, self.block_rows, self.r, self.ws_r)
+            bm.moe_forward(self.X_e2e[rows], self.routed[s], self.shared[s], self.r, self.Y[rows], self.ws_f)
+            self.ev_out[c].record(main)
+            cs.wait_event(self.ev_out[c])
+            with torch.cuda.stream(cs):
+                self.Y_pin[rows].copy_(self.Y[rows], non_blocking=True)
+        self.ev_done.record(cs)
+        main.wait_event(self.ev_done)  # the step ends when its last Y has reached the host buffer
 
     def flops_per_step(self):
         cfg = self.cfg

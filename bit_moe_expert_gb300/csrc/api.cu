@@ -82,7 +82,7 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lock(g_maps_mu);
-    g_maps[slot].key = key;
+    std::memcpy(&g_maps[slot].key, &key, sizeof(key));  // keys compare as bytes
     g_maps[slot].map = *map;
     g_maps[slot].used = true;
     return true;
@@ -347,6 +347,75 @@ namespace {
 
 // moe_forward; with `logits` set and T on the decode path, the decode kernel
 // also routes the tokens and writes every routing output to *r (moe_layer).
+// The decode kernel's twelve tensor maps for one (routed, shared) expert set
+// and shape, built once and reused: a decode-layer call then spends no host
+// time on encoding.  Keyed by every pointer and size the maps depend on.
+struct DecodeMapsKey {
+  const void* p[12];
+  int E, d, I, I_shared, wpg;
+  bool operator==(const DecodeMapsKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+struct DecodeMapsEntry {
+  DecodeMapsKey key;
+  DecodeMaps mr, ms;
+  bool used;
+};
+constexpr int kDecodeMapsCache = 64;
+DecodeMapsEntry g_dmaps[kDecodeMapsCache];
+std::mutex g_dmaps_mu;
+
+bool decode_maps(const moe_experts* routed, const moe_experts* shared, int E, int d, int I, int I_shared, int wpg,
+                 DecodeMaps* mr, DecodeMaps* ms) {
+  DecodeMapsKey key;
+  std::memset(&key, 0, sizeof(key));
+  const moe_qmat* mats[6] = {&routed->gate, &routed->up, &routed->down, shared ? &shared->gate : nullptr,
+                             shared ? &shared->up : nullptr, shared ? &shared->down : nullptr};
+  for (int i = 0; i < 6; ++i) {
+    key.p[2 * i] = mats[i] ? mats[i]->q : nullptr;
+    key.p[2 * i + 1] = mats[i] ? mats[i]->sb : nullptr;
+  }
+  key.E = E;
+  key.d = d;
+  key.I = I;
+  key.I_shared = shared ? I_shared : 0;
+  key.wpg = wpg;
+  uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+  const unsigned char* kb = reinterpret_cast<const unsigned char*>(&key);
+  for (size_t i = 0; i < sizeof(key); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+  DecodeMapsEntry& slot = g_dmaps[h % kDecodeMapsCache];
+  {
+    std::lock_guard<std::mutex> lock(g_dmaps_mu);
+    if (slot.used && slot.key == key) {
+      *mr = slot.mr;
+      *ms = slot.ms;
+      return true;
+    }
+  }
+  const cuuint32_t G1 = static_cast<cuuint32_t>(d / 64), G2 = static_cast<cuuint32_t>(I / 64);
+  bool ok = encode_codes_rows(&mr->q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+            encode_codes_rows(&mr->q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+            encode_codes_rows(&mr->q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2, wpg) &&
+            encode_groups(&mr->sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, G1) &&
+            encode_groups(&mr->sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, G1) &&
+            encode_groups(&mr->sb_down, routed->down.sb, E, d, I, kDecodeRowsDown, G2);
+  if (ok && shared) {
+    const cuuint32_t G2s = static_cast<cuuint32_t>(I_shared / 64);
+    ok = encode_codes_rows(&ms->q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+         encode_codes_rows(&ms->q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
+         encode_codes_rows(&ms->q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s, wpg) &&
+         encode_groups(&ms->sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
+         encode_groups(&ms->sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
+         encode_groups(&ms->sb_down, shared->down.sb, 1, d, I_shared, kDecodeRowsDown, G2s);
+  }
+  if (!ok) return false;
+  std::lock_guard<std::mutex> lock(g_dmaps_mu);
+  std::memcpy(&slot.key, &key, sizeof(key));  // padding included: keys compare as bytes
+  slot.mr = *mr;
+  slot.ms = *ms;
+  slot.used = true;
+  return true;
+}
+
 moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe_experts* routed,
                         const moe_experts* shared, int I_shared, const moe_routing* r, uint16_t* Y, void* ws,
                         size_t ws_bytes, moe_stream stream, const float* logits) {
@@ -389,23 +458,7 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
 
   if (path == Path::kGemv) {
     DecodeMaps mr, ms;
-    const cuuint32_t G1 = static_cast<cuuint32_t>(d / 64), G2 = static_cast<cuuint32_t>(I / 64);
-    bool ok = encode_codes_rows(&mr.q_gate, routed->gate.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
-              encode_codes_rows(&mr.q_up, routed->up.q, E, I, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
-              encode_codes_rows(&mr.q_down, routed->down.q, E, d, I, kDecodeRowsDown, G2, wpg) &&
-              encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kDecodeRowsGU, G1) &&
-              encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kDecodeRowsGU, G1) &&
-              encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kDecodeRowsDown, G2);
-    if (ok && shared) {
-      const cuuint32_t G2s = static_cast<cuuint32_t>(I_shared / 64);
-      ok = encode_codes_rows(&ms.q_gate, shared->gate.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
-           encode_codes_rows(&ms.q_up, shared->up.q, 1, I_shared, d, kDecodeRowsGU, kDecodeChunkGroups, wpg) &&
-           encode_codes_rows(&ms.q_down, shared->down.q, 1, d, I_shared, kDecodeRowsDown, G2s, wpg) &&
-           encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
-           encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kDecodeRowsGU, G1) &&
-           encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kDecodeRowsDown, G2s);
-    }
-    if (!ok) return MOE_ERR_CUDA;
+    if (!decode_maps(routed, shared, E, d, I, I_shared, wpg, &mr, &ms)) return MOE_ERR_CUDA;
     DecodeArgs a{};
     a.X = X;
     a.ids = r->ids;
