@@ -2,14 +2,17 @@
 """Benchmark of the 4-bit groupwise-affine MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill4096|prefill512|canvas|tiny] [--no-secondary]
+                    [--workload decode|prefill4096|prefill512|canvas|tiny|decode3b|decode2b|
+                                prefill512b3|prefill512b2|sweep] [--no-secondary]
 
 Prints ONE JSON line.  Headline workload: batch-1 decode through 40 distinct
 chained MoE layers (T=1, d=2048, E=256, top-8 + shared expert, I=512); a step
 is the 40-layer pass, captured in a CUDA graph.  The line also carries the
 T=4096 long prefill (four chunks of 1024 tokens, Zipf-skewed routing) measured
 the same way.  `value` is tokens per second through one MoE layer: layer
-invocations x tokens / time.
+invocations x tokens / time.  The low-bit workloads (decode3b, decode2b,
+prefill512b3, prefill512b2) are the same layers with 3- and 2-bit expert codes;
+`--workload sweep` prints the rows-per-expert and canvas-batching tables.
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the layer has no exchange step on one node); value sums the ranks' tokens
