@@ -7,7 +7,9 @@
 // equals +0.0).  Every entry gets the 64-bit key (monotone value key << 32 |
 // ~index), so the order is total and every comparison below is strict.
 //
-// One CTA per row (persistent over rows), three phases:
+// One CTA per row (persistent over rows; two CTAs per SM, so that one CTA's
+// selection overlaps the other's streaming and 256 rows fit one wave), three
+// phases:
 //   1. stream the row once; each 256-entry chunk's largest value goes to
 //      shared memory (a warp per chunk, eight chunks of loads in flight per
 //      warp), as the chunk key (value key << 32 | ~chunk index);
@@ -16,7 +18,10 @@
 //      maximum, and a prefix over the chunks equal to it takes the first ones;
 //   3. re-read those chunks (L2), keep every entry whose value is at least
 //      theta, rank the kept entries' keys (or sort them, when ties make them
-//      many) and write the first K.
+//      many) and write the first K.  When ties make more candidates than the
+//      buffer holds, a radix select over their 64-bit keys (8 bits a pass,
+//      re-reading the chunks) finds the K-th largest key first, and only the K
+//      keys at or above it are kept.
 // Exactness.  Chunks are ranked by (largest value, lower chunk index).  Every
 // chunk ranked above the chunk of an entry x holds an entry of larger key than
 // x (a larger value, or the same value at a lower index, chunks being
@@ -37,7 +42,8 @@ namespace {
 constexpr int kWideThreads = 512;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideChunk = 256;  // entries per chunk: 8 per lane
-constexpr int kWideU = 8;        // chunks of loads in flight per warp (128 KB per CTA)
+constexpr int kWideU = 4;        // chunks of loads in flight per warp (64 KB per CTA, 128 KB per SM)
+constexpr int kWideCand = 2048;  // candidate buffer (keys); more candidates take the radix-select path
 
 __device__ __forceinline__ uint64_t wide_key(float v, int i) {
   return (static_cast<uint64_t>(topk_key(v)) << 32) | static_cast<uint32_t>(~i);
@@ -78,6 +84,36 @@ __device__ __forceinline__ void load_chunk8(const float* __restrict__ x, int V, 
   }
 }
 
+// Warp 0: the bin of s_hist (256 counts, scanned from the top bin down) that
+// holds the take-th largest key; writes it to *bin and the count of the bins
+// above it to *above.  The caller synchronises before and after.
+__device__ __forceinline__ void find_bin(const int* s_hist, int take, int lane, int* bin, int* above) {
+  int cnt[8], tot = 0;  // lane l owns bins 255 - 8l down to 248 - 8l
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    cnt[j] = s_hist[255 - 8 * lane - j];
+    tot += cnt[j];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int p = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += p;
+  }
+  int acc = incl - tot;
+  if (acc < take && take <= incl) {  // the bin holding the take-th largest key is this lane's
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc + cnt[j] >= take) {
+        *bin = 255 - 8 * lane - j;
+        *above = acc;
+        break;
+      }
+      acc += cnt[j];
+    }
+  }
+}
+
 // Exclusive prefix over the CTA of one int per thread; returns the thread's
 // prefix and, in *total, the sum.  Uses s_warp[kWideWarps] and synchronises.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
@@ -102,7 +138,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return before + incl - v;
 }
 
-__global__ void __launch_bounds__(kWideThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, 2)
     topk_wide_kernel(const float* __restrict__ logits, int T, int V, int K, int cand_cap, float* __restrict__ values,
                      int32_t* __restrict__ indices) {
   extern __shared__ uint64_t s_dyn[];  // candidates [cand_cap], then the chunk maxima' value keys
@@ -163,33 +199,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if ((key & mask) == theta) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
         }
         __syncthreads();
-        if (warp == 0) {
-          // lane l owns bins 255 - 8l down to 248 - 8l: counts from the top bin down
-          int cnt[8], tot = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            cnt[j] = s_hist[255 - 8 * lane - j];
-            tot += cnt[j];
-          }
-          int incl = tot;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int p = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += p;
-          }
-          int acc = incl - tot;
-          if (acc < take && take <= incl) {  // the bin holding the take-th largest key is this lane's
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (acc + cnt[j] >= take) {
-                s_bin = 255 - 8 * lane - j;
-                s_above = acc;
-                break;
-              }
-              acc += cnt[j];
-            }
-          }
-        }
+        if (warp == 0) find_bin(s_hist, take, lane, &s_bin, &s_above);
         __syncthreads();
         theta |= static_cast<uint32_t>(s_bin) << shift;
         mask |= 0xFFu << shift;
@@ -217,10 +227,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     __syncthreads();
 
-    // ---- 3. candidates: the selected chunks' entries with values >= theta
-    // (every load of a warp's chunks in flight together)
-    {
-      const int nsel = s_nsel;
+    // ---- 3. candidates: the selected chunks' entries with values >= theta and
+    // keys >= kappa (every load of a warp's chunks in flight together); fn(key)
+    // sees each.  kappa is 0 except on the radix-select path.
+    const int nsel = s_nsel;
+    auto visit = [&](uint64_t kappa, auto&& fn) {
       constexpr int kPerWarp = 64 / kWideWarps;  // K <= 64 chunks over the warps
       float v[kPerWarp][8];
 #pragma unroll
@@ -234,30 +245,66 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (sidx >= nsel) continue;  // warp-uniform
         const int base = s_sel[sidx] * kWideChunk + 8 * lane;
         uint64_t keep[8];
-        int nk = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const bool in = base + j < V && topk_key(v[u][j]) >= theta;
           keep[j] = in ? wide_key(v[u][j], base + j) : 0;
-          nk += in ? 1 : 0;
+          if (keep[j] < kappa) keep[j] = 0;
         }
-        // warp-wide exclusive prefix of the lanes' counts, one shared atomic per warp
-        int incl = nk;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int p = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += p;
-        }
-        int wbase = 0;
-        if (lane == 31) wbase = atomicAdd(&s_n, incl);
-        wbase = __shfl_sync(0xffffffffu, wbase, 31);
-        int pos = wbase + incl - nk;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (keep[j] != 0) cand[pos++] = keep[j];
+        fn(keep);
       }
-    }
+    };
+    // count and store (stores past the buffer are dropped; the count goes on)
+    auto store = [&](const uint64_t (&keep)[8]) {
+      int nk = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) nk += keep[j] != 0 ? 1 : 0;
+      // warp-wide exclusive prefix of the lanes' counts, one shared atomic per warp
+      int incl = nk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int p = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += p;
+      }
+      int wbase = 0;
+      if (lane == 31) wbase = atomicAdd(&s_n, incl);
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      int pos = wbase + incl - nk;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (keep[j] != 0) {
+          if (pos < cand_cap) cand[pos] = keep[j];
+          ++pos;
+        }
+    };
+    visit(0ull, store);
     __syncthreads();
+    if (s_n > cand_cap) {
+      // More candidates than the buffer holds (ties with theta): kappa = the
+      // K-th largest candidate key, by a radix select over the 64-bit keys,
+      // then only the K keys >= kappa are stored (the keys are distinct).
+      uint64_t kappa = 0, kmask = 0;
+      int take = K;
+      for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += kWideThreads) s_hist[i] = 0;
+        __syncthreads();
+        visit(0ull, [&](const uint64_t (&keep)[8]) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (keep[j] != 0 && (keep[j] & kmask) == kappa) atomicAdd(&s_hist[(keep[j] >> shift) & 255u], 1);
+        });
+        __syncthreads();
+        if (warp == 0) find_bin(s_hist, take, lane, &s_bin, &s_above);
+        __syncthreads();
+        kappa |= static_cast<uint64_t>(s_bin) << shift;
+        kmask |= 0xFFull << shift;
+        take -= s_above;
+      }
+      if (threadIdx.x == 0) s_n = 0;
+      __syncthreads();
+      visit(kappa, store);
+      __syncthreads();
+    }
 
     // ---- 4. order: the keys are distinct, so a key's rank is the number of
     // larger keys; few candidates (the usual case) are ranked directly, many
@@ -290,19 +337,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-int next_pow2(int v) {
-  int p = 1;
-  while (p < v) p <<= 1;
-  return p;
-}
-
 }  // namespace
 
-// candidates: up to K chunks of entries, rounded up to a power of two for the
-// sort; then one 4-byte value key per chunk
+// candidates: a buffer of kWideCand keys (a power of two, for the sort); then
+// one 4-byte value key per chunk
 size_t topk_wide_smem_bytes(int V, int K) {
+  (void)K;
   const int nch = (V + kWideChunk - 1) / kWideChunk;
-  return static_cast<size_t>(next_pow2(K)) * kWideChunk * 8 + static_cast<size_t>(nch) * 4;
+  return static_cast<size_t>(kWideCand) * 8 + static_cast<size_t>(nch) * 4;
 }
 
 cudaError_t launch_topk_wide(const float* logits, int T, int V, int K, float* values, int32_t* indices,
@@ -320,7 +362,17 @@ cudaError_t launch_topk_wide(const float* logits, int T, int V, int K, float* va
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(T < num_sms ? T : num_sms));
+  static int per_sm = 0;
+  static size_t per_sm_smem = 0;
+  if (per_sm == 0 || per_sm_smem != smem) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_wide_kernel, kWideThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+    per_sm_smem = smem;
+  }
+  const int ctas = per_sm * num_sms;
+  cfg.gridDim = dim3(static_cast<unsigned>(T < ctas ? T : ctas));
   cfg.blockDim = dim3(kWideThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -328,7 +380,7 @@ cudaError_t launch_topk_wide(const float* logits, int T, int V, int K, float* va
   cfg.numAttrs = 1;
   timer_begin(kKTopkWide, stream);
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, topk_wide_kernel, logits, T, V, K, next_pow2(K) * kWideChunk, values, indices);
+      cudaLaunchKernelEx(&cfg, topk_wide_kernel, logits, T, V, K, kWideCand, values, indices);
   timer_end(kKTopkWide, stream);
   return e;
 }
