@@ -74,6 +74,16 @@ def test_topk_wide_heavy_ties():
     _check(np.zeros((2, 5000), np.float32), 64)
 
 
+def test_topk_wide_candidate_counts_on_each_path():
+    # integer values 0..10: every chunk's maximum is 10 and about 23 of its entries tie with it, so the 64
+    # selected chunks give about 1,500 candidates (sorted in the buffer); 0..2 gives about 5,500 (more
+    # than the buffer: the radix select over the candidates' keys); normal values give about K (ranked)
+    rng = np.random.default_rng(45)
+    _check(rng.integers(0, 11, size=(2, 262144)).astype(np.float32), 64)
+    _check(rng.integers(0, 3, size=(2, 262144)).astype(np.float32), 64)
+    _check(rng.integers(0, 11, size=(3, 70001)).astype(np.float32), 17)
+
+
 def test_topk_wide_clustered_signed_zero_and_infinities():
     rng = np.random.default_rng(43)
     lg = rng.standard_normal((4, 20000)).astype(np.float32)
