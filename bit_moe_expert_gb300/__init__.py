@@ -23,10 +23,11 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes",
             "moe_prepack_codes_bits", "moe_prepack_scales",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
+            "moe_route_noalloc_check_status",
             "moe_router_logits", "moe_route_x", "moe_layer_x", "moe_topk_wide",
             "moe_forward_workspace_bytes",
             "moe_forward", "moe_layer_workspace_bytes", "moe_layer", "moe_check_status", "moe_profile_enable", "moe_profile_kernel_count",
-            "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset")
+            "moe_profile_kernel_name", "moe_profile_read", "moe_profile_reset", "moe_debug_decode")
 
 
 class MoeError(RuntimeError):
@@ -89,6 +90,8 @@ def lib(path: Optional[str] = None):
         L.moe_route_noalloc.restype = C.c_int
         L.moe_route_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                         C.c_void_p]
+        L.moe_route_noalloc_check_status.restype = C.c_int
+        L.moe_route_noalloc_check_status.argtypes = [C.c_void_p]
         L.moe_forward_workspace_bytes.restype = C.c_size_t
         L.moe_forward_workspace_bytes.argtypes = [C.c_int] * 6
         L.moe_forward.restype = C.c_int
@@ -115,6 +118,8 @@ def lib(path: Optional[str] = None):
         L.moe_profile_read.restype = C.c_int
         L.moe_profile_read.argtypes = [C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_longlong)]
         L.moe_profile_reset.restype = None
+        L.moe_debug_decode.restype = C.c_int
+        L.moe_debug_decode.argtypes = [C.c_longlong, C.c_int]
         _lib_handle = L
     return _lib_handle
 
@@ -313,6 +318,12 @@ def moe_route_noalloc(logits, k: int, block_rows: int, out: Routing, stream=None
     out.block_rows = r.block_rows
 
 
+def moe_route_noalloc_check_status(stream=None) -> int:
+    """Synchronises; the first device-side error recorded by moe_route_noalloc
+    calls on the current device since the last check (0 if none), cleared."""
+    return int(lib().moe_route_noalloc_check_status(_stream(stream)))
+
+
 def moe_forward_workspace_bytes(T: int, d: int, I: int, E: int, k: int, I_shared: int) -> int:
     return int(lib().moe_forward_workspace_bytes(T, d, I, E, k, I_shared))
 
@@ -370,6 +381,12 @@ def moe_profile_enable(on: bool) -> bool:
 
 def moe_profile_reset() -> None:
     lib().moe_profile_reset()
+
+
+def moe_debug_decode(wait_limit_cycles: int = 0, drop_cta: int = -1) -> None:
+    """Test hook of the decode kernel: the limit of the wait at its barrier over
+    the grid (cycles, 0 = default) and a CTA whose arrival there is skipped."""
+    _check("moe_debug_decode", lib().moe_debug_decode(int(wait_limit_cycles), int(drop_cta)))
 
 
 def moe_profile_read() -> dict:

@@ -18,6 +18,9 @@
 // weights; they wait for nothing, so they run beside the routing CTAs.
 #include <cuda_runtime.h>
 
+#include <cstddef>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -31,6 +34,14 @@ namespace {
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kBasesSmemLimit = 96 * 1024;  // per-chunk bases kept in shared memory up to this size
+
+constexpr int kRouteMaxDevices = 64;
+struct RouteSetup {
+  bool done;
+  int resident8, resident32;  // CTAs of route_kernel<8>, <32> resident at once (no dynamic shared memory)
+};
+RouteSetup g_route_setup[kRouteMaxDevices] = {};
+std::mutex g_route_setup_mu;
 
 // kPL: logits per lane (E <= 32 * kPL).
 template <int kPL>
@@ -350,26 +361,42 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
   const size_t bases_bytes = nchunks > 1 ? static_cast<size_t>(nchunks) * E * 4 : 0;
   const int bases_in_smem = (nchunks > 1 && bases_bytes <= static_cast<size_t>(kBasesSmemLimit)) ? 1 : 0;
 
-  static bool attr_set = false;
-  static int resident[2] = {0, 0};  // CTAs of route_kernel<8>, <32> resident at once (no dynamic shared memory)
-  if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(route_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
-    cudaError_t e2 = cudaFuncSetAttribute(route_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
-    if (e1 != cudaSuccess) return e1;
-    if (e2 != cudaSuccess) return e2;
-    int dev = 0, sms = 0, per8 = 0, per32 = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per8, route_kernel<8>, kRouteThreads, 0) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per32, route_kernel<32>, kRouteThreads, 0) == cudaSuccess) {
-      resident[0] = sms * per8;
-      resident[1] = sms * per32;
+  // One-time set-up per device (the dynamic shared-memory limit, and how many
+  // CTAs of each instantiation fit at once), under a lock: host threads may
+  // make their first calls on different devices at the same time.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kRouteMaxDevices) return cudaErrorInvalidDevice;
+  int resident8 = 0, resident32 = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_route_setup_mu);
+    RouteSetup& su = g_route_setup[dev];
+    if (!su.done) {
+      cudaError_t e1 = cudaFuncSetAttribute(route_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
+      if (e1 != cudaSuccess) return e1;
+      cudaError_t e2 = cudaFuncSetAttribute(route_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBasesSmemLimit);
+      if (e2 != cudaSuccess) return e2;
+      int sms = 0, per8 = 0, per32 = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per8, route_kernel<8>, kRouteThreads, 0) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per32, route_kernel<32>, kRouteThreads, 0) == cudaSuccess) {
+        su.resident8 = sms * per8;
+        su.resident32 = sms * per32;
+      }
+      su.done = true;
     }
-    attr_set = true;
+    resident8 = su.resident8;
+    resident32 = su.resident32;
   }
   // Grid-synchronised mode when every chunk's CTA can be resident at once
   // (leaving room for other work); otherwise the last CTA finishes alone.
-  const int gridsync = (nchunks > 1 && nchunks <= resident[E <= 256 ? 0 : 1] / 2) ? 1 : 0;
+  // MOE_ROUTE_MODE=ticket or =gridsync forces one of them (A/B and tests; a
+  // forced grid-synchronised launch still needs every CTA resident, so it is
+  // only taken when they fit).
+  int gridsync = (nchunks > 1 && nchunks <= (E <= 256 ? resident8 : resident32) / 2) ? 1 : 0;
+  if (const char* m = std::getenv("MOE_ROUTE_MODE")) {
+    if (!std::strcmp(m, "ticket")) gridsync = 0;
+    if (!std::strcmp(m, "gridsync") && nchunks > 1 && nchunks <= (E <= 256 ? resident8 : resident32)) gridsync = 1;
+  }
   const int nweight = (T + kRouteWarps - 1) / kRouteWarps;  // weight CTAs, one token per warp
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunks + nweight);
@@ -555,7 +582,10 @@ cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, i
 // The scratch of moe_route_noalloc: one file-scope device array, loaded with
 // the module on every device that uses the library.  Host code must not pass
 // the name itself to a kernel (on the host it is only a stand-in); the device
-// address comes from cudaGetSymbolAddress, looked up once per device.
+// address comes from cudaGetSymbolAddress, looked up with the device current.
+// The address belongs to the CUDA context the module was loaded into: it is
+// cached per device together with that context, and looked up again when the
+// device's current context is a different one (after cudaDeviceReset).
 namespace bm {
 namespace {
 
@@ -563,7 +593,46 @@ static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_NOALLOC
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  void* ctx;   // the context the address was looked up in
+  void* addr;  // device address of g_route_scratch in that context
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+typedef int (*CtxGetCurrentFn)(void**);  // cuCtxGetCurrent: CUresult (CUcontext*)
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+
+// The current CUDA context of this thread (null if none or unavailable).
+void* current_context() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+  });
+  void* ctx = nullptr;
+  if (!g_ctx_get || g_ctx_get(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// Device address of the scratch array on the current device (null on error).
+// The first call in a context makes the runtime load the module there.
+void* scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* ctx = current_context();  // null before the runtime has made the device's context current
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchAddr& sa = g_scratch[dev];
+  if (!sa.addr || !ctx || sa.ctx != ctx) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return nullptr;
+    sa.addr = p;
+    sa.ctx = current_context();  // the context the runtime looked the address up in
+  }
+  return sa.addr;
+}
 
 }  // namespace
 }  // namespace bm
@@ -580,23 +649,25 @@ extern "C" moe_status moe_route_noalloc(const float* logits, int T, int E, int k
   if (!out->counts || !out->offsets || !out->block_map || !out->num_blocks) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!logits || !out->ids || !out->w || !out->perm || !out->inv_perm)) return MOE_ERR_INVALID_ARG;
 
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-      g_scratch_addr[dev] = p;
-    }
-    scratch = g_scratch_addr[dev];
-  }
+  void* scratch = scratch_address();
+  if (!scratch) return MOE_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the arrival ticket and the status word must start at zero
-  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+  // The arrival counters must start at zero.  The status word (the header's
+  // first word) is left alone: an error stays recorded until
+  // moe_route_noalloc_check_status reads it.
+  static_assert(offsetof(WsHeader, status) == 0, "status word first");
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + sizeof(uint32_t), 0, sizeof(WsHeader) - sizeof(uint32_t), st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
   out->block_rows = block_rows;
   RouteOut o{out->ids, out->w, out->counts, out->offsets, out->perm, out->inv_perm, out->block_map, out->num_blocks};
   if (launch_route(logits, T, E, k, block_rows, o, scratch, st, false) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status moe_route_noalloc_check_status(moe_stream stream) {
+  using namespace bm;
+  void* scratch = scratch_address();
+  if (!scratch) return MOE_ERR_CUDA;
+  return moe_check_status(scratch, stream);
 }

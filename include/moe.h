@@ -195,20 +195,33 @@ moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, m
  *     as for moe_route.
  *   - The first call on a device looks up the scratch array's device address
  *     (with that device current).  Make that first call before any stream
- *     capture.
+ *     capture.  The address is kept per device together with the CUDA context
+ *     it belongs to; after cudaDeviceReset (a new context) the next call looks
+ *     it up again, so that call, too, must come before any capture.
  *   - Every call shares the one array and leaves its contents behind; each call
  *     first clears the part that must start at zero (cudaMemsetAsync on
  *     `stream`).  Calls that overlap on the GPU -- on different streams or from
  *     different host threads -- race and produce wrong results: keep them
  *     ordered on one stream.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
- *   - A non-finite logit is not reported (there is no workspace status word);
- *     use moe_route with a workspace and moe_check_status to detect it. */
+ *   - Device-side errors (a non-finite logit: MOE_ERR_NONFINITE; a bounded
+ *     wait of the routing kernel that expired: MOE_ERR_TIMEOUT, after which
+ *     the outputs are meaningless) are recorded in a status word inside the
+ *     scratch array.  The word keeps the first error until
+ *     moe_route_noalloc_check_status reads and clears it; the call itself
+ *     still returns MOE_OK, because it does not wait for the GPU. */
 #define MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS 65536
 #define MOE_ROUTE_NOALLOC_MAX_HIST 65536
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (256 + 4 * (MOE_ROUTE_NOALLOC_MAX_HIST + MOE_ROUTE_NOALLOC_MAX_ASSIGNMENTS))
 moe_status moe_route_noalloc(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
                              moe_stream stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded by
+ * moe_route_noalloc calls on the current device since the last check
+ * (MOE_OK if none) and clears it.  Allocates nothing.  For tests and
+ * debugging, like moe_check_status; it must not run while a stream is being
+ * captured. */
+moe_status moe_route_noalloc_check_status(moe_stream stream);
 
 /* ------------------------------------------------------------------ experts
  * Workspace bytes moe_forward needs for these sizes (I_shared = 0: no shared

@@ -8,6 +8,8 @@ workspace.  Its outputs must equal moe_route's bit for bit (routing is integer
 bookkeeping plus weights rounded the same way), including when two calls follow
 each other and share that scratch array.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -56,6 +58,53 @@ def test_route_noalloc_equals_moe_route_on_consecutive_calls():
         for key in ("ids", "w", "counts", "offsets", "perm", "inv_perm", "block_map"):
             np.testing.assert_array_equal(b[key], a[key], err_msg=f"{key} T={T} E={E}")
         assert got.block_rows == block_rows
+
+
+@pytest.mark.parametrize("mode", ["ticket", "gridsync"])
+def test_route_noalloc_both_multi_chunk_modes(mode, monkeypatch):
+    """At T = 8192 (256 chunks of 32 tokens) the routing kernel places the
+    assignments either after a bounded barrier over the grid or in the last CTA
+    to arrive (per-chunk bases in the scratch array); both must equal moe_route
+    (in its default mode) bit for bit."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rng = np.random.default_rng(78)
+    T, E, k, block_rows = 8192, 256, 8, 96
+    lg = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32)).cuda()
+    ref = _route_with_workspace(lg, k, block_rows)
+    torch.cuda.synchronize()
+    monkeypatch.setenv("MOE_ROUTE_MODE", mode)
+    got = []
+    for _ in range(2):
+        r = bm.Routing.empty(T, E, k, block_rows)
+        bm.moe_route_noalloc(lg, k, block_rows, r)
+        got.append(r)
+    torch.cuda.synchronize()
+    assert bm.moe_route_noalloc_check_status() == 0
+    a = _host(ref)
+    for r in got:
+        b = _host(r)
+        assert a["num_blocks"] == b["num_blocks"]
+        for key in ("ids", "w", "counts", "offsets", "perm", "inv_perm", "block_map"):
+            np.testing.assert_array_equal(b[key], a[key], err_msg=f"{key} mode={mode}")
+
+
+def test_route_noalloc_reports_device_errors():
+    """A non-finite logit is recorded in the scratch array's status word, read
+    (and cleared) by moe_route_noalloc_check_status; the next clean call
+    reports nothing."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    T, E, k = 64, 256, 8
+    lg = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    lg[5, 17] = float("nan")
+    r = bm.Routing.empty(T, E, k, 32)
+    assert bm.moe_route_noalloc_check_status() == 0
+    bm.moe_route_noalloc(lg, k, 32, r)
+    assert bm.moe_route_noalloc_check_status() == 6  # MOE_ERR_NONFINITE
+    lg[5, 17] = 0.0
+    bm.moe_route_noalloc(lg, k, 32, r)
+    assert bm.moe_route_noalloc_check_status() == 0
 
 
 def test_route_noalloc_rejects_sizes_beyond_its_scratch():
