@@ -293,6 +293,13 @@ __device__ __forceinline__ void write_routing_outputs(const DecodeArgs& a, const
   }
 }
 
+// Test hooks (moe_debug_decode): the limit of the wait at the barrier over the
+// grid, in SM clock cycles, and one CTA whose arrival at that barrier is
+// skipped, so that every CTA's wait runs out (a bounded wait that expires;
+// nothing faults).
+__device__ long long g_dec_wait_limit = kWaitLimitCycles;
+__device__ int g_dec_drop_cta = -1;
+
 template <int kT, int kBits>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps mr, const __grid_constant__ DecodeMaps ms, const DecodeArgs a,
@@ -632,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* count = &hdr->dec_count[gen & 1u];
       const long long t0 = clock64();
       while (ld_acquire_gpu(count) < static_cast<uint32_t>(nC)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > g_dec_wait_limit) {
           record_status(a.status, MOE_ERR_TIMEOUT);
           break;
         }
@@ -780,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copies after it.
     fence_proxy_async_global();
     cons_sync();
-    if (threadIdx.x == 0) red_release_gpu_add(&hdr->dec_count[gen & 1u], 1u);
+    if (threadIdx.x == 0 && cta != g_dec_drop_cta) red_release_gpu_add(&hdr->dec_count[gen & 1u], 1u);
 
     // One CTA writes every routing output, after it has arrived (no CTA of the
     // call reads them): its own copy of the weights, from the same arithmetic
@@ -1019,6 +1026,13 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const D
     err = launch_bits<4>(a, routed, sh, hdr, want, L.total, stream, pdl);
   timer_end(kKDecode, stream);
   return err;
+}
+
+cudaError_t decode_debug(long long wait_limit_cycles, int drop_cta) {
+  const long long lim = wait_limit_cycles > 0 ? wait_limit_cycles : kWaitLimitCycles;
+  cudaError_t e = cudaMemcpyToSymbol(g_dec_wait_limit, &lim, sizeof(lim));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_dec_drop_cta, &drop_cta, sizeof(drop_cta));
 }
 
 }  // namespace bm

@@ -90,6 +90,11 @@ bool decode_supported(int T, int d, int I, int I_shared, int k);
 size_t decode_scratch_bytes(int T, int I, int I_shared);  // global scratch: the h records
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* shared, void* ws,
                           cudaStream_t stream, bool pdl);
+// Test hooks of the decode kernel: the limit of the wait at its barrier over
+// the grid in SM clock cycles (<= 0: the default of about 2 s), and one CTA
+// (-1: none) whose arrival at that barrier is skipped, so that the wait runs
+// out.
+cudaError_t decode_debug(long long wait_limit_cycles, int drop_cta);
 
 // ---------------------------------------------------------------- prefill GEMM
 constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)

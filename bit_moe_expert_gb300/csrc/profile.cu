@@ -106,3 +106,8 @@ void moe_profile_reset(void) {
 }
 
 }  // extern "C"
+
+extern "C" moe_status moe_debug_decode(long long wait_limit_cycles, int drop_cta) {
+  if (drop_cta < -1) return MOE_ERR_INVALID_ARG;
+  return bm::decode_debug(wait_limit_cycles, drop_cta) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -35,6 +35,23 @@ moe_status moe_profile_read(int id, double* total_ms, long long* launches);
 /* Forgets all recorded times (synchronises on pending events first). */
 void moe_profile_reset(void);
 
+/* Test hook of the decode kernel (moe_forward and moe_layer with T <= 4), for
+ * tests of failure detection only; no counterpart on the source pages.  The
+ * kernel's CTAs meet once at a barrier over the grid (every h value of the
+ * call written) with a bounded wait.
+ *   wait_limit_cycles  limit of that wait, in SM clock cycles (<= 0 restores
+ *                      the default, about 2 s at the maximum clock); a wait
+ *                      that runs out records MOE_ERR_TIMEOUT in the workspace
+ *                      status word and the kernel carries on to its end
+ *   drop_cta           a CTA of the launch whose arrival at the barrier is
+ *                      skipped, so that every CTA's wait runs out; -1 for none
+ *                      (the default)
+ * Applies to the current device, to launches made after it returns.  A call
+ * whose wait ran out leaves its outputs meaningless; the next call on the same
+ * workspace is unaffected.  Synchronous (a copy to device memory); not for
+ * use during stream capture. */
+moe_status moe_debug_decode(long long wait_limit_cycles, int drop_cta);
+
 #ifdef __cplusplus
 }
 #endif
