@@ -611,7 +611,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // records.  Issuing a copy waits while the SM's copy queue is full, so no
     // compute warp issues any.
     issue1_warp(pre1, min(kS1, total1) - pre1);
-    for (int j0 = pre2, n2 = min(L.S2, total2); j0 < n2; j0 += 16) issue2c_warp(j0, min(16, n2 - j0), nsl);
     // The routing weights (fp64, slow on this GPU), while the copies stream:
     // softmax over each token's selected logits, summed in selection order and
     // rounded once (the routing kernel's arithmetic, so the same bits).
@@ -633,6 +632,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok &= mbar_wait(&empty1[j % kS1], static_cast<uint32_t>(j / kS1 - 1) & 1u, nullptr);
         issue1(j);
       }
+    }
+    // The down rows, once this CTA's last gate/up chunk has landed: the gate/up
+    // bytes, on the path to the barrier over the grid, take the memory
+    // bandwidth first; the down rows are needed only after that barrier.
+    __syncwarp();
+    if (total1 > 0)
+      ok &= mbar_wait(&full1[(total1 - 1) % kS1], static_cast<uint32_t>((total1 - 1) / kS1) & 1u, nullptr);
+    for (int j0 = pre2, n2 = min(L.S2, total2); j0 < n2; j0 += 16) issue2c_warp(j0, min(16, n2 - j0), nsl);
+    if (lane == 0) {
       // the barrier: every CTA has written its h records.  CTA 0 then clears
       // the other counter (last used by call g - 1, which has finished) and
       // advances the call number for call g + 1 (read only after this call).
