@@ -173,7 +173,9 @@ size_t moe_route_workspace_bytes(int T, int E, int k);
 /* fp32 router logits [T][E] (row-major) -> all arrays of *out.  One kernel
  * launch, no host synchronisation.  Preconditions: T >= 0 (T = 0 writes zero
  * counts, offsets and num_blocks), 1 <= E <= 1024, 1 <= k <= min(E, 32),
- * 1 <= block_rows <= 128.  Logits must be finite: a NaN or infinity leaves a
+ * 1 <= block_rows <= 128 (moe_forward's tensor-core path, T > 4, takes at most
+ * 96: route with block_rows <= 96 when the routing feeds it).  Logits must be
+ * finite: a NaN or infinity leaves a
  * deterministic but meaningless selection and records MOE_ERR_NONFINITE in
  * the workspace status word.  Sets out->block_rows. */
 moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
@@ -240,8 +242,11 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  * Path: T <= 4 runs the decode kernel (every active expert's bytes streamed
  * once, one launch; warp-level tensor-core MMAs fed from the 4-bit codes, the
  * gate/up projections in bf16 with x exact, h rounded to fp16 for the down
- * projection); larger T runs the grouped tensor-core GEMM
- * (tcgen05, dequantisation fused, SwiGLU and the weighted combine fused).  The
+ * projection); larger T runs the grouped tensor-core GEMM (tcgen05,
+ * dequantisation fused, SwiGLU fused into the gate/up epilogue; the down
+ * projection writes each expert's output rows in fp32 and a separate combine
+ * kernel sums each token's rows with its routing weights and the shared
+ * expert, in slot order, into bf16 Y).  The
  * environment variable MOE_PATH=gemv|gemm overrides the choice (gemv with
  * T > 4 returns MOE_ERR_UNSUPPORTED; for A/B
  * measurements and tests).  Arithmetic: fp32 accumulation; on the GEMM path X,
