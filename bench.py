@@ -800,10 +800,36 @@ def topk_wide_measure(dev, peaks):
             "note": "logits N(0,1) fp32 from a seeded device generator; one launch per call"}
 
 
+def host_cpu():
+    """The host's logical CPU count and model (from /proc/cpuinfo where present)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "cpu model"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+        if not model:  # Arm: implementer and part numbers
+            impl = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU implementer")]
+            part = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU part")]
+            if impl and part:
+                model = f"{platform.machine()} implementer {impl[0]} part {part[0]}"
+    except OSError:
+        pass
+    return {"host_nproc": os.cpu_count(), "host_cpu": model or platform.machine()}
+
+
 def cpu_baseline(wl, budget_s):
     tokens, secs, desc = wl.cpu_sample(budget_s)
-    return {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
-            "seconds": secs}
+    out = {"value": tokens / secs, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": desc,
+           "seconds": secs}
+    out.update(host_cpu())
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm (the oracle)
@@ -875,7 +901,8 @@ def reference_arm(args, dist):
             "data": "synthetic (seeded)",
             "config": {"workload": f"decode: T={cfg.T}, d={cfg.d}, E={cfg.E}, top-{cfg.k} + shared expert, "
                                    f"I={cfg.I}; CPU oracle", "reference_sample": sample},
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+                                 **host_cpu()),
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -942,19 +969,41 @@ def main():
     del wl
     torch.cuda.empty_cache()
 
-    secondary = None
-    if args.workload == "decode" and not args.no_secondary:
-        wl2 = PrefillWorkload(dev, "prefill4096")
+    def secondary_run(name, budget):
+        wl2 = PrefillWorkload(dev, name)
         steps2 = max(3, min(args.steps, 200))
         a2 = argparse.Namespace(**vars(args))
         a2.steps = steps2
         r2 = run_workload(wl2, a2, dist, peaks, ClockSampler(dist.local_rank))
-        r2["cpu_baseline"] = cpu_baseline(wl2, args.cpu_budget) if dist.rank == 0 else None
+        r2["cpu_baseline"] = cpu_baseline(wl2, budget) if dist.rank == 0 else None
         r2["workload"] = wl2.workload_desc()
         r2["steps"] = steps2
         r2["gpu_launches"] = wl2.launches_per_step() * steps2
-        secondary = r2
+        r2["tok_s"] = r2["value"]
+        if name == "canvas":
+            # the block-diffusion canvas step runs the layer once per each of its 30 layers
+            cfg2 = wl2.cfg
+            per_layer = cfg2.E * synth.ffn_bytes(cfg2.d, cfg2.I, cfg2.bits)  # every expert active
+            n_act = wl2.active_experts()
+            r2["canvas_step"] = {"layers": cfg2.layers, "active_experts_per_layer": n_act,
+                                 "expert_bytes_per_layer": per_layer,
+                                 "gb_per_step": cfg2.layers * n_act * synth.ffn_bytes(cfg2.d, cfg2.I, cfg2.bits) / 1e9,
+                                 "ms_per_step": cfg2.layers * r2["ms_per_step"],
+                                 "canvases_per_s": 1e3 / (cfg2.layers * r2["ms_per_step"]),
+                                 "note": "30 distinct layers of the canvas layer per denoising step; each layer "
+                                         "timed on its own weight set (4 sets rotated, beyond L2)"}
         del wl2
+        torch.cuda.empty_cache()
+        return r2
+
+    secondary = None
+    extra = {}
+    if args.workload == "decode" and not args.no_secondary:
+        secondary = secondary_run("prefill4096", args.cpu_budget)
+        extra["prefill512"] = secondary_run("prefill512", args.cpu_budget / 2)
+        extra["canvas"] = secondary_run("canvas", args.cpu_budget / 2)
+        sw = run_sweep(dev, peaks, args)
+        extra["sweep"] = {k: sw[k] for k in ("sweep", "canvas_batching", "steps", "config", "peak_hbm_gbs")}
         torch.cuda.empty_cache()
     router = router_measure(dev, peaks) if (args.workload == "decode" and not args.no_secondary) else None
     wide = topk_wide_measure(dev, peaks) if (args.workload == "decode" and not args.no_secondary) else None
@@ -976,6 +1025,7 @@ def main():
                 line[key] = main_res[key]
         if secondary is not None:
             line["prefill4096"] = secondary
+        line.update(extra)
         if router is not None:
             line["router_projection"] = router
         if wide is not None:
