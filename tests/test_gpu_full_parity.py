@@ -1,0 +1,150 @@
+"""Parity on every token of the full-size workloads, and at the routing shapes
+of the rows-per-expert sweep.
+
+The layer runs on the GPU exactly as the benchmark runs it (moe_route with
+96-row tiles, then moe_forward on the same chunk); the CPU oracle -- the same
+single-threaded C routine as everywhere, unchanged -- runs on several host
+threads over disjoint token ranges (it keeps no state between calls, and the
+foreign call releases the interpreter lock), so that every token of a
+512-token, 1024-token or 256-token layer is compared, not a sample.
+
+Each case prints the literal errors next to the bound the tests apply: the
+maximum absolute error against the fp64 result and against that result
+rounded to bf16 (no bf16 output can be within 2e-2 of values near 16, whose
+bf16 spacing is 0.0625), the relative L2 error, and the mixed elementwise
+error |dY| / max(1, |Y|).
+"""
+import concurrent.futures as cf
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import bit_moe_expert_gb300 as bm  # noqa: E402
+from bit_moe_expert_gb300 import synth  # noqa: E402
+from tests import gpu_util as G  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_moe_expert_gb300 import build
+    build.build()
+    bm.lib()
+
+
+def _oracle_tokens(X, routed, shared, ids, w, tokens):
+    """oracle.forward on the given tokens, split over the host's cores."""
+    tokens = np.asarray(tokens)
+    nthreads = max(1, min(os.cpu_count() or 1, 32))
+    runs = []  # contiguous runs of tokens, at most ~4 per thread
+    start = 0
+    while start < len(tokens):
+        end = start + 1
+        while end < len(tokens) and tokens[end] == tokens[end - 1] + 1 and end - start < max(1, len(tokens) // (4 * nthreads)):
+            end += 1
+        runs.append((int(tokens[start]), int(tokens[end - 1]) + 1))
+        start = end
+    out64 = np.empty((len(tokens), X.shape[1]), np.float64)
+    out16 = np.empty((len(tokens), X.shape[1]), np.uint16)
+    pos = {t: i for i, t in enumerate(tokens)}
+    with cf.ThreadPoolExecutor(nthreads) as ex:
+        futs = {ex.submit(oracle.forward, X, routed, shared, ids, w, a, b): (a, b) for a, b in runs}
+        for f in cf.as_completed(futs):
+            a, b = futs[f]
+            y64, y16 = f.result()
+            i = pos[a]
+            out64[i:i + (b - a)] = y64
+            out16[i:i + (b - a)] = y16
+    return out64, out16
+
+
+def _report(what, Y, Y64, Y16):
+    e = G.assert_y_close(Y, Y64, what)
+    y = synth.bf16_bits_to_f32(Y).astype(np.float64)
+    lit16 = float(np.max(np.abs(y - synth.bf16_bits_to_f32(Y16).astype(np.float64))))
+    print(f"\n{what}: max |dY| vs fp64 {e['max_abs']:.4g}, vs bf16-rounded oracle {lit16:.4g}; "
+          f"rel L2 {e['rel_l2']:.3g} (bound 5e-3); mixed {e['mixed']:.3g} (bound 2e-2); "
+          f"max |Y| {float(np.max(np.abs(Y64))):.3g}")
+    return e
+
+
+def _gpu_chunk(dl, logits_np, k, block_rows=96):
+    r, _ = G.route_gpu(logits_np, k, block_rows)
+    return r, dl.forward(r)
+
+
+@pytest.mark.parametrize("name", ["prefill512", "canvas"])
+def test_full_layer_every_token(name):
+    cfg = synth.CONFIGS[name]
+    T = cfg.tokens_per_call
+    dl = G.DeviceLayer.from_device_draw(cfg, 0, T)
+    r, Y = _gpu_chunk(dl, dl.logits, cfg.k)
+    rh = G.routing_to_host(r)
+    ref = oracle.route(dl.logits, cfg.k, 96)
+    G.assert_routing_equal(rh, ref)
+    Y64, Y16 = _oracle_tokens(dl.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"], range(T))
+    _report(f"{name}, all {T} tokens", Y, Y64, Y16)
+
+
+def test_long_prefill_chunk_every_token_and_every_chunk_routing():
+    """The skewed 4096-token prompt: the routing of all four 1024-token chunks
+    bit for bit, and every token of one chunk through the layer."""
+    cfg = synth.CONFIGS["prefill4096"]
+    C = cfg.tokens_per_call
+    dl = G.DeviceLayer.from_device_draw(cfg, 0, cfg.T)
+    X_all, lg_all = dl.X_host, dl.logits
+    for c in range(cfg.T // C):
+        lg = np.ascontiguousarray(lg_all[c * C:(c + 1) * C])
+        r, _ = G.route_gpu(lg, cfg.k, 96)
+        G.assert_routing_equal(G.routing_to_host(r), oracle.route(lg, cfg.k, 96))
+    # chunk 0 through the layer, as the benchmark runs it
+    dl0 = G.DeviceLayer(np.ascontiguousarray(X_all[:C]), np.ascontiguousarray(lg_all[:C]), dl.routed_host,
+                        dl.shared_host, dl.routed, dl.shared)
+    r, Y = _gpu_chunk(dl0, dl0.logits, cfg.k)
+    rh = G.routing_to_host(r)
+    Y64, Y16 = _oracle_tokens(dl0.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"], range(C))
+    _report(f"prefill4096 chunk 0, all {C} tokens", Y, Y64, Y16)
+
+
+def _uniform_logits(T, E, k):
+    """Token t routed to experts (k t + j) mod E, j = 0..k-1, in that order: over
+    T = M E / k tokens every expert receives exactly M rows."""
+    lg = np.full((T, E), -10.0, np.float32)
+    for t in range(T):
+        for j in range(k):
+            lg[t, (k * t + j) % E] = 10.0 - j
+    return lg
+
+
+@pytest.mark.parametrize("M", [1, 8, 64, 128])
+def test_uniform_rows_per_expert(M):
+    """The sweep's routing: the decode layer's dimensions with every expert
+    given exactly M rows (T = 32 M tokens).  At M = 128 each expert's rows
+    split into a 96-row and a 32-row tile.  Every token is compared up to
+    M = 8; beyond, tokens from every expert's first and last tile."""
+    cfg = synth.CONFIGS["decode"]
+    T = M * cfg.E // cfg.k
+    dl = G.DeviceLayer.from_device_draw(cfg, 3, T)
+    lg = _uniform_logits(T, cfg.E, cfg.k)
+    r, Y = _gpu_chunk(dl, lg, cfg.k)
+    rh = G.routing_to_host(r)
+    ref = oracle.route(lg, cfg.k, 96)
+    G.assert_routing_equal(rh, ref)
+    assert np.all(rh["counts"] == M)
+    if M <= 8:
+        tokens = np.arange(T)
+    else:
+        # expert e's rows are tokens t with (8 t + j) mod 256 = e: its first rows come from the first tokens and
+        # its last rows (the second tile when M > 96) from the last ones
+        rng = np.random.default_rng(M)
+        tokens = np.unique(np.concatenate([np.arange(16), np.arange(T - 16, T),
+                                           rng.choice(T, size=32, replace=False)]))
+    Y64, Y16 = _oracle_tokens(dl.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"], tokens)
+    _report(f"uniform M={M} (T={T}), {len(tokens)} tokens", Y[tokens], Y64, Y16)
