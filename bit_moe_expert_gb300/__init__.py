@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 # Every symbol the headers in include/ declare.
 EXPORTED = ("moe_status_string", "moe_device_sm_count", "moe_prepack_bytes", "moe_prepack_codes",
-            "moe_prepack_codes_bits", "moe_prepack_scales",
+            "moe_prepack_codes_bits", "moe_prepack_scales", "moe_dequant_experts",
             "moe_route_max_blocks", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
             "moe_route_noalloc_check_status",
             "moe_router_logits", "moe_route_x", "moe_layer_x", "moe_topk_wide",
@@ -87,6 +87,8 @@ def lib(path: Optional[str] = None):
                                   C.POINTER(_Routing), C.c_void_p, C.c_size_t, C.c_void_p]
         L.moe_topk_wide.restype = C.c_int
         L.moe_topk_wide.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p]
+        L.moe_dequant_experts.restype = C.c_int
+        L.moe_dequant_experts.argtypes = [C.POINTER(_QMat), C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.moe_route_noalloc.restype = C.c_int
         L.moe_route_noalloc.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(_Routing),
                                         C.c_void_p]
@@ -402,6 +404,14 @@ def moe_profile_read() -> dict:
 
 
 # ----------------------------------------------------------------------- weight preparation
+
+def moe_dequant_experts(m: QMat, bits: int, W, stream=None) -> None:
+    """W fp16 bits [E][N][K] (int16 tensor) = q * scale + bias of the prepacked matrix m."""
+    E, G, N = m.sb.shape
+    st = m._c()
+    _check("moe_dequant_experts", lib().moe_dequant_experts(C.byref(st), int(E), int(N), int(G) * 64, int(bits),
+                                                            _ptr(W), _stream(stream)))
+
 
 def prepare_experts(ex: dict, device="cuda", stream=None) -> Experts:
     """Device copy of one expert set in the kernels' format.

@@ -263,6 +263,15 @@ moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E
   return MOE_OK;
 }
 
+moe_status moe_dequant_experts(const moe_qmat* m, int E, int N, int K, int bits, uint16_t* W, moe_stream stream) {
+  if (!m || !W || E < 1 || N < 1 || K < 64 || K % 64) return MOE_ERR_INVALID_ARG;
+  if (bits < 2 || bits > 4) return MOE_ERR_INVALID_ARG;
+  if (!qmat_ok(*m) || !aligned16(W)) return MOE_ERR_INVALID_ARG;
+  if (launch_dequant(m->q, m->sb, E, N, K, bits, W, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 int moe_route_max_blocks(int T, int E, int k, int block_rows) {
   if (T < 0 || E < 1 || k < 1 || block_rows < 1) return 0;
   const long long A = static_cast<long long>(T) * k;

@@ -46,6 +46,9 @@ cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, int bit
                                  cudaStream_t stream);
 cudaError_t launch_prepack(const uint16_t* scale, const uint16_t* bias, int E, int N, int K, uint32_t* sb,
                            cudaStream_t stream);
+// fp16 weights W [E][N][K] = q * scale + bias of one prepacked matrix (bits per code 2, 3 or 4)
+cudaError_t launch_dequant(const uint32_t* qp, const uint32_t* sb, int E, int N, int K, int bits, uint16_t* W,
+                           cudaStream_t stream);
 
 // Router projection: logits [T][E] fp32 = X [T][d] bf16 times Wr [E][d] bf16
 // transposed (d a multiple of 32).

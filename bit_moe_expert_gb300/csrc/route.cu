@@ -16,6 +16,7 @@
 // that chain: extra CTAs after the routing CTAs select the top k of 16 tokens
 // each again (the same function, so the same selection) and write only the
 // weights; they wait for nothing, so they run beside the routing CTAs.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -539,6 +540,74 @@ __global__ void prepack_codes_kernel(const uint4* __restrict__ q, int E, int N, 
   }
 }
 }  // namespace
+
+// ------------------------------------------------------------------ dequantisation to fp16
+namespace {
+// W[e][n][k] = fp16(q * scale + bias) of one prepacked matrix: the weights a
+// kernel without fused dequantisation would read.  One thread per 16 columns
+// of one row and group: it reads the row's code words of the group and its
+// (scale, bias) word and writes 32 bytes.  The code of column c of a group, in
+// the prepacked order (see include/moe.h): 4-bit, word c/8, bits 4p + 16h with
+// p = (c%8)/2, h = c%2; 2-bit, word c/16, bits 2p + 16h with p = (c%16)/2;
+// 3-bit, those two bits from words 0..3 and the high bit at bit 16h + 8(j%2)
+// + p of word 4 + j/2, j = c/16.
+template <int kBits>
+__device__ __forceinline__ uint32_t prepacked_code(const uint32_t* w, int c) {
+  if constexpr (kBits == 4) return (w[c >> 3] >> (4 * ((c & 7) >> 1) + 16 * (c & 1))) & 0xFu;
+  const int j = c >> 4, p = (c & 15) >> 1, h = c & 1;
+  const uint32_t lo = (w[j] >> (2 * p + 16 * h)) & 0x3u;
+  if constexpr (kBits == 2) return lo;
+  return lo | (((w[4 + (j >> 1)] >> (16 * h + 8 * (j & 1) + p)) & 1u) << 2);
+}
+
+template <int kBits>
+__global__ void dequant_kernel(const uint32_t* __restrict__ qp, const uint32_t* __restrict__ sb, int E, int N, int G,
+                               uint16_t* __restrict__ W) {
+  constexpr int kWpg = 2 * kBits;
+  const size_t total = static_cast<size_t>(E) * G * N * 4;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int part = static_cast<int>(i & 3);  // columns 16 part .. 16 part + 15 of the group
+    const size_t egn = i >> 2;                   // ((e * G + g) * N + n)
+    const int n = static_cast<int>(egn % N);
+    const size_t eg = egn / N;
+    const int g = static_cast<int>(eg % G);
+    const size_t e = eg / G;
+    uint32_t w[kWpg];
+#pragma unroll
+    for (int u = 0; u < kWpg; ++u) w[u] = __ldg(qp + egn * kWpg + u);
+    const uint32_t p = __ldg(sb + egn);
+    const float scale = __uint_as_float(p << 16), bias = __uint_as_float(p & 0xFFFF0000u);
+    uint32_t out[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const float v0 = fmaf(static_cast<float>(prepacked_code<kBits>(w, 16 * part + c)), scale, bias);
+      const float v1 = fmaf(static_cast<float>(prepacked_code<kBits>(w, 16 * part + c + 1)), scale, bias);
+      out[c / 2] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v0))) |
+                   (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v1))) << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(W + (e * N + n) * static_cast<size_t>(G) * 64 + g * 64 + 16 * part);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+}  // namespace
+
+cudaError_t launch_dequant(const uint32_t* qp, const uint32_t* sb, int E, int N, int K, int bits, uint16_t* W,
+                           cudaStream_t stream) {
+  const int G = K / 64;
+  const size_t total = static_cast<size_t>(E) * G * N * 4;
+  const int threads = 256;
+  const size_t blocks = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(blocks < 65536 ? blocks : 65536);
+  if (bits == 2)
+    dequant_kernel<2><<<grid, threads, 0, stream>>>(qp, sb, E, N, G, W);
+  else if (bits == 3)
+    dequant_kernel<3><<<grid, threads, 0, stream>>>(qp, sb, E, N, G, W);
+  else
+    dequant_kernel<4><<<grid, threads, 0, stream>>>(qp, sb, E, N, G, W);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prepack_codes(const uint32_t* q, int E, int N, int K, int bits, uint32_t* qp,
                                  cudaStream_t stream) {

@@ -131,6 +131,20 @@ moe_status moe_prepack_codes_bits(const uint32_t* q, int E, int N, int K, int bi
 moe_status moe_prepack_scales(const uint16_t* scale, const uint16_t* bias, int E, int N, int K,
                               uint32_t* sb, moe_stream stream);
 
+/* Expanded weights of one prepacked matrix m (E experts, N rows, K columns, b =
+ * `bits` bits per code): W[e][n][k] = q * scale + bias as fp16 (uint16 bit
+ * patterns, row-major [E][N][K], 2*E*N*K bytes, caller-owned device memory,
+ * 16-byte aligned).  The value is formed in fp32 with one fused multiply-add
+ * and rounded to fp16 once (exact for the synthetic weights, whose values
+ * need at most 11 significant bits); values beyond the fp16 range become
+ * infinities.  The layer itself never does this -- "Perplexity's Lily Beats
+ * MLX-LM on MacBook M5", section "Prefill: keep routing on the GPU, dequantize
+ * in flight": dequantising inside the GEMM instead of expanding the weights
+ * first gave +77.4% at 512 tokens -- it serves that comparison's unfused arm
+ * and checks of a weight set.  Asynchronous; allocates nothing.
+ * MOE_ERR_INVALID_ARG on a bad size, width or pointer. */
+moe_status moe_dequant_experts(const moe_qmat* m, int E, int N, int K, int bits, uint16_t* W, moe_stream stream);
+
 /* ------------------------------------------------------------------ routing
  * Output arrays of moe_route, all caller-owned device memory:
  *   ids        int32 [T][k]  selected experts, descending logit, lower index
