@@ -1074,8 +1074,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS) + ["sweep"],
-                    help="sweep: rows-per-expert and canvas-batching measurements (one JSON line)")
+    ap.add_argument("--workload", default="decode",
+                    choices=sorted(synth.CONFIGS) + ["sweep", "router", "topk_wide", "ablations"],
+                    help="sweep: rows-per-expert and canvas-batching measurements; router, topk_wide, ablations: "
+                         "those measurements of the default run alone (one JSON line each)")
     ap.add_argument("--no-secondary", action="store_true", help="skip the T=4096 prefill object")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--layers", type=int, default=0,
@@ -1102,9 +1104,16 @@ def main():
     peaks = measured_peaks()
     clocks = ClockSampler(dist.local_rank)
 
-    if args.workload == "sweep":
+    if args.workload in ("sweep", "router", "topk_wide", "ablations"):
         clocks.start()
-        res = run_sweep(dev, peaks, args)
+        if args.workload == "sweep":
+            res = run_sweep(dev, peaks, args)
+        elif args.workload == "router":
+            res = router_measure(dev, peaks)
+        elif args.workload == "topk_wide":
+            res = topk_wide_measure(dev, peaks)
+        else:
+            res = ablations_measure(dev, peaks)
         res["clocks"] = clocks.stop()
         if dist.rank == 0:
             print(json.dumps(res), flush=True)

@@ -497,29 +497,29 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
   // swizzle, or 16 bytes (2-bit), already conflict-free; 24 bytes (3-bit) in
   // two boxes of 64 rows, read as 8-byte units (conflict-free too)
   const CUtensorMapSwizzle code_swizzle = bits == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  auto enc_q = [&](CUtensorMap* map, const uint32_t* q, int ne, int N, int K) {
+  auto enc_q = [&](CUtensorMap* map, const uint32_t* q, int ne, int N, int K, int groups) {
     return bits == 3 ? encode_codes3(map, q, ne, N, K, kGemmBM / 2)
-                     : encode_codes(map, q, ne, N, K, kGemmBM, 1, code_swizzle, wpg);
+                     : encode_codes(map, q, ne, N, K, kGemmBM, groups, code_swizzle, wpg);
   };
   GemmMaps mr, ms;
   GemmActMaps act;
   uint16_t* hr = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_routed);
   uint16_t* hs = reinterpret_cast<uint16_t*>(wsb + L.gemm_h_shared);
   uint16_t* xh = reinterpret_cast<uint16_t*>(wsb + L.gemm_xh);
-  bool ok = enc_q(&mr.q_gate, routed->gate.q, E, I, d) &&
-            enc_q(&mr.q_up, routed->up.q, E, I, d) &&
-            enc_q(&mr.q_down, routed->down.q, E, d, I) &&
-            encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, 1) &&
-            encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, 1) &&
-            encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, 1) &&
+  bool ok = enc_q(&mr.q_gate, routed->gate.q, E, I, d, kGemmGroupsGU) &&
+            enc_q(&mr.q_up, routed->up.q, E, I, d, kGemmGroupsGU) &&
+            enc_q(&mr.q_down, routed->down.q, E, d, I, kGemmGroupsDown) &&
+            encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, kGemmGroupsGU) &&
+            encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, kGemmGroupsGU) &&
+            encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, kGemmGroupsDown) &&
             encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
   if (ok && shared)
-    ok = enc_q(&ms.q_gate, shared->gate.q, 1, I_shared, d) &&
-         enc_q(&ms.q_up, shared->up.q, 1, I_shared, d) &&
-         enc_q(&ms.q_down, shared->down.q, 1, d, I_shared) &&
-         encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, 1) &&
-         encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, 1) &&
-         encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, 1) &&
+    ok = enc_q(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmGroupsGU) &&
+         enc_q(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmGroupsGU) &&
+         enc_q(&ms.q_down, shared->down.q, 1, d, I_shared, kGemmGroupsDown) &&
+         encode_groups(&ms.sb_gate, shared->gate.sb, 1, I_shared, d, kGemmBM, kGemmGroupsGU) &&
+         encode_groups(&ms.sb_up, shared->up.sb, 1, I_shared, d, kGemmBM, kGemmGroupsGU) &&
+         encode_groups(&ms.sb_down, shared->down.sb, 1, d, I_shared, kGemmBM, kGemmGroupsDown) &&
          encode_act(&act.h_shared, hs, T, I_shared);
   if (ok && !shared) act.h_shared = act.h_routed;  // never read without a shared expert
   if (!ok) return MOE_ERR_CUDA;

@@ -53,24 +53,32 @@ static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns,
 template <bool kGateUp, int kBits>
 struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
+  static constexpr int kG = kGateUp ? kGemmGroupsGU : kGemmGroupsDown;  // quantisation groups (K = 64) per stage
   static constexpr int kDqWarps = 4 * kMats;
   static constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
-  static constexpr int kStages = kGateUp ? 6 : 8;
-  static constexpr int kAStages = kGateUp ? 2 : 4;
-  static constexpr int kACols = 32 * kMats;  // 64 fp16 per lane per matrix = 32 columns
-  // two accumulator buffers of two halves each: gate|up (gate/up GEMM) or the
-  // even|odd k-block partial sums (down GEMM)
+  static constexpr int kStages = kGateUp ? (kG > 1 ? 4 : 6) : 8 / kG;
+  static constexpr int kAStages = kGateUp ? 2 : 4 / kG;
+  static constexpr int kACols = 32 * kMats * kG;  // 64 fp16 per lane per matrix and group = 32 columns
+  // accumulator buffers of two halves each: gate|up (gate/up GEMM) or the
+  // even|odd stage partial sums (down GEMM).  The gate/up GEMM's two-group A
+  // stages leave TMEM room for one buffer only; the down GEMM keeps two, so
+  // its epilogue overlaps the next item's products.
+  static constexpr int kAccBufs = kGateUp ? (kG > 1 ? 1 : 2) : 2;
   static constexpr int kAccBufCols = 2 * kGemmBN;
-  static constexpr int kABase = 2 * kAccBufCols;
+  static constexpr int kABase = kAccBufs * kAccBufCols;
   static_assert(kABase + kAStages * kACols <= static_cast<int>(kTmemCols), "TMEM budget");
   // the down GEMM splits stages between its two issuers by parity; the stage
   // and A-stage rings must then agree on parity
   static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "stage rings must have even length");
-  static constexpr int kBBytes = kGemmBN * 128;  // token tile: up to kGemmBN rows x 64 fp16 (128-byte swizzle)
-  // 128 rows x (2 kBits) code words: 4-bit codes with a 32-byte swizzle, 2- and 3-bit codes (16 or 24
-  // bytes a row) plain
-  static constexpr int kQBytes = kGemmBM * 8 * kBits;
-  static constexpr int kSBBytes = kGemmBM * 4;
+  // token tile: one box of up to kGemmBN rows x 64 fp16 (128-byte swizzle) per group
+  static constexpr int kBBoxBytes = kGemmBN * 128;
+  static constexpr int kBBytes = kBBoxBytes * kG;
+  // per group, 128 rows x (2 kBits) code words: 4-bit codes with a 32-byte swizzle, 2- and 3-bit codes (16
+  // or 24 bytes a row) plain
+  static constexpr int kQBytesG = kGemmBM * 8 * kBits;
+  static constexpr int kQBytes = kQBytesG * kG;
+  static constexpr int kSBBytesG = kGemmBM * 4;
+  static constexpr int kSBBytes = kSBBytesG * kG;
   static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
   static constexpr int kStageBytes = (kStageTxBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
@@ -79,7 +87,7 @@ struct Cfg {
 };
 
 struct Item {
-  int e, row0, rows, mt, nk;
+  int e, row0, rows, mt, nk;  // nk: quantisation groups along K
   bool shared;
   bool ok;  // false: a malformed block-map entry; every role skips it
 };
@@ -115,6 +123,11 @@ __device__ __forceinline__ Item get_item(const GemmArgs& a, const Sched& s, int 
 }
 
 __device__ __forceinline__ int tile_n(int rows) { return max(16, (rows + 15) & ~15); }
+
+// pipeline stages of an item of nk groups, kG groups a stage (the last may
+// hold fewer)
+template <int kG>
+__device__ __forceinline__ int n_stages(int nk) { return (nk + kG - 1) / kG; }
 
 // Eight 4-bit codes of one word in the interleaved order of the prepacked
 // layout (code 2p in bits 4p, code 2p+1 in bits 4p+16) -> four f16x2 values of
@@ -265,11 +278,22 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
   // one k-block's codes of one 128-row tile: 4- and 2-bit codes one 3-D box;
   // 3-bit codes (24 bytes a row, a line of 8-byte units [E*K/64][N*3]) two
   // boxes of 64 rows, `half` choosing one
-  auto load_codes = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int mt, int eg, int half) {
-    if constexpr (kBits == 3)
-      tma_load_2d(dst + half * (C::kQBytes / 2), map, bar, (mt * kGemmBM + half * (kGemmBM / 2)) * 3, eg);
-    else
+  // one stage's codes of one 128-row tile from group eg on: 4- and 2-bit
+  // codes one 3-D box of kG groups; 3-bit codes (24 bytes a row, a line of
+  // 8-byte units [E*K/64][N*3]) two boxes of 64 rows per group.  Groups past
+  // the item's last are read (the next expert's, or zeros past the tensor) and
+  // then ignored.
+  auto load_codes = [&](uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int mt, int eg) {
+    if constexpr (kBits == 3) {
+#pragma unroll
+      for (int g = 0; g < C::kG; ++g)
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+          tma_load_2d(dst + g * C::kQBytesG + half * (C::kQBytesG / 2), map, bar,
+                      (mt * kGemmBM + half * (kGemmBM / 2)) * 3, eg + g);
+    } else {
       tma_load_3d(dst, map, bar, 0, mt * kGemmBM, eg);
+    }
   };
   auto fail = [&]() {
     record_status(a.status, MOE_ERR_TIMEOUT);
@@ -295,7 +319,8 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       const CUtensorMap* mb = (!kGateUp && m.shared) ? &act1 : &act0;
       const int brow = (kGateUp && m.shared) ? a.T * a.k + m.row0 : m.row0;
       if (lane == 0) {
-        for (int kb = 0; kb < m.nk; ++kb) {
+        for (int ks = 0; ks < n_stages<C::kG>(m.nk); ++ks) {
+          const int kb = ks * C::kG;  // first group of the stage
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             fail();
             ok = false;
@@ -306,16 +331,14 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
           uint8_t* sb_tile = q_tile + C::kMats * C::kQBytes;
           const int eg = m.e * m.nk + kb;
           mbar_arrive_expect_tx(&full[stage], C::kStageTxBytes);
-          tma_load_2d(st, mb, &full[stage], kb * 64, brow);
-          load_codes(q_tile, mq0, &full[stage], m.mt, eg, 0);
+#pragma unroll
+          for (int g = 0; g < C::kG; ++g)  // columns past the tensor's last are zeros
+            tma_load_2d(st + g * C::kBBoxBytes, mb, &full[stage], (kb + g) * 64, brow);
+          load_codes(q_tile, mq0, &full[stage], m.mt, eg);
           tma_load_3d(sb_tile, msb0, &full[stage], m.mt * kGemmBM, kb, m.e);
           if (kGateUp) {
-            load_codes(q_tile + C::kQBytes, mq1, &full[stage], m.mt, eg, 0);
+            load_codes(q_tile + C::kQBytes, mq1, &full[stage], m.mt, eg);
             tma_load_3d(sb_tile + C::kSBBytes, msb1, &full[stage], m.mt * kGemmBM, kb, m.e);
-          }
-          if (kBits == 3) {
-            load_codes(q_tile, mq0, &full[stage], m.mt, eg, 1);
-            if (kGateUp) load_codes(q_tile + C::kQBytes, mq1, &full[stage], m.mt, eg, 1);
           }
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -361,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       tc_fence_after();
       const uint32_t d = tmem + accb * C::kAccBufCols + who * kGemmBN;
       bool first = true;
-      for (int kb = 0; kb < m.nk; ++kb) {
+      for (int ks = 0; ks < n_stages<C::kG>(m.nk); ++ks) {
         const bool mine = kGateUp || ((stage & 1) == who);
         if (mine) {
           // a_full completes only after every dequantisation warp has seen
@@ -375,15 +398,20 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
           }
           tc_fence_after();
           if (elect_one()) {
-            // the four K = 16 slices of the stage: 32 bytes apart in the
-            // swizzled token tile (2 in the descriptor's address field), 8
-            // columns apart in the A stage
+            // the four K = 16 slices of each group: 32 bytes apart in the
+            // group's swizzled token box (2 in the descriptor's address
+            // field), 8 columns apart in the A stage; a group past the item's
+            // last multiplies zero weights by zero tokens
             const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (C::kStageBytes >> 4));
-            const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 : 0);
-            tc_mma_ts(d, a0, bd, idesc, first ? 0u : 1u);
-            tc_mma_ts(d, a0 + 8, bd + 2, idesc, 1u);
-            tc_mma_ts(d, a0 + 16, bd + 4, idesc, 1u);
-            tc_mma_ts(d, a0 + 24, bd + 6, idesc, 1u);
+            const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 * C::kG : 0);
+#pragma unroll
+            for (int g = 0; g < C::kG; ++g) {
+              const uint64_t bg = bd + static_cast<uint64_t>(g * (C::kBBoxBytes >> 4));
+              tc_mma_ts(d, a0 + 32 * g, bg, idesc, (first && g == 0) ? 0u : 1u);
+              tc_mma_ts(d, a0 + 32 * g + 8, bg + 2, idesc, 1u);
+              tc_mma_ts(d, a0 + 32 * g + 16, bg + 4, idesc, 1u);
+              tc_mma_ts(d, a0 + 32 * g + 24, bg + 6, idesc, 1u);
+            }
             tc_commit(&empty[stage]);
             tc_commit(&a_empty[astage]);
           }
@@ -399,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       if (!ok) break;
       if (lane == 0) tc_commit(&acc_full[accb]);  // arrives at once if this issuer had no k-block
       __syncwarp();
-      if (++accb == 2) {
+      if (++accb == C::kAccBufs) {
         accb = 0;
         accphase ^= 1;
       }
@@ -422,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     for (int it = blockIdx.x; it < s.n_total && ok; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) continue;
-      for (int kb = 0; kb < m.nk; ++kb) {
+      for (int ks = 0; ks < n_stages<C::kG>(m.nk); ++ks) {
         // every warp waits for itself: no warp holds the others back, and the
         // warps drift apart, so their bursts do not all compete for issue
         // slots with the MMA issuer at once
@@ -433,51 +461,66 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         }
         tc_fence_after();
         const uint8_t* st = stages + stage * C::kStageBytes;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols;
-        // the warp's 32 rows of its matrix, all 64 columns: the row's 32 code
-        // bytes are two 16-byte halves, swapped in rows where the 32-byte
-        // swizzle flips bit 4 of the address; half h holds words 4h .. 4h+3 =
-        // columns 32h .. 32h+31
-        const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes;
-        const uint32_t sbv = *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes +
-                                                                mat * C::kSBBytes + row * 4);
-        const float sf = __uint_as_float(sbv << 16);  // bf16 -> fp32 is exact
-        const float bf = __uint_as_float(sbv & 0xFFFF0000u);
-        const uint32_t s2 = f32x2_to_f16x2(sf, sf);
-        const uint32_t b2 = f32x2_to_f16x2(bf, bf);
-        if constexpr (kBits == 4) {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols +
+                               mat * 32 * C::kG;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
-            uint32_t v[16];
-            dequant_word(w.x, s2, b2, v + 0);
-            dequant_word(w.y, s2, b2, v + 4);
-            dequant_word(w.z, s2, b2, v + 8);
-            dequant_word(w.w, s2, b2, v + 12);
-            tmem_st16(taddr + mat * 32 + h * 16, v);
+        for (int g = 0; g < C::kG; ++g) {
+          const uint32_t tg = taddr + 32 * g;
+          if (g > 0 && ks * C::kG + g >= m.nk) {
+            // past the item's last group: zero weights (the token columns there are zeros too, but the codes
+            // and parameters read for them belong to another matrix)
+            uint32_t z[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) z[c] = 0u;
+            tmem_st16(tg, z);
+            tmem_st16(tg + 16, z);
+            continue;
           }
-        } else if constexpr (kBits == 3) {
-          // the row's 24 code bytes: low-bit words j = 0..3 (columns 16j .. 16j+15), then the high-bit
-          // words of blocks 0, 1 and 2, 3 (block 2i+1 in the upper byte of each half)
-          const uint2* rp = reinterpret_cast<const uint2*>(q_tile + row * 24);
-          const uint2 l01 = rp[0], l23 = rp[1], hh = rp[2];
-          uint32_t v[16];
-          dequant_word3(l01.x, hh.x, s2, b2, v + 0);
-          dequant_word3(l01.y, hh.x >> 8, s2, b2, v + 8);
-          tmem_st16(taddr + mat * 32, v);
-          dequant_word3(l23.x, hh.y, s2, b2, v + 0);
-          dequant_word3(l23.y, hh.y >> 8, s2, b2, v + 8);
-          tmem_st16(taddr + mat * 32 + 16, v);
-        } else {
-          // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
-          const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
-          uint32_t v[16];
-          dequant_word2(w.x, s2, b2, v + 0);
-          dequant_word2(w.y, s2, b2, v + 8);
-          tmem_st16(taddr + mat * 32, v);
-          dequant_word2(w.z, s2, b2, v + 0);
-          dequant_word2(w.w, s2, b2, v + 8);
-          tmem_st16(taddr + mat * 32 + 16, v);
+          // the warp's 32 rows of its matrix, all 64 columns of group g: the
+          // row's 32 code bytes are two 16-byte halves, swapped in rows where
+          // the 32-byte swizzle flips bit 4 of the address; half h holds words
+          // 4h .. 4h+3 = columns 32h .. 32h+31
+          const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes + g * C::kQBytesG;
+          const uint32_t sbv = *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes +
+                                                                  mat * C::kSBBytes + g * C::kSBBytesG + row * 4);
+          const float sf = __uint_as_float(sbv << 16);  // bf16 -> fp32 is exact
+          const float bf = __uint_as_float(sbv & 0xFFFF0000u);
+          const uint32_t s2 = f32x2_to_f16x2(sf, sf);
+          const uint32_t b2 = f32x2_to_f16x2(bf, bf);
+          if constexpr (kBits == 4) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
+              uint32_t v[16];
+              dequant_word(w.x, s2, b2, v + 0);
+              dequant_word(w.y, s2, b2, v + 4);
+              dequant_word(w.z, s2, b2, v + 8);
+              dequant_word(w.w, s2, b2, v + 12);
+              tmem_st16(tg + h * 16, v);
+            }
+          } else if constexpr (kBits == 3) {
+            // the row's 24 code bytes: low-bit words j = 0..3 (columns 16j .. 16j+15), then the high-bit
+            // words of blocks 0, 1 and 2, 3 (block 2i+1 in the upper byte of each half)
+            const uint2* rp = reinterpret_cast<const uint2*>(q_tile + row * 24);
+            const uint2 l01 = rp[0], l23 = rp[1], hh = rp[2];
+            uint32_t v[16];
+            dequant_word3(l01.x, hh.x, s2, b2, v + 0);
+            dequant_word3(l01.y, hh.x >> 8, s2, b2, v + 8);
+            tmem_st16(tg, v);
+            dequant_word3(l23.x, hh.y, s2, b2, v + 0);
+            dequant_word3(l23.y, hh.y >> 8, s2, b2, v + 8);
+            tmem_st16(tg + 16, v);
+          } else {
+            // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
+            const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
+            uint32_t v[16];
+            dequant_word2(w.x, s2, b2, v + 0);
+            dequant_word2(w.y, s2, b2, v + 8);
+            tmem_st16(tg, v);
+            dequant_word2(w.z, s2, b2, v + 0);
+            dequant_word2(w.w, s2, b2, v + 8);
+            tmem_st16(tg + 16, v);
+          }
         }
         tc_wait_st();
         tc_fence_before();
@@ -504,7 +547,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     const int row = lanegrp * 32 + lane;
     int accb = 0;
     uint32_t accphase = 0;
-    uint32_t kcount = 0;  // k-blocks of the items before this one (sets which issuer took a lone k-block)
+    uint32_t kcount = 0;  // stages of the items before this one (sets which issuer took a lone stage)
     for (int it = blockIdx.x; it < s.n_total; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) {
@@ -555,7 +598,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         // expert output rows: routed items in permuted order (row p of the
         // routing), shared-expert items after them in token order; the combine
         // kernel applies the routing weights and gathers rows back to tokens
-        const bool two = m.nk > 1;  // both halves hold partial sums unless the item has one k-block
+        const bool two = n_stages<C::kG>(m.nk) > 1;  // both halves hold partial sums unless the item has one stage
         const uint32_t h0 = two ? 0u : (kcount & 1u) * kGemmBN;
         const size_t row_base = (m.shared ? static_cast<size_t>(a.T) * a.k : 0) + m.row0;
         float* Yp = a.ypart + row_base * a.d + n;
@@ -573,11 +616,11 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
           }
         }
       }
-      kcount += static_cast<uint32_t>(m.nk);
+      kcount += static_cast<uint32_t>(n_stages<C::kG>(m.nk));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[accb]);
-      if (++accb == 2) {
+      if (++accb == C::kAccBufs) {
         accb = 0;
         accphase ^= 1;
       }

@@ -101,12 +101,16 @@ cudaError_t decode_debug(long long wait_limit_cycles, int drop_cta);
 
 // ---------------------------------------------------------------- prefill GEMM
 constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)
-constexpr int kGemmBK = 64;    // K per stage = one quantisation group
+constexpr int kGemmBK = 64;    // K of one quantisation group
+constexpr int kGemmGroupsGU = 2;    // quantisation groups per pipeline stage, gate/up GEMM
+constexpr int kGemmGroupsDown = 2;  // ... down GEMM
 constexpr int kGemmBN = 96;    // max tokens per tile (MMA N); two double-buffered accumulators fit TMEM
 
 struct GemmMaps {
-  CUtensorMap q_gate, q_up, q_down;     // codes, box (wpg words, 128 rows, 1); 32-byte swizzle for 4-bit codes
-  CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (128 rows, 1, 1)
+  // codes, box (wpg words, 128 rows, groups per stage); 32-byte swizzle for 4-bit codes.  3-bit codes: box
+  // (64 rows x 3 units, 1)
+  CUtensorMap q_gate, q_up, q_down;
+  CUtensorMap sb_gate, sb_up, sb_down;  // group parameters, box (128 rows, groups per stage, 1)
 };
 
 struct GemmArgs {
@@ -123,7 +127,7 @@ struct GemmArgs {
   uint16_t* Y;                // [T][d] bf16
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms, max_blocks;
-  int bits;  // bits per weight code: 4 or 2
+  int bits;  // bits per weight code: 4, 3 or 2
 };
 
 struct GemmActMaps {
