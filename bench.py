@@ -38,6 +38,8 @@ import numpy as np  # noqa: E402
 
 from bit_moe_expert_gb300 import synth  # noqa: E402
 
+TILE_ROWS = 128  # rows per tensor-core tile (moe_route block_rows) on the prefill path
+
 METRIC = "MoE layer tokens/s at T=1 decode (40 distinct chained layers); T=4096 prefill reported alongside"
 
 
@@ -228,7 +230,7 @@ class DecodeWorkload(Workload):
             self.logits_host.append(lh)
             self.X.append(torch.from_numpy(xh.view(np.int16)).to(dev))
             self.logits.append(torch.from_numpy(lh).to(dev))
-        self.block_rows = 96
+        self.block_rows = TILE_ROWS
         self.r = bm.Routing.empty(self.T, cfg.E, cfg.k, self.block_rows, dev)
         self.ws = bm.workspace(bm.moe_layer_workspace_bytes(self.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
         self.Y = torch.empty((self.L, self.T, cfg.d), dtype=torch.int16, device=dev)
@@ -344,7 +346,7 @@ class PrefillWorkload(Workload):
         self.logits_host = [synth.draw_logits(cfg, cfg.T, l) for l in range(self.sets)]
         self.X = torch.from_numpy(self.X_host.view(np.int16)).to(dev)
         self.logits = [torch.from_numpy(x).to(dev) for x in self.logits_host]
-        self.block_rows = 96
+        self.block_rows = TILE_ROWS
         C = self.chunk
         self.r = bm.Routing.empty(C, cfg.E, cfg.k, self.block_rows, dev)
         self.ws_r = bm.workspace(bm.moe_route_workspace_bytes(C, cfg.E, cfg.k), dev)
@@ -693,7 +695,7 @@ def run_sweep(dev, peaks, args):
 
     def point(cfg, T, logits_np, sets, steps):
         C = T
-        r = bm.Routing.empty(C, cfg.E, cfg.k, 96, dev)
+        r = bm.Routing.empty(C, cfg.E, cfg.k, TILE_ROWS, dev)
         ws_r = bm.workspace(bm.moe_route_workspace_bytes(C, cfg.E, cfg.k), dev)
         ws_f = bm.workspace(bm.moe_forward_workspace_bytes(C, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared), dev)
         X = torch.from_numpy(synth.draw_x(cfg, C, 0).view(np.int16)).to(dev)
@@ -701,7 +703,7 @@ def run_sweep(dev, peaks, args):
         Y = torch.empty((C, cfg.d), dtype=torch.int16, device=dev)
 
         def call(i):
-            bm.moe_route(lg, cfg.k, 96, r, ws_r)
+            bm.moe_route(lg, cfg.k, TILE_ROWS, r, ws_r)
             bm.moe_forward(X, sets[i % len(sets)][0], sets[i % len(sets)][1], r, Y, ws_f)
 
         s = torch.cuda.Stream(device=dev)
@@ -844,7 +846,7 @@ def ablations_measure(dev, peaks, calls=20):
     sets = [_dev_layer(cfg, l, dev)[2:] for l in range(nsets)]
     X = torch.from_numpy(synth.draw_x(cfg, T, 0).view(np.int16)).to(dev)
     lg = torch.from_numpy(synth.draw_logits(cfg, T, 0)).to(dev)
-    r = bm.Routing.empty(T, E, k, 96, dev)
+    r = bm.Routing.empty(T, E, k, TILE_ROWS, dev)
     ws_r = bm.workspace(bm.moe_route_workspace_bytes(T, E, k), dev)
     ws_f = bm.workspace(bm.moe_forward_workspace_bytes(T, d, I, E, k, Ish), dev)
     Y = torch.empty((T, d), dtype=torch.int16, device=dev)
@@ -869,7 +871,7 @@ def ablations_measure(dev, peaks, calls=20):
         return e0.elapsed_time(e1) / calls * 1e3  # us per call
 
     def fused(i):
-        bm.moe_route(lg, k, 96, r, ws_r)
+        bm.moe_route(lg, k, TILE_ROWS, r, ws_r)
         bm.moe_forward(X, sets[i % nsets][0], sets[i % nsets][1], r, Y, ws_f)
 
     t_fused = timed_graph(fused)
@@ -878,7 +880,7 @@ def ablations_measure(dev, peaks, calls=20):
     Y_fused = Y.clone()
 
     # unfused: static padding layout from this layer's routing (the same every call)
-    bm.moe_route(lg, k, 96, r, ws_r)
+    bm.moe_route(lg, k, TILE_ROWS, r, ws_r)
     torch.cuda.synchronize()
     counts = r.counts.cpu().numpy()
     Mmax = int(counts.max())
@@ -897,7 +899,7 @@ def ablations_measure(dev, peaks, calls=20):
 
     def unfused(i):
         routed, shared = sets[i % nsets]
-        bm.moe_route(lg, k, 96, r, ws_r)
+        bm.moe_route(lg, k, TILE_ROWS, r, ws_r)
         for m in ("gate", "up", "down"):
             bm.moe_dequant_experts(getattr(routed, m), routed.bits, W16[m])
             bm.moe_dequant_experts(getattr(shared, m), shared.bits, Ws16[m])
@@ -932,7 +934,7 @@ def ablations_measure(dev, peaks, calls=20):
 
     def host_routing(i):
         routed, shared = sets[i % nsets]
-        bm.moe_route(lg, k, 96, r, ws_r)  # its top-k (ids, w) is what the host receives
+        bm.moe_route(lg, k, TILE_ROWS, r, ws_r)  # its top-k (ids, w) is what the host receives
         ids_h.copy_(r.ids, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         ids = ids_h.numpy().reshape(-1)
@@ -944,8 +946,8 @@ def ablations_measure(dev, peaks, calls=20):
         inv[order] = np.arange(order.size, dtype=np.int32)
         bmap = []
         for e in np.nonzero(cnt)[0]:
-            for r0 in range(0, int(cnt[e]), 96):
-                bmap += [int(e), int(off[e]) + r0, min(96, int(cnt[e]) - r0)]
+            for r0 in range(0, int(cnt[e]), TILE_ROWS):
+                bmap += [int(e), int(off[e]) + r0, min(TILE_ROWS, int(cnt[e]) - r0)]
         bufs["counts"].numpy()[:] = cnt
         bufs["offsets"].numpy()[:] = off
         bufs["perm"].numpy()[:] = order

@@ -56,20 +56,17 @@ struct Cfg {
   static constexpr int kG = kGateUp ? kGemmGroupsGU : kGemmGroupsDown;  // quantisation groups (K = 64) per stage
   static constexpr int kDqWarps = 4 * kMats;
   static constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
-  static constexpr int kStages = kGateUp ? (kG > 1 ? 4 : 6) : 8 / kG;
-  static constexpr int kAStages = kGateUp ? 2 : 4 / kG;
+  static constexpr int kStages = 4;
+  static constexpr int kAStages = kGateUp ? 2 : 4;
   static constexpr int kACols = 32 * kMats * kG;  // 64 fp16 per lane per matrix and group = 32 columns
-  // accumulator buffers of two halves each: gate|up (gate/up GEMM) or the
-  // even|odd stage partial sums (down GEMM).  The gate/up GEMM's two-group A
-  // stages leave TMEM room for one buffer only; the down GEMM keeps two, so
-  // its epilogue overlaps the next item's products.
-  static constexpr int kAccBufs = kGateUp ? (kG > 1 ? 1 : 2) : 2;
-  static constexpr int kAccBufCols = 2 * kGemmBN;
+  // accumulators: gate|up in one buffer (the gate/up GEMM's two-group A stages
+  // leave TMEM room for one), the down GEMM's in two, so that its epilogue
+  // overlaps the next item's products
+  static constexpr int kAccBufs = kGateUp ? 1 : 2;
+  static constexpr int kAccBufCols = kMats * kGemmBN;
   static constexpr int kABase = kAccBufs * kAccBufCols;
   static_assert(kABase + kAStages * kACols <= static_cast<int>(kTmemCols), "TMEM budget");
-  // the down GEMM splits stages between its two issuers by parity; the stage
-  // and A-stage rings must then agree on parity
-  static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "stage rings must have even length");
+  static constexpr int kMmaIssuers = kMats;  // gate/up: one per matrix; down: one
   // token tile: one box of up to kGemmBN rows x 64 fp16 (128-byte swizzle) per group
   static constexpr int kBBoxBytes = kGemmBN * 128;
   static constexpr int kBBytes = kBBoxBytes * kG;
@@ -82,8 +79,8 @@ struct Cfg {
   static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
   static constexpr int kStageBytes = (kStageTxBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
-  static constexpr int kEmptyArrivals = kDqWarps + (kGateUp ? 2 : 1);  // dequant warps + MMA commits
-  static constexpr int kAEmptyArrivals = kGateUp ? 2 : 1;
+  static constexpr int kEmptyArrivals = kDqWarps + kMmaIssuers;  // dequant warps + MMA commits
+  static constexpr int kAEmptyArrivals = kMmaIssuers;
 };
 
 struct Item {
@@ -234,7 +231,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       mbar_init(&a_empty[i], C::kAEmptyArrivals);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 2);  // one commit per MMA issuer
+      mbar_init(&acc_full[i], C::kMmaIssuers);  // one commit per MMA issuer
       mbar_init(&acc_empty[i], kEpiWarps);
     }
     mbar_init(&done[0], 1);
@@ -358,13 +355,12 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         }
     }
     __syncwarp();
+  } else if (warp == kMmaWarp0 + 1 && C::kMmaIssuers == 1) {
+    // the down GEMM's second MMA warp idles
   } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
     // ------------------------------------------------------------ MMA issuers
     // gate/up: issuer 0 multiplies the gate tile, issuer 1 the up tile, both
-    // over every stage.  down: each issuer owns the stages (and A stages) of
-    // one parity and accumulates its k-blocks into its own half of the buffer;
-    // a fixed stage-to-issuer map means every issuer waits on every phase of
-    // the barriers it uses, so no wait can mistake an old phase for the next.
+    // over every stage.  down: one issuer.
     const int who = warp - kMmaWarp0;
     // shared-memory addresses stay below 2^18, so the descriptor's 14-bit
     // address field never carries into its neighbours
@@ -385,39 +381,36 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       const uint32_t d = tmem + accb * C::kAccBufCols + who * kGemmBN;
       bool first = true;
       for (int ks = 0; ks < n_stages<C::kG>(m.nk); ++ks) {
-        const bool mine = kGateUp || ((stage & 1) == who);
-        if (mine) {
-          // a_full completes only after every dequantisation warp has seen
-          // full[stage] complete (the stage's token tile has landed) and
-          // arrived with release semantics, so waiting on a_full alone orders
-          // these MMAs after the tile's TMA writes as well
-          if (!mbar_wait(&a_full[astage], aphase, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (elect_one()) {
-            // the four K = 16 slices of each group: 32 bytes apart in the
-            // group's swizzled token box (2 in the descriptor's address
-            // field), 8 columns apart in the A stage; a group past the item's
-            // last multiplies zero weights by zero tokens
-            const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (C::kStageBytes >> 4));
-            const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 * C::kG : 0);
-#pragma unroll
-            for (int g = 0; g < C::kG; ++g) {
-              const uint64_t bg = bd + static_cast<uint64_t>(g * (C::kBBoxBytes >> 4));
-              tc_mma_ts(d, a0 + 32 * g, bg, idesc, (first && g == 0) ? 0u : 1u);
-              tc_mma_ts(d, a0 + 32 * g + 8, bg + 2, idesc, 1u);
-              tc_mma_ts(d, a0 + 32 * g + 16, bg + 4, idesc, 1u);
-              tc_mma_ts(d, a0 + 32 * g + 24, bg + 6, idesc, 1u);
-            }
-            tc_commit(&empty[stage]);
-            tc_commit(&a_empty[astage]);
-          }
-          __syncwarp();
-          first = false;
+        // a_full completes only after every dequantisation warp has seen
+        // full[stage] complete (the stage's token tile has landed) and
+        // arrived with release semantics, so waiting on a_full alone orders
+        // these MMAs after the tile's TMA writes as well
+        if (!mbar_wait(&a_full[astage], aphase, abort_flag)) {
+          fail();
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        if (elect_one()) {
+          // the four K = 16 slices of each group: 32 bytes apart in the
+          // group's swizzled token box (2 in the descriptor's address
+          // field), 8 columns apart in the A stage; a group past the item's
+          // last multiplies zero weights by zero tokens
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage * (C::kStageBytes >> 4));
+          const uint32_t a0 = tmem + C::kABase + astage * C::kACols + (kGateUp ? who * 32 * C::kG : 0);
+#pragma unroll
+          for (int g = 0; g < C::kG; ++g) {
+            const uint64_t bg = bd + static_cast<uint64_t>(g * (C::kBBoxBytes >> 4));
+            tc_mma_ts(d, a0 + 32 * g, bg, idesc, (first && g == 0) ? 0u : 1u);
+            tc_mma_ts(d, a0 + 32 * g + 8, bg + 2, idesc, 1u);
+            tc_mma_ts(d, a0 + 32 * g + 16, bg + 4, idesc, 1u);
+            tc_mma_ts(d, a0 + 32 * g + 24, bg + 6, idesc, 1u);
+          }
+          tc_commit(&empty[stage]);
+          tc_commit(&a_empty[astage]);
+        }
+        __syncwarp();
+        first = false;
         if (++stage == C::kStages) stage = 0;
         if (++astage == C::kAStages) {
           astage = 0;
@@ -543,11 +536,10 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ep = warp - kEpiWarp0;
     const int lanegrp = warp & 3;
-    const int colhalf = ep >> 2;  // this warp handles columns [48*colhalf, 48*colhalf + 48)
+    const int colhalf = ep >> 2;  // this warp handles columns [colhalf * kGemmBN / 2, (colhalf + 1) * kGemmBN / 2)
     const int row = lanegrp * 32 + lane;
     int accb = 0;
     uint32_t accphase = 0;
-    uint32_t kcount = 0;  // stages of the items before this one (sets which issuer took a lone stage)
     for (int it = blockIdx.x; it < s.n_total; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) {
@@ -598,25 +590,20 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         // expert output rows: routed items in permuted order (row p of the
         // routing), shared-expert items after them in token order; the combine
         // kernel applies the routing weights and gathers rows back to tokens
-        const bool two = n_stages<C::kG>(m.nk) > 1;  // both halves hold partial sums unless the item has one stage
-        const uint32_t h0 = two ? 0u : (kcount & 1u) * kGemmBN;
         const size_t row_base = (m.shared ? static_cast<size_t>(a.T) * a.k : 0) + m.row0;
         float* Yp = a.ypart + row_base * a.d + n;
         const int c_valid = min(c_end, m.rows);
         for (int c0 = c_begin; c0 < c_end; c0 += 16) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tbase + h0 + c0, v0);
-          tmem_ld16(tbase + kGemmBN + c0, v1);
+          uint32_t v[16];
+          tmem_ld16(tbase + c0, v);
           tc_wait_ld();
           if (n < a.d) {
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              if (c0 + c < c_valid)
-                Yp[static_cast<size_t>(c0 + c) * a.d] = __uint_as_float(v0[c]) + (two ? __uint_as_float(v1[c]) : 0.0f);
+              if (c0 + c < c_valid) Yp[static_cast<size_t>(c0 + c) * a.d] = __uint_as_float(v[c]);
           }
         }
       }
-      kcount += static_cast<uint32_t>(n_stages<C::kG>(m.nk));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[accb]);

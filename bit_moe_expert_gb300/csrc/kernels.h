@@ -104,7 +104,7 @@ constexpr int kGemmBM = 128;   // weight rows per tile (MMA M)
 constexpr int kGemmBK = 64;    // K of one quantisation group
 constexpr int kGemmGroupsGU = 2;    // quantisation groups per pipeline stage, gate/up GEMM
 constexpr int kGemmGroupsDown = 2;  // ... down GEMM
-constexpr int kGemmBN = 96;    // max tokens per tile (MMA N); two double-buffered accumulators fit TMEM
+constexpr int kGemmBN = 128;   // max tokens per tile (MMA N)
 
 struct GemmMaps {
   // codes, box (wpg words, 128 rows, groups per stage); 32-byte swizzle for 4-bit codes.  3-bit codes: box

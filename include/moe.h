@@ -187,9 +187,9 @@ size_t moe_route_workspace_bytes(int T, int E, int k);
 /* fp32 router logits [T][E] (row-major) -> all arrays of *out.  One kernel
  * launch, no host synchronisation.  Preconditions: T >= 0 (T = 0 writes zero
  * counts, offsets and num_blocks), 1 <= E <= 1024, 1 <= k <= min(E, 32),
- * 1 <= block_rows <= 128 (moe_forward's tensor-core path, T > 4, takes at most
- * 96: route with block_rows <= 96 when the routing feeds it).  Logits must be
- * finite: a NaN or infinity leaves a
+ * 1 <= block_rows <= 128 (the tile height of moe_forward's tensor-core path,
+ * T > 4, whose MMA N is the tile's row count rounded up to 16).  Logits must
+ * be finite: a NaN or infinity leaves a
  * deterministic but meaningless selection and records MOE_ERR_NONFINITE in
  * the workspace status word.  Sets out->block_rows. */
 moe_status moe_route(const float* logits, int T, int E, int k, int block_rows, moe_routing* out,
@@ -249,8 +249,8 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  *   routed   E = routed->n_experts experts, I columns of intermediate
  *   shared   NULL, or one always-on expert (n_experts = 1) with I_shared
  *   r        the routing written by moe_route for the same T, E, k on this
- *            stream; the tensor-core path (below) needs block_rows <= 96
- *            and returns MOE_ERR_UNSUPPORTED otherwise
+ *            stream (block_rows <= 128, as moe_route accepts; a routing
+ *            struct claiming more is refused with MOE_ERR_UNSUPPORTED)
  * Preconditions: T >= 0 (T = 0 does nothing), d, I and I_shared multiples of
  * 64 (I_shared = 0 iff shared is NULL), 1 <= k <= min(E, 32), E <= 1024.
  * Path: T <= 4 runs the decode kernel (every active expert's bytes streamed

@@ -2,7 +2,7 @@
 of the rows-per-expert sweep.
 
 The layer runs on the GPU exactly as the benchmark runs it (moe_route with
-96-row tiles, then moe_forward on the same chunk); the CPU oracle -- the same
+128-row tiles, then moe_forward on the same chunk); the CPU oracle -- the same
 single-threaded C routine as everywhere, unchanged -- runs on several host
 threads over disjoint token ranges (it keeps no state between calls, and the
 foreign call releases the interpreter lock), so that every token of a
@@ -75,7 +75,10 @@ def _report(what, Y, Y64, Y16):
     return e
 
 
-def _gpu_chunk(dl, logits_np, k, block_rows=96):
+TILE = 128  # rows per tensor-core tile, as the benchmark routes
+
+
+def _gpu_chunk(dl, logits_np, k, block_rows=TILE):
     r, _ = G.route_gpu(logits_np, k, block_rows)
     return r, dl.forward(r)
 
@@ -87,7 +90,7 @@ def test_full_layer_every_token(name):
     dl = G.DeviceLayer.from_device_draw(cfg, 0, T)
     r, Y = _gpu_chunk(dl, dl.logits, cfg.k)
     rh = G.routing_to_host(r)
-    ref = oracle.route(dl.logits, cfg.k, 96)
+    ref = oracle.route(dl.logits, cfg.k, TILE)
     G.assert_routing_equal(rh, ref)
     Y64, Y16 = _oracle_tokens(dl.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"], range(T))
     _report(f"{name}, all {T} tokens", Y, Y64, Y16)
@@ -102,8 +105,8 @@ def test_long_prefill_chunk_every_token_and_every_chunk_routing():
     X_all, lg_all = dl.X_host, dl.logits
     for c in range(cfg.T // C):
         lg = np.ascontiguousarray(lg_all[c * C:(c + 1) * C])
-        r, _ = G.route_gpu(lg, cfg.k, 96)
-        G.assert_routing_equal(G.routing_to_host(r), oracle.route(lg, cfg.k, 96))
+        r, _ = G.route_gpu(lg, cfg.k, TILE)
+        G.assert_routing_equal(G.routing_to_host(r), oracle.route(lg, cfg.k, TILE))
     # chunk 0 through the layer, as the benchmark runs it
     dl0 = G.DeviceLayer(np.ascontiguousarray(X_all[:C]), np.ascontiguousarray(lg_all[:C]), dl.routed_host,
                         dl.shared_host, dl.routed, dl.shared)
@@ -123,28 +126,29 @@ def _uniform_logits(T, E, k):
     return lg
 
 
-@pytest.mark.parametrize("M", [1, 8, 64, 128])
-def test_uniform_rows_per_expert(M):
+@pytest.mark.parametrize("M,tile", [(1, TILE), (8, TILE), (64, TILE), (128, TILE), (128, 96), (160, TILE)])
+def test_uniform_rows_per_expert(M, tile):
     """The sweep's routing: the decode layer's dimensions with every expert
-    given exactly M rows (T = 32 M tokens).  At M = 128 each expert's rows
-    split into a 96-row and a 32-row tile.  Every token is compared up to
-    M = 8; beyond, tokens from every expert's first and last tile."""
+    given exactly M rows (T = 32 M tokens).  At M = 128 each expert fills one
+    128-row tile, or splits into a 96-row and a 32-row tile; at M = 160 into
+    a 128-row and a 32-row tile.  Every token is compared up to M = 8; beyond,
+    tokens from every expert's first and last tile."""
     cfg = synth.CONFIGS["decode"]
     T = M * cfg.E // cfg.k
     dl = G.DeviceLayer.from_device_draw(cfg, 3, T)
     lg = _uniform_logits(T, cfg.E, cfg.k)
-    r, Y = _gpu_chunk(dl, lg, cfg.k)
+    r, Y = _gpu_chunk(dl, lg, cfg.k, tile)
     rh = G.routing_to_host(r)
-    ref = oracle.route(lg, cfg.k, 96)
+    ref = oracle.route(lg, cfg.k, tile)
     G.assert_routing_equal(rh, ref)
     assert np.all(rh["counts"] == M)
     if M <= 8:
         tokens = np.arange(T)
     else:
         # expert e's rows are tokens t with (8 t + j) mod 256 = e: its first rows come from the first tokens and
-        # its last rows (the second tile when M > 96) from the last ones
+        # its last rows (its last tile) from the last ones
         rng = np.random.default_rng(M)
         tokens = np.unique(np.concatenate([np.arange(16), np.arange(T - 16, T),
                                            rng.choice(T, size=32, replace=False)]))
     Y64, Y16 = _oracle_tokens(dl.X_host, dl.routed_host, dl.shared_host, rh["ids"], rh["w"], tokens)
-    _report(f"uniform M={M} (T={T}), {len(tokens)} tokens", Y[tokens], Y64, Y16)
+    _report(f"uniform M={M} (T={T}, {tile}-row tiles), {len(tokens)} tokens", Y[tokens], Y64, Y16)

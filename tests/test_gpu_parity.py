@@ -174,16 +174,20 @@ def test_forward_small(name, kw, path):
     G.assert_y_close(Y, Y64, f"{name}/{path}")
 
 
-@pytest.mark.parametrize("block_rows", [1, 16, 32, 50, 64, 96])
-def test_forward_gemm_block_rows(block_rows):
-    cfg = synth.small_config(T=200, d=256, E=8, k=2, I=128, I_shared=128)
+@pytest.mark.parametrize("block_rows,T,E", [(1, 200, 8), (16, 200, 8), (32, 200, 8), (50, 200, 8), (64, 200, 8),
+                                             (96, 200, 8), (128, 200, 8), (128, 600, 4), (96, 600, 4)])
+def test_forward_gemm_block_rows(block_rows, T, E):
+    """Tiles of every height up to the 128-row maximum; with T = 600 over four
+    experts each expert fills two 128-row tiles (or three of 96) and a ragged
+    one, and the shared expert's 600 tokens make four full tiles and a tail."""
+    cfg = synth.small_config(T=T, d=256, E=E, k=2, I=128, I_shared=128)
     layer = synth.draw_layer(cfg)
     dl = G.DeviceLayer.from_host(layer)
     r, _ = G.route_gpu(layer.logits, cfg.k, block_rows)
     rh = G.routing_to_host(r)
     Y = dl.forward(r, "gemm")
     Y64, _ = oracle.forward(layer.X, layer.routed, layer.shared, rh["ids"], rh["w"])
-    G.assert_y_close(Y, Y64, f"block_rows={block_rows}")
+    G.assert_y_close(Y, Y64, f"block_rows={block_rows}, T={T}, E={E}")
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4])
@@ -209,13 +213,15 @@ def test_forward_decode_rejects_more_than_4_tokens():
     assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
 
 
-def test_forward_gemm_rejects_tiles_over_96_rows():
-    """The tensor-core path holds at most 96 tokens per tile; a routing made
-    with taller tiles is refused before any launch."""
+def test_forward_gemm_rejects_routing_over_128_rows():
+    """The tensor-core path holds at most 128 tokens per tile (moe_route's
+    own limit); a routing struct that claims taller tiles is refused before
+    any launch."""
     cfg = synth.small_config(T=40, d=128, E=4, k=2, I=64, I_shared=0)
     layer = synth.draw_layer(cfg)
     dl = G.DeviceLayer.from_host(layer)
     r, _ = G.route_gpu(layer.logits, cfg.k, 128)
+    r.block_rows = 129
     with pytest.raises(bm.MoeError) as ei:
         dl.forward(r, "gemm")
     assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
