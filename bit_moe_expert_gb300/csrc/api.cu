@@ -140,6 +140,15 @@ bool encode_act(CUtensorMap* map, const uint16_t* p, int rows, int cols) {
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// fp32 expert outputs [rows][cols]: boxes of 32 columns x 16 rows (the down
+// GEMM's epilogue stores one warp's 32 weight rows for 16 tokens at a time)
+bool encode_out(CUtensorMap* map, const float* p, int rows, int cols) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  const cuuint32_t box[2] = {32, 16};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // group parameters sb [E][K/64][N] uint32
 bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_rows,
                    cuuint32_t box_groups) {
@@ -512,7 +521,8 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
             encode_groups(&mr.sb_gate, routed->gate.sb, E, I, d, kGemmBM, kGemmGroupsGU) &&
             encode_groups(&mr.sb_up, routed->up.sb, E, I, d, kGemmBM, kGemmGroupsGU) &&
             encode_groups(&mr.sb_down, routed->down.sb, E, d, I, kGemmBM, kGemmGroupsDown) &&
-            encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I);
+            encode_act(&act.x, xh, A + (shared ? T : 0), d) && encode_act(&act.h_routed, hr, A, I) &&
+            encode_out(&act.ypart, reinterpret_cast<const float*>(wsb + L.gemm_ypart), A + (shared ? T : 0), d);
   if (ok && shared)
     ok = enc_q(&ms.q_gate, shared->gate.q, 1, I_shared, d, kGemmGroupsGU) &&
          enc_q(&ms.q_up, shared->up.q, 1, I_shared, d, kGemmGroupsGU) &&

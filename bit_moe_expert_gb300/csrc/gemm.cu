@@ -78,7 +78,10 @@ struct Cfg {
   static constexpr int kSBBytes = kSBBytesG * kG;
   static constexpr int kStageTxBytes = kBBytes + kMats * (kQBytes + kSBBytes);
   static constexpr int kStageBytes = (kStageTxBytes + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
+  // down GEMM epilogue: per epilogue warp two staging buffers of [16 tokens][32 rows] fp32 for its TMA stores
+  static constexpr int kEpiBufFloats = 16 * 32;
+  static constexpr int kEpiStageBytes = kGateUp ? 0 : kEpiWarps * 2 * kEpiBufFloats * 4;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiStageBytes + 1024 /*barriers etc.*/ + 1024 /*align*/;
   static constexpr int kEmptyArrivals = kDqWarps + kMmaIssuers;  // dequant warps + MMA commits
   static constexpr int kAEmptyArrivals = kMmaIssuers;
 };
@@ -202,12 +205,14 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
                     const __grid_constant__ CUtensorMap sb0_r, const __grid_constant__ CUtensorMap sb1_r,
                     const __grid_constant__ CUtensorMap q0_s, const __grid_constant__ CUtensorMap q1_s,
                     const __grid_constant__ CUtensorMap sb0_s, const __grid_constant__ CUtensorMap sb1_s,
-                    const __grid_constant__ CUtensorMap act0, const __grid_constant__ CUtensorMap act1, GemmArgs a) {
+                    const __grid_constant__ CUtensorMap act0, const __grid_constant__ CUtensorMap act1,
+                    const __grid_constant__ CUtensorMap out_map, GemmArgs a) {
   using C = Cfg<kGateUp, kBits>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  float* epi_stage = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kEpiStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + C::kStages;
   uint64_t* a_full = empty + C::kStages;
@@ -540,6 +545,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     const int row = lanegrp * 32 + lane;
     int accb = 0;
     uint32_t accphase = 0;
+    uint32_t nstore = 0;  // TMA stores issued by this warp (down GEMM), alternating its two staging buffers
     for (int it = blockIdx.x; it < s.n_total; it += gridDim.x) {
       const Item m = get_item(a, s, it, kGateUp);
       if (!m.ok) {
@@ -589,18 +595,35 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       } else {
         // expert output rows: routed items in permuted order (row p of the
         // routing), shared-expert items after them in token order; the combine
-        // kernel applies the routing weights and gathers rows back to tokens
+        // kernel applies the routing weights and gathers rows back to tokens.
+        // A full round of 16 tokens goes out as one TMA store of the warp's 32
+        // rows, staged in shared memory; a partial round (the item's last
+        // rows) as plain stores, so that no row past the item is written.
         const size_t row_base = (m.shared ? static_cast<size_t>(a.T) * a.k : 0) + m.row0;
-        float* Yp = a.ypart + row_base * a.d + n;
+        const int n0 = m.mt * kGemmBM + lanegrp * 32;
         const int c_valid = min(c_end, m.rows);
         for (int c0 = c_begin; c0 < c_end; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tbase + c0, v);
           tc_wait_ld();
-          if (n < a.d) {
+          if (c_valid - c0 >= 16) {
+            float* buf = epi_stage + (ep * 2 + (nstore & 1u)) * C::kEpiBufFloats;
+            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) buf[c * 32 + lane] = __uint_as_float(v[c]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&out_map, buf, n0, static_cast<int>(row_base + c0));
+              bulk_commit_group();
+            }
+            ++nstore;
+          } else if (n < a.d) {
+            float* Yp = a.ypart + (row_base + c0) * a.d + n;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              if (c0 + c < c_valid) Yp[static_cast<size_t>(c0 + c) * a.d] = __uint_as_float(v[c]);
+              if (c0 + c < c_valid) Yp[static_cast<size_t>(c) * a.d] = __uint_as_float(v[c]);
           }
         }
       }
@@ -612,6 +635,8 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         accphase ^= 1;
       }
     }
+    if (!kGateUp && lane == 0) bulk_wait_group_all();  // the staged stores are done before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -775,7 +800,8 @@ cudaError_t launch_gemm_t(const GemmArgs& a, const GemmMaps* routed, const GemmM
   cfg.blockDim = dim3(CG::kThreads);
   timer_begin(kKGemmGateUp, stream);
   cudaError_t err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true, kBits>, routed->q_gate, routed->q_up, routed->sb_gate,
-                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x, a);
+                                       routed->sb_up, sh->q_gate, sh->q_up, sh->sb_gate, sh->sb_up, act->x, act->x,
+                                       act->ypart, a);
   timer_end(kKGemmGateUp, stream);
   if (err != cudaSuccess) return err;
 
@@ -785,7 +811,7 @@ cudaError_t launch_gemm_t(const GemmArgs& a, const GemmMaps* routed, const GemmM
   timer_begin(kKGemmDown, stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<false, kBits>, routed->q_down, routed->q_down, routed->sb_down,
                            routed->sb_down, sh->q_down, sh->q_down, sh->sb_down, sh->sb_down, act->h_routed,
-                           act->h_shared, a);
+                           act->h_shared, act->ypart, a);
   timer_end(kKGemmDown, stream);
   if (err != cudaSuccess) return err;
 

@@ -134,6 +134,7 @@ struct GemmActMaps {
   CUtensorMap x;         // gathered X [A + T][d] fp16, box (64, kGemmBN), 128-byte swizzle
   CUtensorMap h_routed;  // H [A][I] fp16, box (64, kGemmBN), 128-byte swizzle
   CUtensorMap h_shared;  // H [T][I_shared] fp16, same box
+  CUtensorMap ypart;     // expert outputs [A + T][d] fp32, box (32, 16): the down GEMM's stores
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, const GemmMaps* routed, const GemmMaps* shared, const GemmActMaps* act,

@@ -133,6 +133,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Tiled shared -> global store of one 2-D box, in this thread's current bulk
+// async group.  The writes to the shared-memory source must be made visible
+// to the async proxy first (fence_proxy_async_smem by the writing threads,
+// then a barrier among them).  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most kPending of this thread's bulk groups still read their
+// shared-memory sources (their buffers may then be rewritten).
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+// Wait until all of this thread's bulk groups are complete (writes performed).
+__device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Contiguous global -> shared copy of `bytes` (a multiple of 16; both
 // addresses 16-byte aligned) that completes `bytes` of the mbarrier's
 // transaction count.
