@@ -461,6 +461,50 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         const uint8_t* st = stages + stage * C::kStageBytes;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + C::kABase + astage * C::kACols +
                                mat * 32 * C::kG;
+        // every code word and group parameter of this row in the stage is
+        // loaded before any is used, so that the loads' latency is paid once
+        // (the TMEM stores below are ordered memory operations, which the
+        // compiler does not move loads across)
+        const uint8_t* q_base = st + C::kBBytes + mat * C::kQBytes;
+        const uint8_t* sb_base = st + C::kBBytes + C::kMats * C::kQBytes + mat * C::kSBBytes + row * 4;
+        constexpr int kRaw = 2 * kBits;  // code words of one row and group
+        uint32_t raw[C::kG][kRaw], sbv[C::kG];
+#pragma unroll
+        for (int g = 0; g < C::kG; ++g) {
+          const uint8_t* q_tile = q_base + g * C::kQBytesG;
+          sbv[g] = *reinterpret_cast<const uint32_t*>(sb_base + g * C::kSBBytesG);
+          if constexpr (kBits == 4) {
+            // the row's 32 code bytes are two 16-byte halves, swapped in rows
+            // where the 32-byte swizzle flips bit 4 of the address; half h
+            // holds words 4h .. 4h+3 = columns 32h .. 32h+31
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
+              raw[g][4 * h + 0] = w.x;
+              raw[g][4 * h + 1] = w.y;
+              raw[g][4 * h + 2] = w.z;
+              raw[g][4 * h + 3] = w.w;
+            }
+          } else if constexpr (kBits == 3) {
+            // the row's 24 code bytes: low-bit words j = 0..3 (columns 16j .. 16j+15), then the high-bit
+            // words of blocks 0, 1 and 2, 3 (block 2i+1 in the upper byte of each half)
+            const uint2* rp = reinterpret_cast<const uint2*>(q_tile + row * 24);
+            const uint2 l01 = rp[0], l23 = rp[1], hh = rp[2];
+            raw[g][0] = l01.x;
+            raw[g][1] = l01.y;
+            raw[g][2] = l23.x;
+            raw[g][3] = l23.y;
+            raw[g][4] = hh.x;
+            raw[g][5] = hh.y;
+          } else {
+            // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
+            const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
+            raw[g][0] = w.x;
+            raw[g][1] = w.y;
+            raw[g][2] = w.z;
+            raw[g][3] = w.w;
+          }
+        }
 #pragma unroll
         for (int g = 0; g < C::kG; ++g) {
           const uint32_t tg = taddr + 32 * g;
@@ -474,49 +518,33 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
             tmem_st16(tg + 16, z);
             continue;
           }
-          // the warp's 32 rows of its matrix, all 64 columns of group g: the
-          // row's 32 code bytes are two 16-byte halves, swapped in rows where
-          // the 32-byte swizzle flips bit 4 of the address; half h holds words
-          // 4h .. 4h+3 = columns 32h .. 32h+31
-          const uint8_t* q_tile = st + C::kBBytes + mat * C::kQBytes + g * C::kQBytesG;
-          const uint32_t sbv = *reinterpret_cast<const uint32_t*>(st + C::kBBytes + C::kMats * C::kQBytes +
-                                                                  mat * C::kSBBytes + g * C::kSBBytesG + row * 4);
-          const float sf = __uint_as_float(sbv << 16);  // bf16 -> fp32 is exact
-          const float bf = __uint_as_float(sbv & 0xFFFF0000u);
+          const float sf = __uint_as_float(sbv[g] << 16);  // bf16 -> fp32 is exact
+          const float bf = __uint_as_float(sbv[g] & 0xFFFF0000u);
           const uint32_t s2 = f32x2_to_f16x2(sf, sf);
           const uint32_t b2 = f32x2_to_f16x2(bf, bf);
+          uint32_t v[16];
           if constexpr (kBits == 4) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 32 + ((h ^ swz) << 4));
-              uint32_t v[16];
-              dequant_word(w.x, s2, b2, v + 0);
-              dequant_word(w.y, s2, b2, v + 4);
-              dequant_word(w.z, s2, b2, v + 8);
-              dequant_word(w.w, s2, b2, v + 12);
+              dequant_word(raw[g][4 * h + 0], s2, b2, v + 0);
+              dequant_word(raw[g][4 * h + 1], s2, b2, v + 4);
+              dequant_word(raw[g][4 * h + 2], s2, b2, v + 8);
+              dequant_word(raw[g][4 * h + 3], s2, b2, v + 12);
               tmem_st16(tg + h * 16, v);
             }
           } else if constexpr (kBits == 3) {
-            // the row's 24 code bytes: low-bit words j = 0..3 (columns 16j .. 16j+15), then the high-bit
-            // words of blocks 0, 1 and 2, 3 (block 2i+1 in the upper byte of each half)
-            const uint2* rp = reinterpret_cast<const uint2*>(q_tile + row * 24);
-            const uint2 l01 = rp[0], l23 = rp[1], hh = rp[2];
-            uint32_t v[16];
-            dequant_word3(l01.x, hh.x, s2, b2, v + 0);
-            dequant_word3(l01.y, hh.x >> 8, s2, b2, v + 8);
+            dequant_word3(raw[g][0], raw[g][4], s2, b2, v + 0);
+            dequant_word3(raw[g][1], raw[g][4] >> 8, s2, b2, v + 8);
             tmem_st16(tg, v);
-            dequant_word3(l23.x, hh.y, s2, b2, v + 0);
-            dequant_word3(l23.y, hh.y >> 8, s2, b2, v + 8);
+            dequant_word3(raw[g][2], raw[g][5], s2, b2, v + 0);
+            dequant_word3(raw[g][3], raw[g][5] >> 8, s2, b2, v + 8);
             tmem_st16(tg + 16, v);
           } else {
-            // the row's 16 code bytes: words j = 0..3 hold columns 16j .. 16j+15
-            const uint4 w = *reinterpret_cast<const uint4*>(q_tile + row * 16);
-            uint32_t v[16];
-            dequant_word2(w.x, s2, b2, v + 0);
-            dequant_word2(w.y, s2, b2, v + 8);
+            dequant_word2(raw[g][0], s2, b2, v + 0);
+            dequant_word2(raw[g][1], s2, b2, v + 8);
             tmem_st16(tg, v);
-            dequant_word2(w.z, s2, b2, v + 0);
-            dequant_word2(w.w, s2, b2, v + 8);
+            dequant_word2(raw[g][2], s2, b2, v + 0);
+            dequant_word2(raw[g][3], s2, b2, v + 8);
             tmem_st16(tg + 16, v);
           }
         }
@@ -583,8 +611,16 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               if (c0 + c < c_valid) {
-                const float gv = __uint_as_float(g[c]);
-                const float h = __fdividef(gv * __uint_as_float(u[c]), 1.0f + __expf(-gv));
+                // SiLU(g) u = (g/2) u (1 + tanh(g/2)), the logistic function
+                // written through tanh: one special-function instruction
+                // instead of an exponential and a reciprocal.  tanh.approx's
+                // absolute error (about 2^-11) puts at most about |g u| 2^-12 on
+                // h, the order of h's own rounding to fp16.
+                const float t = 0.5f * __uint_as_float(g[c]);
+                const float pv = t * __uint_as_float(u[c]);
+                float th;
+                asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(t));
+                const float h = fmaf(pv, th, pv);
                 range_ok &= fabsf(h) <= 65504.0f;
                 H[static_cast<size_t>(c0 + c) * Icur] = __half_as_ushort(__float2half_rn(h));
               }
