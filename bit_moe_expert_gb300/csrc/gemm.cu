@@ -697,7 +697,11 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int d8 = d / 8;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (kGatherThreads / 32);
-  bool range_ok = true, idx_ok = true;
+  // |x| <= 65504 (the fp16 range) for a bf16 x is (bits & 0x7FFF) <= 0x477F,
+  // 0x477F being the largest finite bf16 below 65504 (NaN and infinity lie
+  // above it): a running maximum of both halves of every word, checked once
+  uint32_t amax = 0;
+  bool idx_ok = true;
   for (int r = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); r < rows; r += nwarps) {
     const int t = r < A ? __ldg(perm + r) / k : r - A;
     if (t < 0 || t >= T) {
@@ -718,16 +722,14 @@ __global__ void __launch_bounds__(kGatherThreads)
         uint32_t out[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(in[j] << 16);
-          const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
-          range_ok &= fabsf(lo) <= 65504.0f && fabsf(hi) <= 65504.0f;
-          out[j] = f32x2_to_f16x2(lo, hi);
+          amax = __vmaxu2(amax, in[j] & 0x7FFF7FFFu);
+          out[j] = f32x2_to_f16x2(__uint_as_float(in[j] << 16), __uint_as_float(in[j] & 0xFFFF0000u));
         }
         dst[c0 + 32 * u] = make_uint4(out[0], out[1], out[2], out[3]);
       }
     }
   }
-  if (!range_ok) record_status(status, MOE_ERR_UNSUPPORTED);
+  if ((amax & 0xFFFFu) > 0x477Fu || (amax >> 16) > 0x477Fu) record_status(status, MOE_ERR_UNSUPPORTED);
   if (!idx_ok) record_status(status, MOE_ERR_INVALID_ARG);
 }
 

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   __shared__ int32_t s_ids[kRouteTokensPerCta * kMaxK];
   __shared__ int32_t s_rank[kRouteTokensPerCta * kMaxK];
   __shared__ int32_t s_cnt[kMaxE];
+  __shared__ uint32_t s_mask[kMaxE];  // tokens of the chunk (bit = token within the chunk) that chose expert e
   __shared__ int32_t s_off[kMaxE + 1];
   __shared__ int32_t s_boff[kMaxE + 1];
   __shared__ int32_t s_part[2][kRouteThreads];
@@ -88,14 +89,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
     return;
   }
 
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) s_mask[e] = 0u;
+  __syncthreads();
 
   // ---- top-k, one warp per token
+  static_assert(kRouteTokensPerCta <= 32, "a chunk's tokens are the bits of one word");
   auto publish = [&](int tl, int sel_i, bool finite) {
     if (!finite && lane == 0) record_status(status, MOE_ERR_NONFINITE);
     if (lane < k) {
       out.ids[static_cast<size_t>(t0 + tl) * k + lane] = sel_i;
       s_ids[tl * k + lane] = sel_i;
+      atomicOr(&s_mask[sel_i], 1u << tl);
     }
   };
   if constexpr (kPL == 8) {
@@ -129,26 +133,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   }
   __syncthreads();
 
-  // ---- stable per-chunk ranks: one warp walks the chunk's assignments in order
+  // ---- stable per-chunk ranks: a token picks an expert at most once, so the
+  // rank of assignment (token tl, slot j) among the chunk's assignments to
+  // expert e, in assignment order, is the number of earlier tokens of the
+  // chunk that chose e
   const int na = ntok * k;
-  if (warp == 0) {
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < na; base += 32) {
-      const int a = base + lane;
-      const bool valid = a < na;
-      const int e = valid ? s_ids[a] : -1 - lane;  // distinct dummy keys for idle lanes
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int before = __popc(peers & lt_mask);
-      int cnt_before = 0;
-      if (valid) cnt_before = s_cnt[e];
-      __syncwarp();
-      if (valid) {
-        s_rank[a] = cnt_before + before;
-        if (before == 0) s_cnt[e] = cnt_before + __popc(peers);  // group leader publishes
-      }
-      __syncwarp();
-    }
+  for (int a = threadIdx.x; a < na; a += kRouteThreads) {
+    const int tl = a / k;
+    s_rank[a] = __popc(s_mask[s_ids[a]] & ((1u << tl) - 1u));
   }
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = __popc(s_mask[e]);
   __syncthreads();
 
   if (nchunks > 1 && gridsync) {

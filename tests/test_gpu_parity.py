@@ -227,6 +227,38 @@ def test_forward_gemm_rejects_routing_over_128_rows():
     assert bm.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
 
 
+@pytest.mark.parametrize("bits,expect", [(0x477F, 0), (0xC77F, 0), (0x4780, 2), (0xFF80, 2), (0x7FC0, 2)],
+                         ids=["65280", "-65280", "65536", "-inf", "nan"])
+def test_forward_gemm_x_range_check(bits, expect):
+    """The tensor-core path converts X to fp16: a value outside the fp16 range
+    (|x| > 65504; for bf16 input, anything above 65280 = 0x477F, and
+    infinities and NaN) is recorded as MOE_ERR_UNSUPPORTED (2); the largest
+    bf16 inside the range passes.  The planted value sits in a column whose
+    quantisation group has zero scale and bias in every gate and up row, so
+    the layer's other outputs stay finite and still match the oracle."""
+    cfg = synth.small_config(T=64, d=256, E=8, k=2, I=128, I_shared=128)
+    layer = synth.draw_layer(cfg)
+    X = layer.X.copy()
+    X[17, 101] = bits  # group 1 of the d = 256 input columns
+    for ex in (layer.routed, layer.shared):
+        for mat in ("gate", "up"):
+            q, sc, bi = ex[mat]
+            sc[..., 1] = 0
+            bi[..., 1] = 0
+    dl = G.DeviceLayer(X, layer.logits, layer.routed, layer.shared, bm.prepare_experts(layer.routed),
+                       bm.prepare_experts(layer.shared))
+    r, _ = G.route_gpu(layer.logits, cfg.k, 32)
+    ws = bm.workspace(bm.moe_forward_workspace_bytes(cfg.T, cfg.d, cfg.I, cfg.E, cfg.k, cfg.I_shared))
+    Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
+    bm.moe_forward(dl.X, dl.routed, dl.shared, r, Y, ws)
+    torch.cuda.synchronize()
+    assert bm.STATUS_NAMES[bm.moe_check_status(ws)] == bm.STATUS_NAMES[expect]
+    if expect == 0:
+        rh = G.routing_to_host(r)
+        Y64, _ = oracle.forward(X, layer.routed, layer.shared, rh["ids"], rh["w"])
+        G.assert_y_close(Y.cpu().numpy().view(np.uint16), Y64, f"x = bf16 {bits:#06x}")
+
+
 @pytest.mark.parametrize("path,T", [("gemv", 1), ("gemv", 4), ("gemm", 64)])
 def test_forward_deterministic(path, T):
     cfg = synth.small_config(T=T, d=256, E=8, k=2, I=128, I_shared=128)
