@@ -605,12 +605,13 @@ def run_workload(wl, args, dist, peaks, clocks):
 # reports null.
 _CSRC = os.path.join(ROOT, "bit_moe_expert_gb300", "csrc")
 PROFILED_TRAFFIC = {
-    # profiles/prefill4096_chunk_kernels.md: 87.344384 MB read + 2.607872 MB written
-    "prefill4096/gemm_gateup": (89_952_256, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "0ff914f5b9c1ae3a"),
-    # profiles/decode_kernel_decode.md: median of five launches, 16,030,720 B read, 0 written
-    "decode/decode": (16_030_720, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "701771da065854f2"),
-    # profiles/decode_kernel_decode.md (3-bit codes): median of five launches, 12,494,080 B read, 0 written
-    "decode3b/decode": (12_494_080, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "701771da065854f2"),
+    # ncu --set full of one gate/up launch of the long-prefill chunk: 83.803136 MB read + 2.589696 MB written
+    # (a cold-cache capture: the gathered X, 37.7 MB, comes back from DRAM there; in the timed step it is in L2)
+    "prefill4096/gemm_gateup": (86_392_832, ("gemm.cu", "ptx.cuh", "kernels.h", "status.h"), "3526a30c312c4af1"),
+    # ncu dram__bytes of five decode launches inside the 40-layer step: median 16,032,256 B read, 0 written
+    "decode/decode": (16_032_256, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "d439f7e021d4f873"),
+    # the same with 3-bit codes: median 12,495,360 B read, 0 written
+    "decode3b/decode": (12_495_360, ("decode.cu", "topk.cuh", "ptx.cuh", "kernels.h", "status.h"), "d439f7e021d4f873"),
 }
 
 
