@@ -4,11 +4,16 @@
 // flight": the grouped GEMM dequantises one small tile at a time on chip,
 // accumulates in FP32, writes bf16 and never materialises the expanded
 // weights; the expert input projections are fused with the gate activation and
-// the output projection with the routing scores and the shared expert).
+// the output projection with the routing scores and the shared expert).  Here
+// SwiGLU is fused into the gate/up epilogue; the routing scores and the shared
+// expert are applied by a separate combine kernel after the down GEMM (a
+// combine fused into the down epilogue serialised on the shared expert's
+// items, which every token waits for, and ran 2.3x slower).
 //
 // Operands are fp16 (the pages' Metal kernels use bf16): fp16 holds the
 // dequantised weights of this format exactly and rounds h and X 8x more finely,
-// at the same tensor-core rate; X is converted once per call.
+// at the same tensor-core rate; X is converted as it is gathered into the
+// routing's row order.
 //
 // sm_103a design ("swap AB"): the weights are the M = 128 operand and an
 // expert's tokens the N operand (16..128, a multiple of 16), so an expert with
@@ -16,16 +21,18 @@
 // weight tile never touches shared memory: dequantisation warps turn the TMA-
 // loaded codes into fp16 and store them with tcgen05.st straight into tensor
 // memory, where tcgen05.mma reads them as its A operand; shared memory carries
-// only the packed codes, the group parameters and the token tile (TMA gather4
-// of the expert's token rows).  Accumulators live in tensor memory.
+// only the packed codes, the group parameters and the token tile (TMA boxes of
+// the gathered fp16 X, or of h).  Accumulators live in tensor memory.  A
+// pipeline stage covers two quantisation groups (K = 128).
 //
 // Roles (one persistent CTA per SM):
-//   warp 0       TMA producer (codes, group parameters, token rows)
-//   warps 1-2    MMA issuers (gate and up matrices; in the down GEMM, the
-//                k-blocks of one parity each), one elected lane each
-//   warps 3-10   epilogue: TMEM -> registers -> SwiGLU (gate/up) or the
-//                expert-output rows (down)
-//   warps 11-    dequantise codes -> fp16 A tiles in TMEM: four warps per
+//   warp 0       TMA producer (token tile, codes, group parameters)
+//   warps 1-2    MMA issuers (gate and up matrices; the down GEMM uses one),
+//                one elected lane each
+//   warps 3-     epilogue (gate/up: 12 warps, down: 8): TMEM -> registers ->
+//                SwiGLU and fp16 h (gate/up) or the fp32 expert-output rows,
+//                staged in shared memory and stored by TMA (down)
+//   then         dequantise codes -> fp16 A tiles in TMEM: four warps per
 //                matrix (gate/up: 8, down: 4), one per quarter of the rows
 // Synchronisation is by mbarriers; every wait is bounded (2 s) and records
 // MOE_ERR_TIMEOUT instead of hanging.
@@ -43,17 +50,21 @@ namespace {
 // Warp roles.
 constexpr int kProducerWarp = 0;   // TMA of codes and group parameters; cp.async gather of the token tile
 constexpr int kMmaWarp0 = 1;       // two MMA issuers (warps 1 and 2)
-constexpr int kEpiWarp0 = 3;       // eight epilogue warps (3..10)
-constexpr int kEpiWarps = 8;
-constexpr int kDqWarp0 = 11;       // dequantisation warps from 11: four per matrix, one per TMEM lane quarter
+constexpr int kEpiWarp0 = 3;       // epilogue warps from 3 (Cfg::kEpiWarps of them), then the dequantisation warps
 constexpr uint32_t kBarEpilogue = 1;  // named barrier of the epilogue warps (0 is __syncthreads)
 constexpr uint32_t kTmemCols = 512;
-static_assert(kGemmBN % 32 == 0, "each epilogue warp drains kGemmBN / 2 columns, 16 at a time");
+static_assert(kGemmBN % 16 == 0, "epilogue warps drain columns 16 at a time");
 
 template <bool kGateUp, int kBits>
 struct Cfg {
   static constexpr int kMats = kGateUp ? 2 : 1;
   static constexpr int kG = kGateUp ? kGemmGroupsGU : kGemmGroupsDown;  // quantisation groups (K = 64) per stage
+  // epilogue warps: two or three per TMEM lane quarter, each draining kEpiCols columns of the tile.  The
+  // gate/up GEMM's single accumulator holds the next item's products back during its epilogue, so it takes
+  // three (49.9 against 51.7 us for the long-prefill chunk); the down GEMM's epilogue overlaps them.
+  static constexpr int kEpiWarps = kGateUp ? 12 : 8;
+  static constexpr int kEpiCols = 16 * ((kGemmBN / 16 + kEpiWarps / 4 - 1) / (kEpiWarps / 4));
+  static constexpr int kDqWarp0 = kEpiWarp0 + kEpiWarps;  // four dequantisation warps per matrix, one per lane quarter
   static constexpr int kDqWarps = 4 * kMats;
   static constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
   static constexpr int kStages = 4;
@@ -237,7 +248,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], C::kMmaIssuers);  // one commit per MMA issuer
-      mbar_init(&acc_empty[i], kEpiWarps);
+      mbar_init(&acc_empty[i], C::kEpiWarps);
     }
     mbar_init(&done[0], 1);
     mbar_init(&done[1], 1);
@@ -436,11 +447,11 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
       if (!mbar_wait(&done[who], 0, nullptr)) record_status(a.status, MOE_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp >= kDqWarp0) {
+  } else if (warp >= C::kDqWarp0) {
     // ------------------------------------------------------------ dequantisation
     const int lanegrp = warp & 3;
     const int row = lanegrp * 32 + lane;  // weight row inside the tile = TMEM lane
-    const int mat = (warp - kDqWarp0) >> 2;
+    const int mat = (warp - C::kDqWarp0) >> 2;
     const int swz = (row >> 2) & 1;
     int stage = 0, astage = 0;
     uint32_t phase = 0, aphase = 0;
@@ -569,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ep = warp - kEpiWarp0;
     const int lanegrp = warp & 3;
-    const int colhalf = ep >> 2;  // this warp handles columns [colhalf * kGemmBN / 2, (colhalf + 1) * kGemmBN / 2)
+    const int colpart = ep >> 2;  // this warp handles columns [colpart * kEpiCols, (colpart + 1) * kEpiCols)
     const int row = lanegrp * 32 + lane;
     int accb = 0;
     uint32_t accphase = 0;
@@ -581,14 +592,14 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         continue;
       }
       const int bn = tile_n(m.rows);
-      const int c_begin = colhalf * (kGemmBN / 2);
-      const int c_end = min(bn, c_begin + kGemmBN / 2);
+      const int c_begin = colpart * C::kEpiCols;
+      const int c_end = min(bn, c_begin + C::kEpiCols);
       bool bad = false;
       if (ep == 0) {
         bad = !mbar_wait(&acc_full[accb], accphase, abort_flag);
         if (bad && lane == 0) fail();
       }
-      if (bar_sync_or(kBarEpilogue, kEpiWarps * 32, bad)) break;
+      if (bar_sync_or(kBarEpilogue, C::kEpiWarps * 32, bad)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(lanegrp * 32) << 16) + accb * C::kAccBufCols;
       const int n = m.mt * kGemmBM + row;
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(Cfg<kGateUp, kBits>::kThreads, 1)
         const int c_valid = min(c_end, m.rows);
         bool range_ok = true;
         // 16 columns of gate and up per TMEM round trip (the column ranges
-        // are multiples of 16: kGemmBN / 2 and the tile width both are)
+        // are multiples of 16: kEpiCols and the tile width both are)
         for (int c0 = c_begin; c0 < c_end; c0 += 16) {
           uint32_t g[16], u[16];
           tmem_ld16(tbase + c0, g);
