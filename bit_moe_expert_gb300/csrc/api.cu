@@ -221,8 +221,58 @@ bool experts_ok(const moe_experts* ex) {
 
 int code_bits(const moe_experts* ex) { return ex->bits == 0 ? 4 : ex->bits; }
 
+// One-time launch set-up shared by the launchers: the dynamic shared-memory
+// limit of a kernel and its resident CTAs per SM, per device (both depend on
+// the device's context), under one lock, since host threads may make their
+// first calls on different devices at the same time.
+struct FuncEntry {
+  int dev;
+  const void* func;
+  int threads;
+  size_t smem;
+  int value;  // the limit set (attribute entries, threads = -1), or CTAs per SM
+};
+constexpr int kFuncEntries = 128;
+FuncEntry g_func[kFuncEntries];
+int g_func_n = 0;
+std::mutex g_func_mu;
+
 }  // namespace
 
+cudaError_t set_max_dynamic_smem(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_func_mu);
+  for (int i = 0; i < g_func_n; ++i)
+    if (g_func[i].dev == dev && g_func[i].func == func && g_func[i].threads == -1) {
+      if (g_func[i].value >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) g_func[i].value = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && g_func_n < kFuncEntries) g_func[g_func_n++] = FuncEntry{dev, func, -1, 0, bytes};
+  return e;
+}
+
+cudaError_t occupancy_per_sm(const void* func, int threads, size_t smem, int* per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_func_mu);
+  for (int i = 0; i < g_func_n; ++i)
+    if (g_func[i].dev == dev && g_func[i].func == func && g_func[i].threads == threads && g_func[i].smem == smem) {
+      *per_sm = g_func[i].value;
+      return cudaSuccess;
+    }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (g_func_n < kFuncEntries) g_func[g_func_n++] = FuncEntry{dev, func, threads, smem, n};
+  *per_sm = n;
+  return cudaSuccess;
+}
 
 }  // namespace bm
 

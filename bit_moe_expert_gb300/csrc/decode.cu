@@ -946,21 +946,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // on error).  The barrier over the grid needs every CTA resident together.
 template <int kT, int kBits>
 int max_ctas(size_t smem, int num_sms) {
-  static int cached_dev = -1, cached = 0;
-  static size_t cached_smem = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev == cached_dev && smem == cached_smem) return cached;
-  if (cudaFuncSetAttribute(decode_kernel<kT, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemMax)) != cudaSuccess)
-    return 0;
+  const void* f = reinterpret_cast<const void*>(decode_kernel<kT, kBits>);
+  if (set_max_dynamic_smem(f, static_cast<int>(kSmemMax)) != cudaSuccess) return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kT, kBits>, kThreads, smem) != cudaSuccess)
-    return 0;
-  cached_dev = dev;
-  cached_smem = smem;
-  cached = per_sm * num_sms;
-  return cached;
+  if (occupancy_per_sm(f, kThreads, smem, &per_sm) != cudaSuccess) return 0;
+  return per_sm * num_sms;
 }
 
 template <int kT, int kBits>

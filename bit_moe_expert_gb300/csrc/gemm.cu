@@ -812,15 +812,11 @@ cudaError_t launch_gemm_t(const GemmArgs& a, const GemmMaps* routed, const GemmM
                           const GemmActMaps* act, cudaStream_t stream, bool pdl) {
   using CG = Cfg<true, kBits>;
   using CD = Cfg<false, kBits>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<true, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CG::kSmemBytes);
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(moe_gemm_kernel<true, kBits>), CG::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(moe_gemm_kernel<false, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CD::kSmemBytes);
+    e = set_max_dynamic_smem(reinterpret_cast<const void*>(moe_gemm_kernel<false, kBits>), CD::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const GemmMaps* sh = shared ? shared : routed;
   cudaLaunchAttribute attr[1];

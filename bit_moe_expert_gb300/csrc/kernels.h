@@ -38,6 +38,12 @@ struct RouteOut {
   int32_t* num_blocks;
 };
 
+// One-time launch set-up, per device and kernel, thread-safe: raise the
+// kernel's dynamic shared-memory limit to at least `bytes`; the kernel's
+// resident CTAs per SM at (threads, smem).
+cudaError_t set_max_dynamic_smem(const void* func, int bytes);
+cudaError_t occupancy_per_sm(const void* func, int threads, size_t smem, int* per_sm);
+
 size_t route_hist_elems(int T, int E);
 // status: where device-side errors go (null: the workspace header's status word)
 cudaError_t launch_route(const float* logits, int T, int E, int k, int block_rows, const RouteOut& out, void* ws,

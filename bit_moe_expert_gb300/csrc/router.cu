@@ -187,12 +187,9 @@ __global__ void __launch_bounds__(kRouterThreads)
 cudaError_t launch_router(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, float* logits,
                           cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(router_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSSmemBytes);
+  {
+    const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(router_smem_kernel), kSSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -351,25 +351,20 @@ cudaError_t launch_topk_wide(const float* logits, int T, int V, int K, float* va
                              int num_sms, cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
   const size_t smem = topk_wide_smem_bytes(V, K);
-  static size_t attr_bytes = 0;
-  if (smem > attr_bytes) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(topk_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  {
+    const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_wide_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_bytes = smem;
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  static int per_sm = 0;
-  static size_t per_sm_smem = 0;
-  if (per_sm == 0 || per_sm_smem != smem) {
-    int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_wide_kernel, kWideThreads, smem);
+  int per_sm = 0;
+  {
+    const cudaError_t e =
+        occupancy_per_sm(reinterpret_cast<const void*>(topk_wide_kernel), kWideThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-    per_sm_smem = smem;
+    if (per_sm < 1) per_sm = 1;
   }
   const int ctas = per_sm * num_sms;
   cfg.gridDim = dim3(static_cast<unsigned>(T < ctas ? T : ctas));
