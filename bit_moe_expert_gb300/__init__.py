@@ -132,9 +132,13 @@ def _check(fn: str, status: int):
 
 
 def _stream(stream) -> int:
+    if stream is not None:
+        return stream.cuda_stream
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:  # the current stream's handle without building a Stream object (~0.2 against ~3 us)
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _ptr(t) -> int:

@@ -156,6 +156,7 @@ SMALL = [
     ("k1_E1", dict(T=7, E=1, k=1, I=128, I_shared=0)),
     ("many_tokens", dict(T=300, d=128, E=4, k=2, I=64, I_shared=64)),
     ("skewed", dict(T=130, d=256, E=6, k=1, I=256, I_shared=0)),
+    ("max_E_and_k", dict(T=40, d=128, E=1024, k=32, I=64, I_shared=64)),  # the largest E and k the library takes
 ]
 
 
