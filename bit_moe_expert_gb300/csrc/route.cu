@@ -13,7 +13,7 @@
 // every assignment, and writes the block map.
 //
 // The routing weights (a softmax in fp64, which is slow on this GPU) are not on
-// that chain: extra CTAs after the routing CTAs select the top k of 16 tokens
+// that chain: extra CTAs after the routing CTAs select the top k of 8 tokens
 // each again (the same function, so the same selection) and write only the
 // weights; they wait for nothing, so they run beside the routing CTAs.
 #include <cuda_fp16.h>
@@ -35,6 +35,13 @@ namespace {
 constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kBasesSmemLimit = 96 * 1024;  // per-chunk bases kept in shared memory up to this size
+// Tokens per weight CTA (one per warp; the CTA's other warps leave at once).
+// fp64 is slow on this GPU and shared by an SM's warps: 8 tokens per CTA
+// instead of 16 spread the weights over twice the SMs (the 1024-token chunk's
+// weight CTAs finished at 8.9 us, after the routing CTAs; the long-prefill
+// step went from 0.467 to 0.452 ms).
+constexpr int kWeightTokensPerCta = 8;
+static_assert(kWeightTokensPerCta <= kRouteWarps, "a weight CTA's tokens fit its warps");
 
 constexpr int kRouteMaxDevices = 64;
 struct RouteSetup {
@@ -77,8 +84,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   if (chunk >= nroute) {
     // ---- a weight CTA: one token per warp; the softmax over the selected
     // logits in fp64, summed in selection order, rounded once
-    const int t = (chunk - nroute) * kRouteWarps + warp;
-    if (t < T) {
+    const int t = (chunk - nroute) * kWeightTokensPerCta + warp;
+    if (warp < kWeightTokensPerCta && t < T) {
       int sel_i;
       float sel_v;
       bool finite;
@@ -392,7 +399,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int block_row
     if (!std::strcmp(m, "ticket")) gridsync = 0;
     if (!std::strcmp(m, "gridsync") && nchunks > 1 && nchunks <= (E <= 256 ? resident8 : resident32)) gridsync = 1;
   }
-  const int nweight = (T + kRouteWarps - 1) / kRouteWarps;  // weight CTAs, one token per warp
+  const int nweight = (T + kWeightTokensPerCta - 1) / kWeightTokensPerCta;  // weight CTAs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nchunks + nweight);
   cfg.blockDim = dim3(kRouteThreads);
