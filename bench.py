@@ -643,9 +643,15 @@ def router_measure(dev, peaks):
             W[i] = W[i - i % 50]
     out = {}
     s = torch.cuda.Stream(device=dev)
-    for T in (1, 1024):
+    # (tokens, key, MOE_ROUTER_TC): the default kernels, and at 1024 tokens the
+    # warp-MMA kernel the tensor-core one replaces
+    for T, key, tc in ((1, "T1", None), (1024, "T1024", None), (4096, "T4096", None),
+                       (1024, "T1024_warp_mma", "0")):
         X = torch.from_numpy(synth.draw_x(cfg, T, 0).view(np.int16)).to(dev)
         lg = torch.empty((T, cfg.E), dtype=torch.float32, device=dev)
+        old_tc = os.environ.get("MOE_ROUTER_TC")
+        if tc is not None:
+            os.environ["MOE_ROUTER_TC"] = tc
         with torch.cuda.stream(s):
             for i in range(3):
                 bm.moe_router_logits(X, W[i], lg)
@@ -661,6 +667,11 @@ def router_measure(dev, peaks):
             g.replay()
             e1.record(s)
             e1.synchronize()
+        if tc is not None:
+            if old_tc is None:
+                del os.environ["MOE_ROUTER_TC"]
+            else:
+                os.environ["MOE_ROUTER_TC"] = old_tc
         us = e0.elapsed_time(e1) / nw * 1e3
         nbytes = cfg.E * cfg.d * 2 + T * cfg.d * 2 + T * cfg.E * 4
         flops = 2 * T * cfg.E * cfg.d
@@ -670,7 +681,10 @@ def router_measure(dev, peaks):
         else:
             ent.update(bound="tensor", frac=ent["tflops"] / peaks["bf16_tflops"], peak=peaks["bf16_tflops"],
                        unit="TFLOP/s")
-        out[f"T{T}"] = ent
+        ent["kernel"] = ("router_rows_kernel (CUDA cores)" if T <= 32 else
+                         "router_smem_kernel (mma.sync)" if tc == "0" else
+                         "router_tc_kernel (tcgen05, TMA, 4-CTA cluster split-K)")
+        out[key] = ent
     out["note"] = (f"logits = X W_r^T, d={cfg.d}, E={cfg.E}, bf16 in, fp32 out; 200 calls on distinct routers "
                    "in one CUDA graph")
     del W

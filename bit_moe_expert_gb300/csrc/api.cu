@@ -149,6 +149,16 @@ bool encode_out(CUtensorMap* map, const float* p, int rows, int cols) {
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// bf16 rows [rows][cols] (the router projection's X and W_r): boxes of 64
+// columns (128 bytes) x box_rows rows, 128-byte swizzle; rows past the end
+// read as zeros
+bool encode_bf16_rows(CUtensorMap* map, const uint16_t* p, int rows, int cols, int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // group parameters sb [E][K/64][N] uint32
 bool encode_groups(CUtensorMap* map, const uint32_t* sb, int E, int N, int K, cuuint32_t box_rows,
                    cuuint32_t box_groups) {
@@ -370,7 +380,17 @@ moe_status moe_router_logits(const uint16_t* X, int T, int d, const uint16_t* W_
   if (T > 0 && ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W_r)) & 15u)) return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * E > (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;
   const bool pdl = env_flag("MOE_PDL", true);
-  if (launch_router(X, T, d, W_r, E, logits, reinterpret_cast<cudaStream_t>(stream), pdl) != cudaSuccess)
+  // the tensor-core shape wants 16-byte rows of logits for its vector stores;
+  // MOE_ROUTER_TC=0 keeps the warp-MMA shapes (for comparisons)
+  RouterMaps maps;
+  const RouterMaps* mp = nullptr;
+  if (router_tc_shape(T, d, E) && !(reinterpret_cast<uintptr_t>(logits) & 15u) && env_flag("MOE_ROUTER_TC", true)) {
+    if (!get_encoder() || !encode_bf16_rows(&maps.x, X, T, d, kRouterTcT) ||
+        !encode_bf16_rows(&maps.wr, W_r, E, d, kRouterTcE))
+      return MOE_ERR_CUDA;
+    mp = &maps;
+  }
+  if (launch_router(X, T, d, W_r, E, logits, mp, reinterpret_cast<cudaStream_t>(stream), pdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

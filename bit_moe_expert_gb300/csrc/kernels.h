@@ -57,9 +57,18 @@ cudaError_t launch_dequant(const uint32_t* qp, const uint32_t* sb, int E, int N,
                            cudaStream_t stream);
 
 // Router projection: logits [T][E] fp32 = X [T][d] bf16 times Wr [E][d] bf16
-// transposed (d a multiple of 32).
+// transposed (d a multiple of 32).  With `maps` (router_tc_shape true), the
+// tensor-core path: TMA tiles, tcgen05 MMAs, K split over a 4-CTA cluster.
+constexpr int kRouterTcE = 128;     // experts per CTA (the MMA's M)
+constexpr int kRouterTcT = 64;      // tokens per CTA (the MMA's N)
+constexpr int kRouterTcSplit = 4;   // CTAs of a cluster, each a quarter of K
+struct RouterMaps {
+  CUtensorMap x;   // X [T][d] bf16, box (64, kRouterTcT), 128-byte swizzle
+  CUtensorMap wr;  // Wr [E][d] bf16, box (64, kRouterTcE), 128-byte swizzle
+};
+bool router_tc_shape(int T, int d, int E);
 cudaError_t launch_router(const uint16_t* X, int T, int d, const uint16_t* Wr, int E, float* logits,
-                          cudaStream_t stream, bool pdl);
+                          const RouterMaps* maps, cudaStream_t stream, bool pdl);
 
 // Exact top-K (K <= 64) of each row of logits [T][V] (V <= 2^20): values and
 // indices [T][K], descending, a lower index first among equal values.

@@ -1,6 +1,7 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA (cp.async.bulk.tensor),
-// tcgen05 (TMEM allocation, MMA with the A operand in TMEM, loads/stores),
-// programmatic dependent launch, and waits bounded in time.
+// tcgen05 (TMEM allocation, MMA with the A operand in TMEM or in shared
+// memory, loads/stores), thread-block clusters (barrier, distributed shared
+// memory), programmatic dependent launch, and waits bounded in time.
 #pragma once
 
 #include <cuda.h>
@@ -237,6 +238,17 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, both operands by descriptor.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives on the mbarrier once every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -292,6 +304,45 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// The same with bf16 A and B (format code 1).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return idesc_f16_f32(M, N) | (1u << 7) | (1u << 10);
+}
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The cluster barrier in two halves, every thread of every CTA of the
+// cluster taking part: arrive (relaxed: it orders nothing by itself; an
+// mbarrier initialisation is published to the cluster by fence_mbar_init
+// before it), then wait until every thread has arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// arrive with release semantics: this thread's earlier shared-memory writes
+// are visible to every thread of the cluster that has passed the next wait
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// The shared::cluster address of this CTA's shared-memory location p in the
+// CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
   // (a & mask) | orv

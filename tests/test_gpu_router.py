@@ -59,8 +59,9 @@ def _assert_logits_close(got, X, Wr):
 
 
 # (T, d, E): the decode token, the tiny layer, ragged experts and tokens on
-# both kernel shapes (T <= 8 splits K over warps; larger T tiles 64 x 64), the
-# widest router and a full 1024-token prefill chunk
+# the three kernel shapes (up to 32 tokens a warp per router row; more tokens
+# the tensor-core kernel when E is a multiple of 128 and d of 256, else the
+# warp-MMA tiles of 32 x 64), the widest router and a full 1024-token chunk
 CASES = [
     ("decode", 1, 2048, 256),
     ("decode4", 4, 2048, 256),
@@ -73,6 +74,13 @@ CASES = [
     ("wide", 33, 256, 1024),
     ("chunk", 1024, 2048, 256),
     ("canvas", 256, 2816, 128),
+    # the tensor-core shape (more than 32 tokens, E a multiple of 128, d of
+    # 256): a ragged last token tile over three router-row tiles, a K quarter
+    # of one stage, two passes over the stage ring, and a long prompt
+    ("tc_ragged", 65, 512, 384),
+    ("tc_one_stage", 200, 256, 128),
+    ("tc_two_rings", 300, 4096, 128),
+    ("tc_long", 4096, 2048, 256),
 ]
 
 
@@ -81,6 +89,34 @@ def test_router_logits_parity(name, T, d, E):
     X, Wr = _draw(T, d, E, seed=zlib.crc32(name.encode()))
     got, _ = _gpu_logits(X, Wr)
     _assert_logits_close(got, X, Wr)
+
+
+@pytest.mark.parametrize("T,d,E,tc", [
+    (1024, 2048, 256, True), (33, 256, 1024, True), (300, 4096, 128, True), (32, 2048, 256, False),
+    (100, 192, 48, False), (64, 2048, 200, False),
+])
+def test_router_shape_choice(T, d, E, tc, monkeypatch):
+    # MOE_ROUTER_TC=0 keeps the warp-MMA kernels.  On a shape the tensor-core
+    # kernel takes, the two sum in different orders, so some of the fp32
+    # logits differ in their last bits (identical logits would mean the
+    # tensor-core kernel did not run); both agree with the oracle within the
+    # accumulation bound.  On any other shape the switch changes nothing.
+    X, Wr = _draw(T, d, E, seed=T + d + E)
+    default, _ = _gpu_logits(X, Wr)
+    monkeypatch.setenv("MOE_ROUTER_TC", "0")
+    warp_mma, _ = _gpu_logits(X, Wr)
+    _assert_logits_close(default, X, Wr)
+    _assert_logits_close(warp_mma, X, Wr)
+    assert (not np.array_equal(default.view(np.uint32), warp_mma.view(np.uint32))) == tc
+
+
+def test_router_tc_tile_independence():
+    # a token's logits do not depend on the other tokens of its tile or on the
+    # tile it falls in (zero-filled rows past T multiply into nothing)
+    X, Wr = _draw(200, 512, 256, seed=77)
+    whole, _ = _gpu_logits(X, Wr)
+    shifted, _ = _gpu_logits(np.ascontiguousarray(X[37:]), Wr)
+    assert np.array_equal(whole[37:].view(np.uint32), shifted.view(np.uint32))
 
 
 def test_router_logits_one_hot_tokens_are_exact():
@@ -96,7 +132,24 @@ def test_router_logits_one_hot_tokens_are_exact():
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("T", [1, 300])
+def test_router_tc_one_hot_tokens_are_exact():
+    # the same on the tensor-core shape: unit tokens in every K quarter, every
+    # 16-wide K slice of a stage and both halves of a 128-byte swizzled row
+    # pick out single router columns, so a misplaced quarter, stage or slice
+    # shows as a wrong column
+    d, E = 1024, 256
+    _, Wr = _draw(1, d, E, seed=6)
+    cols = [0, 15, 16, 31, 32, 47, 48, 63, 64, 100, 255, 256, 300, 511, 512, 700, 767, 768, 1000, 1023]
+    cols = cols + [(37 * j) % d for j in range(70 - len(cols))]
+    X = np.zeros((len(cols), d), np.uint16)
+    for t, i in enumerate(cols):
+        X[t, i] = 0x3F80
+    got, _ = _gpu_logits(X, Wr)
+    want = synth.bf16_bits_to_f32(Wr)[:, cols].T
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("T", [1, 300, 1024])
 def test_router_logits_deterministic(T):
     X, Wr = _draw(T, 1024, 256, seed=9)
     a, _ = _gpu_logits(X, Wr)
