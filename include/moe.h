@@ -281,9 +281,16 @@ moe_status moe_forward(const uint16_t* X, int T, int d, int I, int k, const moe_
  *   logits  fp32 [T][E] row-major (device, caller-owned), written
  * Preconditions: T >= 0 (T = 0 does nothing), d a multiple of 64,
  * 1 <= E <= 1024, X and W_r 16-byte aligned.  Arithmetic: bf16 products
- * accumulated in fp32 on the tensor cores; the additions are not in index
- * order, so the logits agree with an exact sum to within fp32 accumulation
- * error, not bit for bit.  Asynchronous on `stream`; allocates nothing. */
+ * accumulated in fp32 (on the CUDA cores up to 32 tokens, else on the tensor
+ * cores); the additions are not in index order, so the logits agree with an
+ * exact sum to within fp32 accumulation error, not bit for bit.  The result
+ * does not depend on timing: the same call gives the same bits.  More than
+ * 32 tokens with E a multiple of 128, d of 256 and logits 16-byte aligned take
+ * the fifth-generation tensor cores (environment variable MOE_ROUTER_TC=0
+ * keeps the warp-level MMA kernel, for comparisons); a device-side wait there
+ * that gives up leaves NaN in the affected logits, which moe_route then
+ * reports as MOE_ERR_NONFINITE.  Asynchronous on `stream`; allocates
+ * nothing. */
 moe_status moe_router_logits(const uint16_t* X, int T, int d, const uint16_t* W_r, int E, float* logits,
                              moe_stream stream);
 
