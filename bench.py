@@ -365,7 +365,8 @@ class PrefillWorkload(Workload):
         # while earlier chunks compute, and its Y leaves while later chunks compute
         self.copy_stream = torch.cuda.Stream(device=dev)
         self.ev_step = torch.cuda.Event()
-        self.ev_in = [torch.cuda.Event() for _ in range(self.nchunks)]
+        self.ev_lg = [torch.cuda.Event() for _ in range(self.nchunks)]  # chunk c's logits landed (routing may start)
+        self.ev_in = [torch.cuda.Event() for _ in range(self.nchunks)]  # and its X
         self.ev_out = [torch.cuda.Event() for _ in range(self.nchunks)]
         self.ev_done = torch.cuda.Event()
         self.h2d_bytes = self.X_host.nbytes + self.nchunks * C * cfg.E * 4
@@ -395,13 +396,15 @@ class PrefillWorkload(Workload):
         with torch.cuda.stream(cs):
             for c in range(self.nchunks):
                 rows = slice(c * C, (c + 1) * C)
-                self.X_e2e[rows].copy_(self.X_pin[rows], non_blocking=True)
                 self.lg_e2e[rows].copy_(self.lg_pin[rows], non_blocking=True)
+                self.ev_lg[c].record(cs)
+                self.X_e2e[rows].copy_(self.X_pin[rows], non_blocking=True)
                 self.ev_in[c].record(cs)
         for c in range(self.nchunks):
             s, rows = self._set(c), slice(c * C, (c + 1) * C)
-            main.wait_event(self.ev_in[c])
+            main.wait_event(self.ev_lg[c])
             bm.moe_route(self.lg_e2e[rows], cfg.k, self.block_rows, self.r, self.ws_r)
+            main.wait_event(self.ev_in[c])
             bm.moe_forward(self.X_e2e[rows], self.routed[s], self.shared[s], self.r, self.Y[rows], self.ws_f)
             self.ev_out[c].record(main)
             cs.wait_event(self.ev_out[c])
