@@ -402,10 +402,17 @@ class PrefillWorkload(Workload):
                 self.ev_in[c].record(cs)
         for c in range(self.nchunks):
             s, rows = self._set(c), slice(c * C, (c + 1) * C)
-            main.wait_event(self.ev_lg[c])
+            # the first chunk's routing starts once its logits have landed, its expert kernels once its X
+            # has; the later chunks' inputs land while the first computes, so one wait after it covers them
+            # and leaves their kernels chained
+            if c == 0:
+                main.wait_event(self.ev_lg[0])
             bm.moe_route(self.lg_e2e[rows], cfg.k, self.block_rows, self.r, self.ws_r)
-            main.wait_event(self.ev_in[c])
+            if c == 0:
+                main.wait_event(self.ev_in[0])
             bm.moe_forward(self.X_e2e[rows], self.routed[s], self.shared[s], self.r, self.Y[rows], self.ws_f)
+            if c == 0 and self.nchunks > 1:
+                main.wait_event(self.ev_in[self.nchunks - 1])
             self.ev_out[c].record(main)
             cs.wait_event(self.ev_out[c])
             with torch.cuda.stream(cs):
