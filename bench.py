@@ -698,6 +698,52 @@ def router_measure(dev, peaks):
     out["note"] = (f"logits = X W_r^T, d={cfg.d}, E={cfg.E}, bf16 in, fp32 out; 200 calls on distinct routers "
                    "in one CUDA graph")
     del W
+    torch.cuda.empty_cache()
+    out["T1_in_decode_step"] = decode_router_measure(dev)
+    return out
+
+
+def decode_router_measure(dev, reps=20):
+    """The one-token projection inside the chained decode step: 40 distinct layers of moe_layer_x (projection,
+    then the one-launch layer) against moe_layer on precomputed logits, each step one CUDA graph."""
+    import torch
+    import bit_moe_expert_gb300 as bm
+    wl = DecodeWorkload(dev)
+    cfg = wl.cfg
+    Wr = [torch.from_numpy(synth.draw_router(cfg, l).view(np.int16)).to(dev) for l in range(wl.L)]
+    lg = [torch.empty((wl.T, cfg.E), dtype=torch.float32, device=dev) for _ in range(wl.L)]
+
+    def step_x():
+        for l in range(wl.L):
+            bm.moe_layer_x(wl.X[l], Wr[l], wl.routed[l], wl.shared[l], cfg.k, wl.block_rows, lg[l], wl.r,
+                           wl.Y_l[l], wl.ws)
+
+    s = torch.cuda.Stream(device=dev)
+    res = {}
+    for key, fn in (("moe_layer", wl.step), ("moe_layer_x", step_x)):
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fn()
+            for _ in range(3):
+                g.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+            e1.synchronize()
+        res[key] = e0.elapsed_time(e1) / reps / wl.L * 1e3
+    out = {"us_per_layer_moe_layer": res["moe_layer"], "us_per_layer_moe_layer_x": res["moe_layer_x"],
+           "router_us_per_layer": res["moe_layer_x"] - res["moe_layer"],
+           "note": "40 distinct decode layers chained in one CUDA graph (PDL); moe_layer_x adds the router "
+                   "projection (router_rows_kernel) ahead of each layer's decode kernel"}
+    del wl, Wr, lg
+    torch.cuda.empty_cache()
     return out
 
 

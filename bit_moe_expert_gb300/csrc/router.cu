@@ -52,7 +52,6 @@ constexpr int kRouterThreads = 256;
 constexpr int kRowsThreads = 128;
 constexpr int kRowsMaxT = 32;
 constexpr int kRowsU = 8;  // 16-byte pieces of the row per lane in flight (a 2048-wide row in one round)
-constexpr int kRowsG = 4;  // tokens whose loads are in flight together
 
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -64,41 +63,69 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   return acc;
 }
 
+// kG tokens have their loads in flight together: 4 in general, 1 for the
+// decode token (fewer registers, so that the CTAs fit beside a decode
+// kernel's and can start while it finishes).
+template <int kG>
 __global__ void __launch_bounds__(kRowsThreads)
     router_rows_kernel(const uint16_t* __restrict__ X, int T, int d, const uint16_t* __restrict__ Wr, int E,
                        float* __restrict__ logits) {
-  pdl_wait();  // X may come from the previous kernel on the stream
-  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * (kRowsThreads / 32) + (threadIdx.x >> 5);
-  if (e >= E) return;
+  const bool live = e < E;
   const int n16 = d / 8;  // 16-byte pieces per row
-  const uint4* w = reinterpret_cast<const uint4*>(Wr + static_cast<size_t>(e) * d);
+  const uint4* w = reinterpret_cast<const uint4*>(Wr + static_cast<size_t>(live ? e : 0) * d);
   const uint4* xr = reinterpret_cast<const uint4*>(X);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  // tokens in groups of kRowsG, every load of a group in flight together (the
-  // router row comes from HBM for the first group and from L1 after it)
-  for (int t0 = 0; t0 < T; t0 += kRowsG) {
-    float acc[kRowsG];
+  // the router row does not come from the previous kernel: when it fits one
+  // round (d <= 2048) it is loaded before waiting for that kernel and kept
+  // in registers for every token
+  const bool one_round = n16 <= 32 * kRowsU;
+  uint4 w0[kRowsU];
 #pragma unroll
-    for (int j = 0; j < kRowsG; ++j) acc[j] = 0.0f;
-    for (int i0 = lane; i0 < n16; i0 += 32 * kRowsU) {
-      uint4 wv[kRowsU], xv[kRowsG][kRowsU];
+  for (int u = 0; u < kRowsU; ++u)
+    w0[u] = (one_round && live && lane + 32 * u < n16) ? __ldg(w + lane + 32 * u) : zero;
+  pdl_wait();  // X may come from the previous kernel on the stream
+  pdl_launch_dependents();
+  if (!live) return;
+  // tokens in groups of kG, every load of a group in flight together (longer
+  // rows: the router row comes from HBM for the first group and from L1 after)
+  for (int t0 = 0; t0 < T; t0 += kG) {
+    float acc[kG];
+#pragma unroll
+    for (int j = 0; j < kG; ++j) acc[j] = 0.0f;
+    if (one_round) {
+      uint4 xv[kG][kRowsU];
 #pragma unroll
       for (int u = 0; u < kRowsU; ++u) {
-        const bool in = i0 + 32 * u < n16;
-        wv[u] = in ? __ldg(w + i0 + 32 * u) : zero;
+        const bool in = lane + 32 * u < n16;
 #pragma unroll
-        for (int j = 0; j < kRowsG; ++j)
-          xv[j][u] = (in && t0 + j < T) ? __ldg(xr + static_cast<size_t>(t0 + j) * n16 + i0 + 32 * u) : zero;
+        for (int j = 0; j < kG; ++j)
+          xv[j][u] = (in && t0 + j < T) ? __ldg(xr + static_cast<size_t>(t0 + j) * n16 + lane + 32 * u) : zero;
       }
 #pragma unroll
-      for (int j = 0; j < kRowsG; ++j)
+      for (int j = 0; j < kG; ++j)
 #pragma unroll
-        for (int u = 0; u < kRowsU; ++u) acc[j] = dot8_bf16(wv[u], xv[j][u], acc[j]);
+        for (int u = 0; u < kRowsU; ++u) acc[j] = dot8_bf16(w0[u], xv[j][u], acc[j]);
+    } else {
+      for (int i0 = lane; i0 < n16; i0 += 32 * kRowsU) {
+        uint4 wv[kRowsU], xv[kG][kRowsU];
+#pragma unroll
+        for (int u = 0; u < kRowsU; ++u) {
+          const bool in = i0 + 32 * u < n16;
+          wv[u] = in ? __ldg(w + i0 + 32 * u) : zero;
+#pragma unroll
+          for (int j = 0; j < kG; ++j)
+            xv[j][u] = (in && t0 + j < T) ? __ldg(xr + static_cast<size_t>(t0 + j) * n16 + i0 + 32 * u) : zero;
+        }
+#pragma unroll
+        for (int j = 0; j < kG; ++j)
+#pragma unroll
+          for (int u = 0; u < kRowsU; ++u) acc[j] = dot8_bf16(wv[u], xv[j][u], acc[j]);
+      }
     }
 #pragma unroll
-    for (int j = 0; j < kRowsG; ++j) {
+    for (int j = 0; j < kG; ++j) {
       float v = acc[j];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -442,7 +469,8 @@ cudaError_t launch_router(const uint16_t* X, int T, int d, const uint16_t* Wr, i
   if (T <= kRowsMaxT) {
     cfg.gridDim = dim3((E + kRowsThreads / 32 - 1) / (kRowsThreads / 32));
     cfg.blockDim = dim3(kRowsThreads);
-    e = cudaLaunchKernelEx(&cfg, router_rows_kernel, X, T, d, Wr, E, logits);
+    e = T == 1 ? cudaLaunchKernelEx(&cfg, router_rows_kernel<1>, X, T, d, Wr, E, logits)
+               : cudaLaunchKernelEx(&cfg, router_rows_kernel<4>, X, T, d, Wr, E, logits);
   } else {
     cfg.gridDim = dim3((E + kSE - 1) / kSE, (T + kST - 1) / kST);
     cfg.blockDim = dim3(kRouterThreads);

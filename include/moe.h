@@ -25,6 +25,14 @@
  *     these paths (moe_check_status is the one synchronising call).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL means the legacy
  *     default stream) and may be captured into a CUDA graph.
+ *   - Kernels are launched with programmatic dependent launch: a call's kernel
+ *     may start while the previous kernel on the stream is finishing, and
+ *     reads weights (expert codes and group parameters, router rows) before
+ *     waiting for it; activations, logits and routing are read only after.
+ *     Weights written by a kernel must therefore be separated from the call
+ *     that reads them by something other than a kernel launch (an event wait,
+ *     a copy, a memset, another stream's completion), or the environment
+ *     variable MOE_PDL=0 turns the early starts off.
  *   - Argument checks happen on the host before anything is launched; a failed
  *     check returns a status and launches nothing.  Errors that only the device
  *     can see (a non-finite logit, a bounded wait that expired) are recorded in
