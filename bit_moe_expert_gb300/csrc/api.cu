@@ -556,6 +556,10 @@ moe_status forward_impl(const uint16_t* X, int T, int d, int I, int k, const moe
     a.block_rows = r->block_rows;
     a.Y = Y;
     a.hbuf = reinterpret_cast<uint8_t*>(wsb + L.dec_h);
+    a.qg_r = routed->gate.q;
+    a.qu_r = routed->up.q;
+    a.qg_s = shared ? shared->gate.q : nullptr;
+    a.qu_s = shared ? shared->up.q : nullptr;
     a.status = status;
     a.T = T;
     a.d = d;

@@ -40,6 +40,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -70,8 +72,10 @@ constexpr size_t kSmemMax = 227 * 1024;
 
 static_assert(kWarps == 2 * kChunk, "phase 1 gives one warp to each (matrix, group) of a stage");
 static_assert(kRows1 == 32 && kRows2 == 16, "fragment layout");
-constexpr int kBars = 2 * kS1 + 3 * kS2Max + 3;  // mbarriers: full/empty per phase-1 stage, full (codes, h)/empty per
-                                                 // phase-2 stage, x, routing weights, first h records
+constexpr int kBars = 2 * kS1 + 3 * kS2Max + 4;  // mbarriers: full/empty per phase-1 stage, full (codes, h)/empty per
+                                                 // phase-2 stage, x, routing weights, first h records, phase-1
+                                                 // codes consumed (register loads)
+constexpr int kRegChunks = 4;  // phase-1 chunks held in registers (d <= 2048) when the codes are loaded directly
 
 // Named barriers over the compute warps only (the producer may be waiting
 // for room in the copy queue).
@@ -196,6 +200,21 @@ __device__ __forceinline__ uint2 load_codes(const uint32_t* row, int q) {
   return make_uint2(row[q], 0u);
 }
 
+// The same code words read straight from global memory into registers (the
+// 3-bit high-bit word unshifted: codes_fix shifts it where it is used, so the
+// load is not waited for where it is issued).
+template <int kBits>
+__device__ __forceinline__ uint2 ldg_codes(const uint32_t* row, int q) {
+  if constexpr (kBits == 4) return ldg_stream_v2(row + 2 * q);
+  if constexpr (kBits == 3) return make_uint2(ldg_stream_u32(row + q), ldg_stream_u32(row + 4 + (q >> 1)));
+  return make_uint2(ldg_stream_u32(row + q), 0u);
+}
+template <int kBits>
+__device__ __forceinline__ uint2 codes_fix(uint2 w, int q) {
+  if constexpr (kBits == 3) w.y >>= 8 * (q & 1);
+  return w;
+}
+
 // The activation operand: 16 consecutive 16-bit values at p (zero when the
 // lane's token does not exist).
 __device__ __forceinline__ void load_b(const uint16_t* p, bool valid, uint32_t (&b)[8]) {
@@ -300,7 +319,12 @@ __device__ __forceinline__ void write_routing_outputs(const DecodeArgs& a, const
 __device__ long long g_dec_wait_limit = kWaitLimitCycles;
 __device__ int g_dec_drop_cta = -1;
 
-template <int kT, int kBits>
+// kReg: every CTA has at most one phase-1 item and d <= 64 * 8 * kRegChunks;
+// the item's gate/up codes go from global memory straight into the MMA
+// fragment registers of the warps that use them, loaded as soon as the
+// item's expert is known (before the wait for the previous kernel for the
+// shared expert), instead of through the phase-1 stage ring.
+template <int kT, int kBits, bool kReg>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps mr, const __grid_constant__ DecodeMaps ms, const DecodeArgs a,
                   WsHeader* hdr) {
@@ -344,12 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_x = empty2 + kS2Max;
   uint64_t* bar_w = bar_x + 1;   // the routing weights are in wt
   uint64_t* bar_h0 = bar_w + 1;  // the h records of the first min(S2, jobs) phase-2 jobs have landed
+  uint64_t* bar_p1 = bar_h0 + 1;  // register path: every compute warp has used its phase-1 codes
   uint8_t* hring = smem + L.hring;
   float* s_v = reinterpret_cast<float*>(smem + L.rid + 3ull * kT * kMaxK * 4);
   double* s_ex = reinterpret_cast<double*>(smem + round_up(L.rid + 4ull * kT * kMaxK * 4, 8));
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kBars; ++i) mbar_init(&full1[i], 1);
+    for (int i = 0; i < kBars; ++i) mbar_init(&full1[i], i == kBars - 1 ? kWarps : 1);
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < kS1 + kS2Max; i += kThreads) cnt1[i] = 0;
@@ -467,16 +492,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  // Register path: the item's group parameters (both matrices) by TMA into
+  // the first parameter buffer, on the first stage's barrier (one lane).
+  auto issue_params = [&](int slot, int rb) {
+    const bool sh = has_shared && slot == 0;
+    const int e = sh ? 0 : slot_e[slot];
+    const DecodeMaps& m = sh ? ms : mr;
+    const uint32_t sbb = static_cast<uint32_t>(L.G1) * kRows1 * 4;
+    mbar_arrive_expect_tx(&full1[0], 2 * sbb);
+    tma_load_3d(smem + L.sbuf1, &m.sb_gate, &full1[0], rb * kRows1, 0, e);
+    tma_load_3d(smem + L.sbuf1 + sbb, &m.sb_up, &full1[0], rb * kRows1, 0, e);
+  };
+  // Register path: compute warp (matrix p1_mat, group p1_gl of each chunk)
+  // loads the code words its MMA fragments take, rows g8, g8 + 8, g8 + 16 and
+  // g8 + 24 of the item's 32 (codes [E][d/64][N][wpg], N = I or I_shared).
+  const int p1_mat = warp >> 3, p1_gl = warp & 7;
+  uint2 cw[kRegChunks][4];
+  auto load_item_codes = [&](int slot, int rb) {
+    const bool sh = has_shared && slot == 0;
+    const int e = sh ? 0 : slot_e[slot];
+    const int N = sh ? a.I_shared : a.I;
+    const uint32_t* base = p1_mat == 0 ? (sh ? a.qg_s : a.qg_r) : (sh ? a.qu_s : a.qu_r);
+    base += static_cast<size_t>(e) * L.G1 * N * kW;
+#pragma unroll
+    for (int ch = 0; ch < kRegChunks; ++ch) {
+      const int gi = ch * kChunk + p1_gl;
+      if (ch < L.nchunk && gi < L.G1) {
+        const uint32_t* row = base + (static_cast<size_t>(gi) * N + rb * kRows1 + g8) * kW;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) cw[ch][r] = ldg_codes<kBits>(row + ((r >> 1) * 16 + (r & 1) * 8) * kW, q4);
+      } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) cw[ch][r] = make_uint2(0u, 0u);
+      }
+    }
+  };
+
   // The shared expert's loads need no routing and do not depend on the
   // previous kernels: issue them first (the CTA's items come in index order,
   // the shared expert's first).  Tensor maps, router logits and X are only
   // pulled towards the SM (an L2 prefetch of a line the previous kernel still
   // writes is harmless: L2 is where writes land).
   const int my_sh_items = cta < it_s ? div_up(it_s - cta, nC) : 0;
-  const int pre1 = min(kS1, my_sh_items * L.nchunk);
+  const int pre1 = kReg ? 0 : min(kS1, my_sh_items * L.nchunk);
   const int pre2 = has_shared && my_rbs > 0 ? 1 : 0;
   if (warp == kProducer) {
-    issue1_warp(0, pre1);
+    if (kReg) {
+      if (my_sh_items > 0 && lane == 0) issue_params(0, cta);
+    } else {
+      issue1_warp(0, pre1);
+    }
     if (pre2) issue2c_warp(0, 1, 1);
     if (lane == 1) {
       tma_prefetch_desc(&mr.q_gate);
@@ -503,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int off = lane * 128; off < kT * a.E * 4; off += 32 * 128) touch_l2(lg + off);
     for (int off = lane * 128; off < kT * d * 2; off += 32 * 128) touch_l2(xp + off);
   }
+  if (kReg && warp < kWarps && my_sh_items > 0) load_item_codes(0, cta);  // a shared-expert item: rows 32 cta ..
   pdl_wait();  // X, the routing and the previous layer's use of the workspace
   // Call g of this workspace counts barrier arrivals in dec_count[g % 2]; read
   // before the CTA's first barrier so it precedes every arrival of the call.
@@ -602,6 +668,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_items = cta < NI ? div_up(NI - cta, nC) : 0;
   const int total1 = my_items * L.nchunk;
   const int total2 = my_rbs * nsl;
+  if (kReg) {
+    if (NI > nC && cta == 0 && threadIdx.x == 0) record_status(a.status, MOE_ERR_UNSUPPORTED);  // never: the host checks
+    if (warp < kWarps && my_sh_items == 0 && my_items > 0) {  // a routed item
+      int slot, rb;
+      item_slot(cta, slot, rb);
+      load_item_codes(slot, rb);
+    }
+  }
 
   if (warp == kProducer) {
     // -------------------------------------------------------- producer
@@ -610,7 +684,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // it), the down rows, then, after the barrier over the grid, the h
     // records.  Issuing a copy waits while the SM's copy queue is full, so no
     // compute warp issues any.
-    issue1_warp(pre1, min(kS1, total1) - pre1);
+    if (kReg) {
+      if (my_sh_items == 0 && my_items > 0 && lane == 0) {
+        int slot, rb;
+        item_slot(cta, slot, rb);
+        issue_params(slot, rb);
+      }
+    } else {
+      issue1_warp(pre1, min(kS1, total1) - pre1);
+    }
     // The routing weights (fp64, slow on this GPU), while the copies stream:
     // softmax over each token's selected logits, summed in selection order and
     // rounded once (the routing kernel's arithmetic, so the same bits).
@@ -627,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_w);  // releases the weights to the compute warps
-    if (lane == 0) {
+    if (!kReg && lane == 0) {
       for (int j = kS1; j < total1; ++j) {
         ok &= mbar_wait(&empty1[j % kS1], static_cast<uint32_t>(j / kS1 - 1) & 1u, nullptr);
         issue1(j);
@@ -637,8 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bytes, on the path to the barrier over the grid, take the memory
     // bandwidth first; the down rows are needed only after that barrier.
     __syncwarp();
-    if (total1 > 0)
+    if (kReg) {
+      if (my_items > 0) ok &= mbar_wait(bar_p1, 0, nullptr);
+    } else if (total1 > 0) {
       ok &= mbar_wait(&full1[(total1 - 1) % kS1], static_cast<uint32_t>((total1 - 1) / kS1) & 1u, nullptr);
+    }
     for (int j0 = pre2, n2 = min(L.S2, total2); j0 < n2; j0 += 16) issue2c_warp(j0, min(16, n2 - j0), nsl);
     if (lane == 0) {
       // the barrier: every CTA has written its h records.  CTA 0 then clears
@@ -709,7 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ phase 1: h of this CTA's items
     const int mat = warp >> 3;  // 0: gate, 1: up
     const int gl = warp & 7;    // group inside a stage
-    for (int il = 0; il < my_items; ++il) {
+    const int n_items = kReg ? min(my_items, 1) : my_items;
+    for (int il = 0; il < n_items; ++il) {
       int slot, rb;
       item_slot(cta + il * nC, slot, rb);
       const uint32_t* sbi =
@@ -718,42 +804,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[2][4];  // [tile][fragment]
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.0f;
-      for (int ch = 0; ch < L.nchunk; ++ch) {
-        const int j = il * L.nchunk + ch, stage = j % kS1;
-        ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
-        const int gi = ch * kChunk + gl;  // this warp's group
-        if (gi < L.G1) {
-          const uint32_t* qm =
-              reinterpret_cast<const uint32_t*>(ring1 + static_cast<size_t>(stage) * kSt1<kBits> + mat * kCodeQ<kBits>) +
-              gl * kRows1 * kW;
-          const uint32_t* sbm = sbi + gi * kRows1;
-          uint32_t b[8];
-          load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
-          const float sxa = 2 * q4 < kT ? sx[(2 * q4) * L.G1 + gi] : 0.0f;
-          const float sxb = 2 * q4 + 1 < kT ? sx[(2 * q4 + 1) * L.G1 + gi] : 0.0f;
-          float dd[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+      // group gi of the item: the MMAs of both 16-row tiles (codes of rows
+      // g8, g8 + 8, g8 + 16, g8 + 24 in w4), then the group's affine map
+      auto group1 = [&](int gi, const uint2 (&w4)[4]) {
+        const uint32_t* sbm = sbi + gi * kRows1;
+        uint32_t b[8];
+        load_b(xs + static_cast<size_t>(g8) * d + gi * 64 + 16 * q4, g8 < kT, b);
+        const float sxa = 2 * q4 < kT ? sx[(2 * q4) * L.G1 + gi] : 0.0f;
+        const float sxb = 2 * q4 + 1 < kT ? sx[(2 * q4 + 1) * L.G1 + gi] : 0.0f;
+        float dd[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-          for (int tile = 0; tile < 2; ++tile) {
-            const int r0 = tile * 16 + g8;
-            const uint2 wa = load_codes<kBits>(qm + r0 * kW, q4);
-            const uint2 wb = load_codes<kBits>(qm + (r0 + 8) * kW, q4);
-            mma_group<true, kBits>(wa, wb, b, dd[tile]);
-          }
+        for (int tile = 0; tile < 2; ++tile) mma_group<true, kBits>(w4[2 * tile], w4[2 * tile + 1], b, dd[tile]);
 #pragma unroll
-          for (int tile = 0; tile < 2; ++tile) {
-            const int r0 = tile * 16 + g8;
-            const uint32_t p0 = sbm[r0], p1 = sbm[r0 + 8];
-            const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 128.0f * s0;
-            const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 128.0f * s1;
-            acc[tile][0] += fmaf(s0, dd[tile][0], c0 * sxa);
-            acc[tile][1] += fmaf(s0, dd[tile][1], c0 * sxb);
-            acc[tile][2] += fmaf(s1, dd[tile][2], c1 * sxa);
-            acc[tile][3] += fmaf(s1, dd[tile][3], c1 * sxb);
+        for (int tile = 0; tile < 2; ++tile) {
+          const int r0 = tile * 16 + g8;
+          const uint32_t p0 = sbm[r0], p1 = sbm[r0 + 8];
+          const float s0 = bf16_lo(p0), c0 = bf16_hi(p0) - 128.0f * s0;
+          const float s1 = bf16_lo(p1), c1 = bf16_hi(p1) - 128.0f * s1;
+          acc[tile][0] += fmaf(s0, dd[tile][0], c0 * sxa);
+          acc[tile][1] += fmaf(s0, dd[tile][1], c0 * sxb);
+          acc[tile][2] += fmaf(s1, dd[tile][2], c1 * sxa);
+          acc[tile][3] += fmaf(s1, dd[tile][3], c1 * sxb);
+        }
+      };
+      if constexpr (kReg) {
+        ok &= mbar_wait(&full1[0], 0, nullptr);  // the item's group parameters
+#pragma unroll
+        for (int ch = 0; ch < kRegChunks; ++ch) {
+          const int gi = ch * kChunk + gl;
+          if (ch < L.nchunk && gi < L.G1) {
+            uint2 w4[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) w4[r] = codes_fix<kBits>(cw[ch][r], q4);
+            group1(gi, w4);
           }
         }
-        // the last warp done with a stage releases it to the producer
+        // the codes have landed and been used: the producer may request the down rows
         __syncwarp();
-        if (lane == 0 && (atomicAdd(&cnt1[stage], 1) + 1) % kWarps == 0) mbar_arrive(&empty1[stage]);
+        if (lane == 0) mbar_arrive(bar_p1);
+      } else {
+        for (int ch = 0; ch < L.nchunk; ++ch) {
+          const int j = il * L.nchunk + ch, stage = j % kS1;
+          ok &= mbar_wait(&full1[stage], static_cast<uint32_t>(j / kS1) & 1u, nullptr);
+          const int gi = ch * kChunk + gl;  // this warp's group
+          if (gi < L.G1) {
+            const uint32_t* qm = reinterpret_cast<const uint32_t*>(ring1 + static_cast<size_t>(stage) * kSt1<kBits> +
+                                                                   mat * kCodeQ<kBits>) +
+                                 gl * kRows1 * kW;
+            uint2 w4[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) w4[r] = load_codes<kBits>(qm + ((r >> 1) * 16 + (r & 1) * 8 + g8) * kW, q4);
+            group1(gi, w4);
+          }
+          // the last warp done with a stage releases it to the producer
+          __syncwarp();
+          if (lane == 0 && (atomicAdd(&cnt1[stage], 1) + 1) % kWarps == 0) mbar_arrive(&empty1[stage]);
+        }
       }
       // h of the item's 32 features for every token
 #pragma unroll
@@ -944,21 +1050,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // CTAs of this kernel that can be resident at once on the current device (0
 // on error).  The barrier over the grid needs every CTA resident together.
-template <int kT, int kBits>
+template <int kT, int kBits, bool kReg>
 int max_ctas(size_t smem, int num_sms) {
-  const void* f = reinterpret_cast<const void*>(decode_kernel<kT, kBits>);
+  const void* f = reinterpret_cast<const void*>(decode_kernel<kT, kBits, kReg>);
   if (set_max_dynamic_smem(f, static_cast<int>(kSmemMax)) != cudaSuccess) return 0;
   int per_sm = 0;
   if (occupancy_per_sm(f, kThreads, smem, &per_sm) != cudaSuccess) return 0;
   return per_sm * num_sms;
 }
 
-template <int kT, int kBits>
-cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
+template <int kT, int kBits, bool kReg>
+cudaError_t launch_k(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int grid,
                      size_t smem, cudaStream_t stream, bool pdl) {
-  const int resident = max_ctas<kT, kBits>(smem, a.num_sms);
-  if (resident < 1) return cudaErrorInvalidConfiguration;
-  const int grid = want < resident ? want : resident;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
@@ -969,7 +1072,29 @@ cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const Decode
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kT, kBits>, *routed, *sh, a, hdr);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kT, kBits, kReg>, *routed, *sh, a, hdr);
+}
+
+// items: phase-1 items of the call at most.  One token whose items fit the
+// grid (one per CTA) and d <= 2048 takes the register-load variant unless
+// MOE_DECODE_REG=0.
+template <int kT, int kBits>
+cudaError_t launch_t(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
+                     size_t smem, cudaStream_t stream, bool pdl, int items) {
+  if constexpr (kT == 1) {
+    const char* env = std::getenv("MOE_DECODE_REG");
+    const bool allow = !(env && env[0] == '0');
+    if (allow && a.d <= 64 * kDecodeChunkGroups * kRegChunks) {
+      const int resident = max_ctas<1, kBits, true>(smem, a.num_sms);
+      if (resident < 1) return cudaErrorInvalidConfiguration;
+      const int grid = want < resident ? want : resident;
+      if (items <= grid) return launch_k<1, kBits, true>(a, routed, sh, hdr, grid, smem, stream, pdl);
+    }
+  }
+  const int resident = max_ctas<kT, kBits, false>(smem, a.num_sms);
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const int grid = want < resident ? want : resident;
+  return launch_k<kT, kBits, false>(a, routed, sh, hdr, grid, smem, stream, pdl);
 }
 
 }  // namespace
@@ -991,12 +1116,12 @@ size_t decode_scratch_bytes(int T, int I, int I_shared) {
 
 template <int kBits>
 cudaError_t launch_bits(const DecodeArgs& a, const DecodeMaps* routed, const DecodeMaps* sh, WsHeader* hdr, int want,
-                        size_t smem, cudaStream_t stream, bool pdl) {
+                        size_t smem, cudaStream_t stream, bool pdl, int items) {
   switch (a.T) {
-    case 1: return launch_t<1, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
-    case 2: return launch_t<2, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
-    case 3: return launch_t<3, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
-    default: return launch_t<4, kBits>(a, routed, sh, hdr, want, smem, stream, pdl);
+    case 1: return launch_t<1, kBits>(a, routed, sh, hdr, want, smem, stream, pdl, items);
+    case 2: return launch_t<2, kBits>(a, routed, sh, hdr, want, smem, stream, pdl, items);
+    case 3: return launch_t<3, kBits>(a, routed, sh, hdr, want, smem, stream, pdl, items);
+    default: return launch_t<4, kBits>(a, routed, sh, hdr, want, smem, stream, pdl, items);
   }
 }
 
@@ -1017,11 +1142,11 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeMaps* routed, const D
   timer_begin(kKDecode, stream);
   cudaError_t err;
   if (a.bits == 2)
-    err = launch_bits<2>(a, routed, sh, hdr, want, L.total, stream, pdl);
+    err = launch_bits<2>(a, routed, sh, hdr, want, L.total, stream, pdl, items);
   else if (a.bits == 3)
-    err = launch_bits<3>(a, routed, sh, hdr, want, L.total, stream, pdl);
+    err = launch_bits<3>(a, routed, sh, hdr, want, L.total, stream, pdl, items);
   else
-    err = launch_bits<4>(a, routed, sh, hdr, want, L.total, stream, pdl);
+    err = launch_bits<4>(a, routed, sh, hdr, want, L.total, stream, pdl, items);
   timer_end(kKDecode, stream);
   return err;
 }

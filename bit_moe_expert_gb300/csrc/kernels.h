@@ -99,6 +99,9 @@ struct DecodeArgs {
   int block_rows;         // tile height of the block map it writes
   uint16_t* Y;            // [T][d] bf16
   uint8_t* hbuf;          // h records of the call's slots, decode_scratch_bytes, 16-byte aligned
+  // gate and up codes of the routed experts and of the shared expert (the prepacked [E][d/64][I][wpg] arrays),
+  // read directly into registers when every CTA has at most one phase-1 item
+  const uint32_t *qg_r, *qu_r, *qg_s, *qu_s;
   uint32_t* status;
   int T, d, I, k, I_shared, E, num_sms;
   int bits;  // bits per weight code: 4 or 2
