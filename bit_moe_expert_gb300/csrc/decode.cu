@@ -17,10 +17,13 @@
 //            down projection of every active expert restricted to those rows,
 //            times that expert's h and the token's routing weight, summed over
 //            the experts, gives Y directly; nothing is reduced across CTAs.
-// Every weight byte is loaded once by TMA into a ring of shared-memory stages
-// (phase 1: chunks of 8 groups of 64 columns; phase 2: 16 rows of one expert),
-// issued as soon as the routing is known (the shared expert's before the wait
-// for the previous kernel); the phase-2 down rows load while phase 1 runs.
+// Every weight byte is loaded once, as soon as the routing is known (the
+// shared expert's before the wait for the previous kernel).  One token (each
+// CTA at most one item): the gate/up codes go straight from global memory
+// into the MMA fragment registers of the warps that use them.  Otherwise TMA
+// loads them into a ring of shared-memory stages (chunks of 8 groups of 64
+// columns).  The phase-2 down rows (16 rows of one expert) come by TMA into a
+// ring of their own and load while phase 1 runs.
 //
 // Arithmetic on the tensor cores (mma.sync m16n8k16, fp32 accumulators):
 // weight rows are the 16 rows of the MMA, tokens its 8 columns (T <= 4 used).
