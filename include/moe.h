@@ -264,7 +264,9 @@ size_t moe_forward_workspace_bytes(int T, int d, int I, int E, int k, int I_shar
  * Path: T <= 4 runs the decode kernel (every active expert's bytes streamed
  * once, one launch; warp-level tensor-core MMAs fed from the 4-bit codes, the
  * gate/up projections in bf16 with x exact, h rounded to fp16 for the down
- * projection); larger T runs the grouped tensor-core GEMM (tcgen05,
+ * projection; with one token and d <= 2048 the gate/up codes are loaded
+ * straight into registers, MOE_DECODE_REG=0 keeps them on the shared-memory
+ * stage ring the other token counts use, with the same result bits); larger T runs the grouped tensor-core GEMM (tcgen05,
  * dequantisation fused, SwiGLU fused into the gate/up epilogue; the down
  * projection writes each expert's output rows in fp32 and a separate combine
  * kernel sums each token's rows with its routing weights and the shared
