@@ -78,6 +78,8 @@ SMALL = [
     # a shared expert wider than the routed ones
     ("wide_shared", dict(T=1, d=2048, E=8, k=2, I=64, I_shared=256)),
     ("k1_E1", dict(T=1, d=512, E=1, k=1, I=128, I_shared=64)),
+    # the largest k: 2 + 32 x 2 items, still one per CTA
+    ("k32", dict(T=1, d=512, E=64, k=32, I=64, I_shared=64)),
 ]
 
 
