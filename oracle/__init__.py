@@ -1,4 +1,4 @@
-"""ctypes wrapper over the C oracle (oracle/moe_oracle.c).
+"""ctypes wrapper over the C++ oracle (oracle/moe_oracle.cpp).
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, by __graft_entry__.smoke() and by
 bench.py's CPU-baseline leg.  The product package never imports it.

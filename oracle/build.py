@@ -1,4 +1,4 @@
-"""Compile the C oracle into oracle/_build/libmoe_oracle.so (plain gcc, no GPU).
+"""Compile the C++ oracle into oracle/_build/libmoe_oracle.so (plain g++, no GPU).
 
 -ffp-contract=off keeps every fp64 operation a separately rounded IEEE
 operation on both x86 and Arm (no fused multiply-add contraction).
@@ -12,7 +12,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_oracle.so")
-SRC = [os.path.join(HERE, "moe_oracle.c")]
+SRC = [os.path.join(HERE, "moe_oracle.cpp")]
 
 
 def up_to_date() -> bool:
@@ -27,7 +27,7 @@ def build(force: bool = False) -> str:
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
            "-o", tmp] + SRC + ["-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)

@@ -5,8 +5,9 @@
  * benchmark's CPU-baseline leg may load this library.  The product path (the
  * CUDA library) never calls it and shares no code with it.
  *
- * Plain, single-threaded C with fp64 arithmetic.  Each function states the
- * passage of the source pages it follows:
+ * Plain, single-threaded C++ (C-style, exported with C linkage) with fp64
+ * arithmetic.  Each function states the passage of the source pages it
+ * follows:
  *   [Lily-news]  "Perplexity builds a custom engine for Qwen on M5 Macs"
  *   [Lily-blog]  "Perplexity's Lily Beats MLX-LM on MacBook M5. Because It Only
  *                Runs One Model." (sections named in each comment)
